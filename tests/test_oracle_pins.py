@@ -1,0 +1,417 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix (no GPU).
+
+Each ``pin_*`` function checks one fact through the public functions of
+``oracle.attn``; the ``test_planted_*`` tests replace one oracle step by a
+plausible mistake (on the CPU, in the oracle) and show that some pin fails.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import attn_workloads as W
+from oracle import attn as OA
+from oracle import naive as ON
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _facts():
+    with open(os.path.join(GOLDEN, "page_facts.json")) as f:
+        return json.load(f)
+
+
+def _rand(shape, seed, mult=1.0):
+    g = np.random.default_rng(seed)
+    return g.standard_normal(shape) * mult
+
+
+def _to_list(x):
+    return np.asarray(x, dtype=np.float64).tolist()
+
+
+# --------------------------------------------------------------------------- pins
+
+def pin_softmax_page_example(o):
+    f = _facts()["softmax_example"]
+    p = o.softmax_rows(np.array([f["input"]]))[0]
+    assert np.allclose(p, f["printed"], atol=0.5 * 10 ** (-f["printed_decimals"]))
+    e = math.e
+    exact = [e * e / (e * e + e + 1), e / (e * e + e + 1), 1 / (e * e + e + 1)]
+    assert np.allclose(p, exact, rtol=0, atol=1e-15)
+
+
+def pin_rows_sum_to_one(o):
+    q = _rand((1, 3, 37, 8), 1)
+    k = _rand((1, 3, 37, 8), 2)
+    s = o.attention_scores(q[0], k[0], 0.3) + o.causal_additive_mask(37, 37)
+    p = o.softmax_rows(s)
+    assert np.all(np.abs(p.sum(-1) - 1.0) < 1e-12)
+    assert np.all(p >= 0)
+
+
+def pin_masked_weight_exactly_zero(o):
+    q = _rand((23, 8), 3)
+    k = _rand((23, 8), 4)
+    s = o.attention_scores(q, k, 0.5) + o.causal_additive_mask(23, 23)
+    p = o.softmax_rows(s)
+    iu = np.triu_indices(23, 1)
+    assert np.all(p[iu] == 0.0)
+    assert np.all(p[np.tril_indices(23)] > 0.0)
+
+
+def pin_mask_variants_differ(o):
+    q = _rand((1, 1, 12, 8), 5)
+    k = _rand((1, 1, 12, 8), 6)
+    v = _rand((1, 1, 12, 8), 7)
+    ref = o.attention(q, k, v, causal=True)
+    s = o.attention_scores(q[0, 0], k[0, 0], 1 / math.sqrt(8))
+    zero_mask = o.softmax_rows(s + np.where(np.triu(np.ones((12, 12)), 1) > 0, 0.0, 0.0)) @ v[0, 0]
+    p_full = o.softmax_rows(s)
+    p_after = np.where(np.triu(np.ones((12, 12)), 1) > 0, 0.0, p_full)
+    after = p_after @ v[0, 0]
+    assert np.max(np.abs(zero_mask - ref[0, 0])) > 1e-3
+    assert np.max(np.abs(after - ref[0, 0])) > 1e-3
+    assert np.all(p_after.sum(-1)[:-1] < 1.0 - 1e-6)
+
+
+def pin_gqa_equals_mha_repeated(o):
+    for rep in (1, 2, 4):
+        Hkv = 2
+        q = _rand((2, Hkv * rep, 19, 16), 10 + rep)
+        k = _rand((2, Hkv, 19, 16), 20 + rep)
+        v = _rand((2, Hkv, 19, 16), 30 + rep)
+        a = o.attention(q, k, v, causal=True, rope_base=10000.0)
+        kr = np.repeat(k, rep, axis=1)
+        vr = np.repeat(v, rep, axis=1)
+        b = o.attention(q, kr, vr, causal=True, rope_base=10000.0)
+        assert np.array_equal(a, b)
+        # and head h of the grouped result equals a single-head run on KV head h // rep
+        for h in range(Hkv * rep):
+            c = o.attention(q[:, h:h + 1], k[:, h // rep:h // rep + 1], v[:, h // rep:h // rep + 1],
+                            causal=True, rope_base=10000.0)
+            assert np.array_equal(a[:, h:h + 1], c)
+
+
+def pin_basis_invariance(o):
+    q = _rand((17, 8), 40)
+    k = _rand((21, 8), 41)
+    rng = np.random.default_rng(42)
+    while True:
+        R = rng.standard_normal((8, 8))
+        if np.linalg.cond(R) < 10:
+            break
+    s0 = o.attention_scores(q, k, 0.25)
+    s1 = o.attention_scores(q @ R, k @ np.linalg.inv(R).T, 0.25)
+    assert np.max(np.abs(s1 - s0)) <= 1e-10 * max(1.0, np.max(np.abs(s0)))
+
+
+def pin_qq_symmetric(o):
+    q = _rand((15, 8), 43)
+    s = o.attention_scores(q, q, 1.0)
+    assert np.array_equal(s, s.T)
+
+
+def pin_rope_relative(o):
+    d = 16
+    qv = _rand((1, d), 50)
+    kv = _rand((1, d), 51)
+    for layout in ("split_half", "adjacent"):
+        def score(m, n):
+            qm = o.rope_rotate(qv, [m], 10000.0, layout)
+            kn = o.rope_rotate(kv, [n], 10000.0, layout)
+            return float(o.attention_scores(qm, kn, 1.0)[0, 0])
+        a, b, c = score(5, 2), score(20, 17), score(20, 10)
+        assert abs(a - b) < 1e-12
+        assert abs(a - c) > 1e-3
+
+
+def pin_rope_orthogonal(o):
+    x = _rand((9, 32), 52)
+    pos = np.arange(9) * 37
+    for layout in ("split_half", "adjacent"):
+        y = o.rope_rotate(x, pos, 500000.0, layout)
+        assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-14)
+        y0 = o.rope_rotate(x[:1], [0], 10000.0, layout)
+        assert np.array_equal(y0, x[:1])
+
+
+def pin_rope_layouts_permute(o):
+    d = 16
+    x = _rand((7, d), 53)
+    perm = np.empty(d, dtype=int)  # adjacent position of each split-half channel
+    perm[: d // 2] = np.arange(0, d, 2)
+    perm[d // 2:] = np.arange(1, d, 2)
+    xa = np.empty_like(x)
+    xa[:, perm] = x
+    ys = o.rope_rotate(x, np.arange(7) * 3, 10000.0, "split_half")
+    ya = o.rope_rotate(xa, np.arange(7) * 3, 10000.0, "adjacent")
+    assert np.allclose(ya[:, perm], ys, rtol=0, atol=1e-14)
+
+
+def pin_rope_angle_formula(o):
+    # theta_i = base^(-2i/d): pair 0 turns by exactly pos radians, pair i by pos*base^(-2i/d)
+    d = 8
+    x = np.zeros((1, d))
+    x[0, 0] = 1.0
+    y = o.rope_rotate(x, [3], 10000.0, "split_half")
+    assert abs(y[0, 0] - math.cos(3.0)) < 1e-15 and abs(y[0, d // 2] - math.sin(3.0)) < 1e-15
+    x = np.zeros((1, d))
+    x[0, 2] = 1.0
+    y = o.rope_rotate(x, [7], 10000.0, "split_half")
+    ang = 7 * 10000.0 ** (-4.0 / d)
+    assert abs(y[0, 2] - math.cos(ang)) < 1e-15 and abs(y[0, 2 + d // 2] - math.sin(ang)) < 1e-15
+
+
+def pin_naive_agreement(o):
+    cases = [
+        dict(B=1, Hkv=2, rep=1, T=9, d=4, causal=True, base=10000.0, layout="split_half"),
+        dict(B=2, Hkv=1, rep=2, T=7, d=16, causal=True, base=10000.0, layout="adjacent"),
+        dict(B=1, Hkv=2, rep=4, T=16, d=4, causal=False, base=0.0, layout="split_half"),
+        dict(B=1, Hkv=1, rep=4, T=11, d=16, causal=True, base=500000.0, layout="split_half"),
+        dict(B=1, Hkv=2, rep=2, T=13, d=4, causal=False, base=10000.0, layout="adjacent"),
+    ]
+    for i, c in enumerate(cases):
+        Hq = c["Hkv"] * c["rep"]
+        q = _rand((c["B"], Hq, c["T"], c["d"]), 60 + i, 2.0)
+        k = _rand((c["B"], c["Hkv"], c["T"], c["d"]), 70 + i, 2.0)
+        v = _rand((c["B"], c["Hkv"], c["T"], c["d"]), 80 + i)
+        for rnd in (False, True):
+            a = o.attention(q, k, v, causal=c["causal"], rope_base=c["base"], scale=0.37,
+                            rope_layout=c["layout"], operand_dtype="bf16" if rnd else None)
+            b = np.array(ON.naive_attention(_to_list(q), _to_list(k), _to_list(v), c["causal"],
+                                            c["base"], 0.37, c["layout"], round_bf16=rnd))
+            assert np.max(np.abs(a - b)) < 1e-12, (i, rnd, np.max(np.abs(a - b)))
+
+
+def pin_degenerate_cases(o):
+    q = _rand((1, 2, 1, 8), 90)
+    k = _rand((1, 2, 1, 8), 91)
+    v = _rand((1, 2, 1, 8), 92)
+    assert np.array_equal(o.attention(q, k, v, causal=False), v)
+    q = _rand((1, 2, 6, 8), 93)
+    k = _rand((1, 2, 6, 8), 94)
+    v = _rand((1, 2, 6, 8), 95)
+    out = o.attention(q, k, v, causal=True, rope_base=10000.0)
+    assert np.array_equal(out[:, :, 0], v[:, :, 0])
+
+
+def pin_decode_equals_prefill_last_row(o):
+    B, Hkv, rep, d = 3, 2, 2, 16
+    T = 29
+    q = _rand((B, Hkv * rep, T, d), 100)
+    k = _rand((B, Hkv, T, d), 101)
+    v = _rand((B, Hkv, T, d), 102)
+    full = o.attention(q, k, v, causal=True, rope_base=10000.0)
+    qr = o.rope_rotate(q, np.arange(T), 10000.0)
+    kr = o.rope_rotate(k, np.arange(T), 10000.0)
+    lens = [T, 17, 1]
+    Lmax = T + 3
+    kc = np.full((B, Hkv, Lmax, d), np.nan)
+    vc = np.full((B, Hkv, Lmax, d), np.nan)
+    qd = np.empty((B, Hkv * rep, 1, d))
+    for b, L in enumerate(lens):
+        kc[b, :, :L] = kr[b, :, :L]
+        vc[b, :, :L] = v[b, :, :L]
+        qd[b, :, 0] = qr[b, :, L - 1]
+    dec = o.decode(qd, kc, vc, lens)
+    assert not np.any(np.isnan(dec))
+    for b, L in enumerate(lens):
+        ref = o.attention(q[b:b + 1, :, :L], k[b:b + 1, :, :L], v[b:b + 1, :, :L],
+                          causal=True, rope_base=10000.0)
+        assert np.max(np.abs(dec[b, :, 0] - ref[0, :, L - 1])) < 1e-12
+    assert np.max(np.abs(dec[0, :, 0] - full[0, :, T - 1])) < 1e-12
+    nd = np.array(ON.naive_decode(_to_list(qd[:, :, 0]), np.nan_to_num(kc).tolist(),
+                                  np.nan_to_num(vc).tolist(), lens))
+    assert np.max(np.abs(nd - dec[:, :, 0])) < 1e-12
+
+
+def pin_merge_partials(o):
+    s = _rand((97,), 110, 3.0)
+    v = _rand((97, 8), 111)
+    ref = o.softmax_rows(s[None])[0] @ v
+    for bounds in ([0, 97], [0, 10, 97], [0, 32, 64, 96, 97], [0, 0, 50, 97, 97], [0, 1, 2, 97]):
+        ms, ls, os_ = o.split_partials(s, v, bounds)
+        out = o.merge_partials(ms, ls, os_)
+        assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def pin_bf16_rounding(o):
+    g = torch.Generator().manual_seed(5)
+    x32 = torch.randn(20000, generator=g) * torch.exp2(torch.randint(-20, 20, (20000,), generator=g).float())
+    x32 = torch.cat([x32, torch.tensor([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -8, 0.0, 2 ** -130,
+                                        3.0e38, 65504.0])])
+    ref = x32.to(torch.bfloat16).double().numpy()
+    got = o.round_to_bf16(x32.double().numpy())
+    assert np.array_equal(got, ref)
+    x64 = _rand((300,), 120, 10.0)
+    naive = np.array([ON.naive_round_bf16(float(t)) for t in x64])
+    assert np.array_equal(o.round_to_bf16(x64), naive)
+
+
+ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exactly_zero,
+            pin_mask_variants_differ, pin_gqa_equals_mha_repeated, pin_basis_invariance,
+            pin_qq_symmetric, pin_rope_relative, pin_rope_orthogonal, pin_rope_layouts_permute,
+            pin_rope_angle_formula, pin_naive_agreement, pin_degenerate_cases,
+            pin_decode_equals_prefill_last_row, pin_merge_partials, pin_bf16_rounding]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(OA)
+
+
+def test_score_variance_of_generator():
+    w = W.WORKLOADS["llama_gqa_bf16"].with_(B=1, Hq=4, Hkv=1, T=512)
+    q, k, _ = W.make_prefill_inputs(w)
+    qd = q.double().numpy()[0, 0]
+    kd = k.double().numpy()[0, 0]
+    s = qd @ kd.T
+    assert abs(np.var(s) / 128.0 - 1.0) < 0.05
+
+
+def test_oracle_golden_regression():
+    """Values written by tests/golden/make_oracle_golden.py (calls oracle/ only)."""
+    with open(os.path.join(GOLDEN, "oracle_tiny_f32.json")) as f:
+        g = json.load(f)
+    w = W.WORKLOADS["tiny_f32"]
+    q, k, v = W.make_prefill_inputs(w)
+    out = OA.attention(q, k, v, causal=True, rope_base=w.rope_base, scale=w.scale,
+                       operand_dtype="f32")
+    for (b, h, t, c), val in zip(g["index"], g["value"]):
+        assert abs(out[b, h, t, c] - val) < 1e-12
+
+
+# ----------------------------------------------------------------- planted mistakes
+
+class _Mutant:
+    """The oracle module with one function replaced."""
+
+    def __init__(self, **repl):
+        self.__dict__.update({n: getattr(OA, n) for n in OA.__all__})
+        self.__dict__.update(repl)
+        me = self
+
+        def attention(q, k, v, *, causal=True, rope_base=0.0, scale=None,
+                      rope_layout="split_half", operand_dtype=None):
+            q = np.asarray(q, np.float64)
+            k = np.asarray(k, np.float64)
+            v = np.asarray(v, np.float64)
+            B, Hq, T, d = q.shape
+            sc = 1 / math.sqrt(d) if (scale is None or scale <= 0) else scale
+            if rope_base > 0:
+                q = me.round_to(me.rope_rotate(q, np.arange(T), rope_base, rope_layout), operand_dtype)
+                k = me.round_to(me.rope_rotate(k, np.arange(T), rope_base, rope_layout), operand_dtype)
+                if "rope_on_v" in repl:
+                    v = me.rope_rotate(v, np.arange(T), rope_base, rope_layout)
+            kf, vf = me.expand_kv_heads(k, Hq), me.expand_kv_heads(v, Hq)
+            mask = me.causal_additive_mask(T, T) if causal else 0.0
+            out = np.empty_like(q)
+            for b in range(B):
+                for h in range(Hq):
+                    out[b, h] = me.softmax_rows(me.attention_scores(q[b, h], kf[b, h], sc) + mask) @ vf[b, h]
+            return out
+
+        if "attention" not in repl:
+            self.attention = attention
+
+
+def _fails(mutant, pins):
+    failed = []
+    for p in pins:
+        try:
+            p(mutant)
+        except AssertionError:
+            failed.append(p.__name__)
+    return failed
+
+
+def test_mutant_harness_is_faithful():
+    assert _fails(_Mutant(), [pin_naive_agreement, pin_gqa_equals_mha_repeated,
+                              pin_degenerate_cases, pin_rows_sum_to_one]) == []
+
+
+def test_planted_gqa_modulo_mapping():
+    def bad_expand(kv, n_q_heads):
+        kv = np.asarray(kv, np.float64)
+        return np.tile(kv, (1,) * (kv.ndim - 3) + (n_q_heads // kv.shape[-3], 1, 1))  # h % Hkv
+    assert _fails(_Mutant(expand_kv_heads=bad_expand), [pin_naive_agreement])
+
+
+def test_planted_softmax_wrong_axis():
+    def bad_softmax(z):
+        z = np.asarray(z, np.float64)
+        e = np.exp(z - np.max(z, axis=-2, keepdims=True))
+        return e / e.sum(axis=-2, keepdims=True)
+    assert _fails(_Mutant(softmax_rows=bad_softmax), [pin_rows_sum_to_one])
+
+
+def test_planted_mask_transposed():
+    def bad_mask(tq, tk, q_offset=0):
+        i = np.arange(tq)[:, None]
+        j = np.arange(tk)[None, :]
+        return np.where(j < i, -np.inf, 0.0)
+    assert _fails(_Mutant(causal_additive_mask=bad_mask),
+                  [pin_masked_weight_exactly_zero, pin_naive_agreement])
+
+
+def test_planted_rope_sign():
+    def bad_rope(x, positions, base, layout="split_half"):
+        x = np.asarray(x, np.float64)
+        d = x.shape[-1]
+        c, s = OA.rope_cos_sin(positions, d, base)
+        out = np.empty_like(x)
+        a, b = x[..., : d // 2], x[..., d // 2:]
+        out[..., : d // 2] = a * c + b * s
+        out[..., d // 2:] = a * s + b * c
+        return out
+    assert _fails(_Mutant(rope_rotate=bad_rope), [pin_rope_orthogonal, pin_rope_relative])
+
+
+def test_planted_rope_on_v():
+    assert _fails(_Mutant(rope_on_v=True), [pin_naive_agreement])
+
+
+def test_planted_dropped_scale():
+    def bad_scores(q, k, scale):
+        return np.asarray(q, np.float64) @ np.swapaxes(np.asarray(k, np.float64), -1, -2)
+    assert _fails(_Mutant(attention_scores=bad_scores), [pin_naive_agreement])
+
+
+def test_planted_rope_frequency_off_by_one():
+    def bad_freq(d, base):
+        i = np.arange(d // 2, dtype=np.float64)
+        return np.power(float(base), -(2.0 * (i + 1)) / float(d))
+
+    def bad_cs(positions, d, base):
+        ang = np.outer(np.asarray(positions, np.float64), bad_freq(d, base))
+        return np.cos(ang), np.sin(ang)
+
+    def bad_rope(x, positions, base, layout="split_half"):
+        x = np.asarray(x, np.float64)
+        d = x.shape[-1]
+        c, s = bad_cs(positions, d, base)
+        out = np.empty_like(x)
+        if layout == "split_half":
+            a, b = x[..., : d // 2], x[..., d // 2:]
+            out[..., : d // 2] = a * c - b * s
+            out[..., d // 2:] = a * s + b * c
+        else:
+            a, b = x[..., 0::2], x[..., 1::2]
+            out[..., 0::2] = a * c - b * s
+            out[..., 1::2] = a * s + b * c
+        return out
+    assert _fails(_Mutant(rope_rotate=bad_rope), [pin_rope_angle_formula, pin_naive_agreement])
+
+
+def test_planted_bf16_truncation():
+    def bad_round(x, dtype):
+        x = np.asarray(x, np.float64)
+        if dtype != "bf16":
+            return x
+        m, e = np.frexp(x)
+        return np.ldexp(np.trunc(np.ldexp(m, 8)), e - 8)
+    assert _fails(_Mutant(round_to=bad_round), [pin_naive_agreement])
