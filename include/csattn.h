@@ -1,0 +1,156 @@
+/*
+ * csattn -- causal multi-head scaled dot-product attention with RoPE and
+ * grouped-query KV heads, for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation, as the source pages state it:
+ *   Attn(Q,K,V;M) = softmax(Q K^T * scale + M) V, computed per head
+ *     ("Transformer" (ai-notes), section "Scaled dot-product attention";
+ *      "The Transformer architecture" (cooking-agi), same section, which also
+ *      fixes the default scale 1/sqrt(d_head) of each head);
+ *   M[t,s] = 0 for s <= t and -inf for s > t (causal)
+ *     ("Transformer" (ai-notes), section "What is the causal mask?";
+ *      "Transformer Math and Implementation Deep Dive", section "Causal Masking");
+ *   q [B, n_q_heads, T, d_head], k and v [B, n_kv_heads, T, d_head], with
+ *   n_q_heads a multiple of n_kv_heads and query head h reading KV head
+ *   h / (n_q_heads / n_kv_heads)
+ *     ("Transformer Math and Implementation Deep Dive", section "Attention Shapes");
+ *   RoPE on q and k only, pair p of channels turned by pos * base^(-2p/d)
+ *     ("The Transformer architecture", section "Now: RoPE" for the split-half
+ *      pairing; "Transformer" (ai-notes), section "RoPE (Rotary Positional
+ *      Embedding)" for the adjacent pairing and the angle formula);
+ *   KV-cache decode: the new query at position L-1 sees cached rows 0..L-1
+ *     ("The Transformer architecture", section "Hands-on").
+ *
+ * Conventions for every call:
+ *   - All tensors are dense, row-major, contiguous, in device memory, and
+ *     16-byte aligned (they are read by TMA).  The caller owns every buffer;
+ *     the library never allocates device memory of its own except one status
+ *     word per device (a static device variable).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and never synchronize.  Argument errors are detected on the host
+ *     before any launch and returned; nothing is launched then.
+ *   - Kernels never trap.  A wait that runs out of time (a hang) or a failed
+ *     device-side check raises a bit in the device status word;
+ *     csattn_check_status() reads and clears it.
+ *   - Return value: a csattn_status; csattn_last_error() gives a message for
+ *     the last failure on the calling thread.
+ */
+#ifndef CSATTN_H_
+#define CSATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSATTN_OK = 0,
+  CSATTN_ERR_INVALID_ARG = -1,  /* bad shape, pointer, alignment or value      */
+  CSATTN_ERR_UNSUPPORTED = -2,  /* valid but not implemented (d, dtype, group) */
+  CSATTN_ERR_CUDA = -3,         /* a CUDA runtime/driver call failed           */
+  CSATTN_ERR_TIMEOUT = -4,      /* a kernel wait ran out of time (status word) */
+  CSATTN_ERR_WORKSPACE = -5,    /* workspace missing or too small              */
+  CSATTN_ERR_DEVICE_ARG = -6    /* a device-side check failed (status word)    */
+} csattn_status;
+
+typedef enum { CSATTN_F32 = 0, CSATTN_BF16 = 1 } csattn_dtype;
+
+typedef enum { CSATTN_ROPE_SPLIT_HALF = 0, CSATTN_ROPE_ADJACENT = 1 } csattn_rope_layout;
+
+/*
+ * Bytes of device workspace csattn_attn_fwd needs for these arguments.
+ * Non-zero only for bf16 with RoPE (rope_base > 0): the rotated keys,
+ * B*Hkv*T*d bf16 values, which are computed once per call rather than once
+ * per query tile.  Returns 0 as well for arguments that csattn_attn_fwd
+ * would reject.
+ */
+size_t csattn_fwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,
+                                 float rope_base);
+
+/*
+ * Prefill forward: out = softmax(RoPE(q) RoPE(k)^T * scale + M) v.
+ *   q    [B, Hq,  T, d]   dtype `dtype` (CSATTN_BF16 or CSATTN_F32)
+ *   k, v [B, Hkv, T, d]   same dtype
+ *   out  [B, Hq,  T, d]   same dtype, written (rounded to nearest even)
+ *   causal       1: M is the causal mask; 0: no mask (M = 0).
+ *   rope_base    > 0: RoPE with theta_p = rope_base^(-2p/d) at positions
+ *                0..T-1 on q and k; <= 0: no RoPE.
+ *   rope_layout  CSATTN_ROPE_SPLIT_HALF (channel p with p + d/2) or
+ *                CSATTN_ROPE_ADJACENT (channel 2p with 2p+1).
+ *   scale        > 0: logit scale; <= 0: 1/sqrt(d).
+ *   lse          NULL, or fp32 [B, Hq, T]: natural-log log-sum-exp of each
+ *                scaled, masked score row.
+ *   workspace    device buffer of at least csattn_fwd_workspace_size() bytes
+ *                (may be NULL when that size is 0), owned by the caller.
+ * Requirements: B, Hq, Hkv, T >= 1; Hq % Hkv == 0; d in {64, 128} for bf16,
+ * d in {16, 32, 64, 128} for fp32; T < 2^24.  The rotated q and k are rounded
+ * to the input dtype before the dot products; accumulation is fp32.
+ */
+int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                    int Hkv, int T, int d, int dtype, int causal, float rope_base,
+                    int rope_layout, float scale, float* lse, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of device workspace csattn_attn_decode needs: fp32 partial results
+ * (running max, sum and un-normalised output) of every key split.
+ * num_splits = 0 means the automatic choice (the size then covers any
+ * max_seq_len <= Lmax); otherwise the explicit number of splits.
+ */
+size_t csattn_decode_workspace_size(int B, int Hq, int Lmax, int d, int num_splits);
+
+/*
+ * KV-cache decode: one new query per sequence.
+ *   q        [B, Hq, 1, d]     bf16, already rotated to position seq_lens[b]-1
+ *   k_cache  [B, Hkv, Lmax, d] bf16, keys already rotated (RoPE) at their positions
+ *   v_cache  [B, Hkv, Lmax, d] bf16
+ *   seq_lens device int32 [B]: valid rows of sequence b, 1 <= seq_lens[b] <= max_seq_len
+ *   out      [B, Hq, 1, d]     bf16
+ *   scale    > 0: logit scale; <= 0: 1/sqrt(d)
+ *   max_seq_len  host-side upper bound of seq_lens (<= Lmax); sizes the grid.
+ *   num_splits   0: automatic; > 0: split every sequence's keys into that many
+ *                parts (a testing and tuning knob; results agree to rounding).
+ *   workspace    >= csattn_decode_workspace_size(B, Hq, Lmax, d, num_splits) bytes.
+ * Rows at or beyond seq_lens[b] are never read.  A seq_lens[b] outside
+ * [1, max_seq_len] raises CSATTN_ERR_DEVICE_ARG in the status word (the
+ * sequence's output is then zero or partial).  Requirements: Hq % Hkv == 0,
+ * Hq / Hkv <= 16, d in {64, 128}.
+ */
+int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int Lmax,
+                       int d, int dtype, float scale, int max_seq_len, int num_splits,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronize `stream`, then read and clear this device's status word.
+ * Returns CSATTN_OK, CSATTN_ERR_TIMEOUT (a kernel wait ran out of time),
+ * CSATTN_ERR_DEVICE_ARG (a device-side argument check failed) or
+ * CSATTN_ERR_CUDA.
+ */
+int csattn_check_status(void* stream);
+
+/*
+ * Launch a one-block kernel whose wait on a barrier nothing will ever
+ * complete, with a limit of `limit_us` microseconds (1..1000000).  The wait
+ * runs out, the kernel returns normally and raises the timeout bit, so
+ * csattn_check_status() afterwards returns CSATTN_ERR_TIMEOUT.  Exercises the
+ * failure-detection path without faulting or hanging the GPU.
+ */
+int csattn_selftest_bounded_wait(int limit_us, void* stream);
+
+/* Message describing the last error returned on the calling thread. */
+const char* csattn_last_error(void);
+
+/* Static name of a csattn_status value. */
+const char* csattn_status_str(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int csattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSATTN_H_ */

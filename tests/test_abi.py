@@ -1,0 +1,140 @@
+"""The C-ABI library loads, exports every symbol include/csattn.h declares, and
+rejects invalid arguments on the host.  No GPU needed: no call here reaches a
+kernel launch or any CUDA runtime call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csattn.h")
+
+
+def declared_symbols():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csattn_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import transformer_causal_self_gb300 as csattn
+    return csattn.load_library()
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for must in ("csattn_attn_fwd", "csattn_attn_decode", "csattn_fwd_workspace_size",
+                 "csattn_decode_workspace_size", "csattn_check_status", "csattn_last_error",
+                 "csattn_status_str"):
+        assert must in names
+
+
+def test_binding_covers_header():
+    import transformer_causal_self_gb300 as csattn
+    assert sorted(csattn.EXPORTED_SYMBOLS) == declared_symbols()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert getattr(lib, name) is not None
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True)
+    assert out.returncode == 0
+    exported = set(line.split()[-1] for line in out.stdout.splitlines() if " T " in line)
+    missing = [n for n in declared_symbols() if n not in exported]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    assert lib.csattn_status_str(0) == b"CSATTN_OK"
+    assert lib.csattn_status_str(-4) == b"CSATTN_ERR_TIMEOUT"
+    assert lib.csattn_status_str(123) == b"CSATTN_UNKNOWN_STATUS"
+    assert lib.csattn_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    # rotated keys B*Hkv*T*d bf16 for bf16 + RoPE; nothing otherwise
+    assert lib.csattn_fwd_workspace_size(4, 32, 8, 4096, 128, 1, 10000.0) == 4 * 8 * 4096 * 128 * 2
+    assert lib.csattn_fwd_workspace_size(4, 32, 8, 4096, 128, 1, 0.0) == 0
+    assert lib.csattn_fwd_workspace_size(1, 2, 2, 64, 16, 0, 10000.0) == 0
+    # decode partials: B*Hq*splits*(d+2) fp32, automatic splits cover Lmax/256
+    assert lib.csattn_decode_workspace_size(64, 32, 8192, 128, 0) == 64 * 32 * 32 * 130 * 4
+    assert lib.csattn_decode_workspace_size(2, 4, 100, 64, 5) == 2 * 4 * 5 * 66 * 4
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case below fails before any CUDA call
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1),
+    (dict(B=0), -1),
+    (dict(T=0), -1),
+    (dict(Hq=6, Hkv=4), -1),
+    (dict(dtype=7), -1),
+    (dict(causal=2), -1),
+    (dict(rope_layout=5), -1),
+    (dict(scale=float("nan")), -1),
+    (dict(d=48), -2),
+    (dict(dtype=1, d=16), -2),
+    (dict(dtype=1, d=32), -2),
+    (dict(T=1 << 24), -2),
+    (dict(T=60000, rope_base=10000.0), -2),
+    (dict(q=FAKE + 8), -1),
+    (dict(lse=FAKE + 2), -1),
+    (dict(dtype=1, rope_base=10000.0, ws=None, ws_bytes=0), -5),
+    (dict(dtype=1, rope_base=10000.0, ws=FAKE, ws_bytes=100), -5),
+])
+def test_fwd_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, Hq=4, Hkv=2, T=64, d=64, dtype=0, causal=1,
+             rope_base=0.0, rope_layout=0, scale=0.0, lse=None, ws=None, ws_bytes=0)
+    a.update(kw)
+    rc = lib.csattn_attn_fwd(a["q"], a["k"], a["v"], a["out"], a["B"], a["Hq"], a["Hkv"], a["T"],
+                             a["d"], a["dtype"], a["causal"], a["rope_base"], a["rope_layout"],
+                             a["scale"], a["lse"], a["ws"], a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert len(lib.csattn_last_error()) > 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(seq=None), -1),
+    (dict(B=0), -1),
+    (dict(Hq=6, Hkv=4), -1),
+    (dict(dtype=0), -2),
+    (dict(dtype=9), -1),
+    (dict(d=96), -2),
+    (dict(Hq=34, Hkv=2), -2),
+    (dict(max_len=0), -1),
+    (dict(max_len=300), -1),
+    (dict(splits=-1), -1),
+    (dict(out=FAKE + 4), -1),
+    (dict(splits=2, ws=None, ws_bytes=0), -5),
+    (dict(splits=2, ws=FAKE, ws_bytes=16), -5),
+])
+def test_decode_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, seq=FAKE, out=FAKE, B=2, Hq=8, Hkv=2, Lmax=256, d=128,
+             dtype=1, scale=0.0, max_len=256, splits=0, ws=FAKE, ws_bytes=1 << 20)
+    a.update(kw)
+    rc = lib.csattn_attn_decode(a["q"], a["k"], a["v"], a["seq"], a["out"], a["B"], a["Hq"],
+                                a["Hkv"], a["Lmax"], a["d"], a["dtype"], a["scale"], a["max_len"],
+                                a["splits"], a["ws"], a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.csattn_selftest_bounded_wait(0, None) == -1
+    assert lib.csattn_selftest_bounded_wait(2000000, None) == -1
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "transformer_causal_self_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                with open(os.path.join(dirpath, f)) as fh:
+                    src = fh.read()
+                assert "oracle" not in re.findall(r"^\s*(?:from|import)\s+(\w+)", src, re.M), f

@@ -1,0 +1,98 @@
+"""Decode parity and the failure-detection paths, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_workloads as W
+import transformer_causal_self_gb300 as csattn
+from oracle import attn as OA
+from tests.gpu_helpers import assert_bf16_close, dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode(q, kc, vc, lens, **kw):
+    out = csattn.attn_decode(q.to(dev()), kc.to(dev()), vc.to(dev()), lens.to(dev()), **kw)
+    csattn.check_status()
+    return out
+
+
+def test_decode_workload_full():
+    w = W.WORKLOADS["decode_bf16"]
+    q, kc, vc, lens = W.make_decode_inputs(w)
+    out = _decode(q, kc, vc, lens, scale=w.scale, max_seq_len=int(lens.max()))
+    ref = OA.decode(q, kc, vc, lens.numpy(), scale=w.scale)
+    assert_bf16_close(to_np(out), ref, "decode")
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 8, 128), (16, 4, 128), (16, 2, 64), (32, 2, 128), (6, 2, 64)])
+def test_decode_groups_and_lengths(Hq, Hkv, d):
+    lens = [1, 63, 64, 65, 128, 1000, 777]
+    w = W.DecodeWorkload("dec", B=len(lens), Hq=Hq, Hkv=Hkv, d=d, Lmax=1000, Lmin=1,
+                         scale=1.0 / math.sqrt(d), seed=Hq + d)
+    q, kc, vc, sl = W.make_decode_inputs(w, seq_lens=lens)
+    ref = OA.decode(q, kc, vc, sl.numpy(), scale=w.scale)
+    for splits in (0, 1, 3, 16):
+        out = _decode(q, kc, vc, sl, scale=w.scale, max_seq_len=1000, num_splits=splits)
+        assert_bf16_close(to_np(out), ref, f"decode splits={splits}")
+
+
+def test_decode_split_count_invariance():
+    w = W.WORKLOADS["decode_bf16"].with_(B=8, Lmax=4096, Lmin=512)
+    q, kc, vc, sl = W.make_decode_inputs(w)
+    outs = [to_np(_decode(q, kc, vc, sl, scale=w.scale, max_seq_len=4096, num_splits=s))
+            for s in (1, 4, 7, 64)]
+    for o in outs[1:]:
+        assert np.max(np.abs(o - outs[0])) <= 1e-2
+        assert np.linalg.norm(o - outs[0]) / np.linalg.norm(outs[0]) <= 1e-3
+
+
+def test_decode_matches_prefill_last_row():
+    """Decode at length L equals row L-1 of the prefill on the same rotated data."""
+    T, d = 700, 128
+    w = W.WORKLOADS["llama_gqa_bf16"].with_(B=2, Hq=8, Hkv=2, T=T)
+    q, k, v = W.make_prefill_inputs(w)
+    full = csattn.attn_fwd(q.to(dev()), k.to(dev()), v.to(dev()), causal=True,
+                           rope_base=w.rope_base, scale=w.scale).cpu()
+    # pre-rotated query and cache as the oracle rounds them (inputs, not expected values)
+    qr = torch.from_numpy(OA.round_to_bf16(OA.rope_rotate(q.double().numpy(), np.arange(T),
+                                                          w.rope_base))).to(torch.bfloat16)
+    kr = torch.from_numpy(OA.round_to_bf16(OA.rope_rotate(k.double().numpy(), np.arange(T),
+                                                          w.rope_base))).to(torch.bfloat16)
+    lens = torch.tensor([T, 311], dtype=torch.int32)
+    qd = torch.stack([qr[0, :, T - 1:T], qr[1, :, 310:311]]).contiguous()
+    out = _decode(qd, kr.contiguous(), v, lens, scale=w.scale, max_seq_len=T).cpu()
+    assert torch.max(torch.abs(out[0, :, 0].float() - full[0, :, T - 1].float())) <= 2e-2
+    ref = OA.decode(qd, kr, v, lens.numpy(), scale=w.scale)
+    assert_bf16_close(to_np(out), ref, "decode vs oracle")
+
+
+def test_decode_bad_seq_len_sets_device_error():
+    w = W.WORKLOADS["decode_bf16"].with_(B=3, Lmax=256, Lmin=1)
+    q, kc, vc, _ = W.make_decode_inputs(w, seq_lens=[10, 20, 30])
+    lens = torch.tensor([10, 0, 30], dtype=torch.int32)
+    out = csattn.attn_decode(q.to(dev()), kc.to(dev()), vc.to(dev()), lens.to(dev()),
+                             scale=w.scale, max_seq_len=256)
+    with pytest.raises(csattn.CsattnError) as e:
+        csattn.check_status()
+    assert e.value.status == -6
+    assert torch.all(out[1].float().cpu() == 0)
+    csattn.check_status()  # cleared
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    csattn.selftest_bounded_wait(2000)
+    with pytest.raises(csattn.CsattnError) as e:
+        csattn.check_status()
+    assert e.value.status == -4
+    csattn.check_status()  # cleared, context usable
+    w = W.WORKLOADS["llama_gqa_bf16"].with_(B=1, Hq=2, Hkv=1, T=130)
+    q, k, v = W.make_prefill_inputs(w)
+    out = csattn.attn_fwd(q.to(dev()), k.to(dev()), v.to(dev()), rope_base=w.rope_base,
+                          scale=w.scale)
+    csattn.check_status()
+    ref = OA.attention(q, k, v, causal=True, rope_base=w.rope_base, scale=w.scale,
+                       operand_dtype="bf16")
+    assert_bf16_close(to_np(out), ref, "after timeout")

@@ -1,0 +1,183 @@
+"""Python binding of libcsattn, the sm_103a causal GQA attention library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/csattn.h.  PyTorch provides the
+device memory (tensors, workspaces) and the stream.  There is no CPU fallback:
+if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "CsattnError", "library_path", "load_library", "attn_fwd", "attn_decode",
+    "fwd_workspace_size", "decode_workspace_size", "check_status",
+    "selftest_bounded_wait", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB: Optional[ctypes.CDLL] = None
+
+CSATTN_F32, CSATTN_BF16 = 0, 1
+_ROPE_LAYOUT = {"split_half": 0, "adjacent": 1}
+_STATUS = {0: "CSATTN_OK", -1: "CSATTN_ERR_INVALID_ARG", -2: "CSATTN_ERR_UNSUPPORTED",
+           -3: "CSATTN_ERR_CUDA", -4: "CSATTN_ERR_TIMEOUT", -5: "CSATTN_ERR_WORKSPACE",
+           -6: "CSATTN_ERR_DEVICE_ARG"}
+
+_c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+# name -> (restype, argtypes); the C declarations are in include/csattn.h
+_SIGNATURES = {
+    "csattn_fwd_workspace_size": (_c_size, [_c_int] * 6 + [_c_float]),
+    "csattn_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _c_float,
+                                                                        _vp, _vp, _c_size, _vp]),
+    "csattn_decode_workspace_size": (_c_size, [_c_int] * 5),
+    "csattn_attn_decode": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp,
+                                                                _c_size, _vp]),
+    "csattn_check_status": (_c_int, [_vp]),
+    "csattn_selftest_bounded_wait": (_c_int, [_c_int, _vp]),
+    "csattn_last_error": (ctypes.c_char_p, []),
+    "csattn_status_str": (ctypes.c_char_p, [_c_int]),
+    "csattn_version": (_c_int, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+
+class CsattnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libcsattn.so")
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libcsattn.so (built by __graft_entry__.build()); raises if it is missing."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built: run `python -c 'import __graft_entry__ as g; "
+                               "g.build()'` first (there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = load_library().csattn_last_error()
+        raise CsattnError(status, msg.decode() if msg else "")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return CSATTN_BF16
+    if t.dtype == torch.float32:
+        return CSATTN_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def fwd_workspace_size(B, Hq, Hkv, T, d, dtype: torch.dtype, rope_base: float) -> int:
+    code = CSATTN_BF16 if dtype == torch.bfloat16 else CSATTN_F32
+    return int(load_library().csattn_fwd_workspace_size(B, Hq, Hkv, T, d, code, float(rope_base)))
+
+
+def decode_workspace_size(B, Hq, Lmax, d, num_splits: int = 0) -> int:
+    return int(load_library().csattn_decode_workspace_size(B, Hq, Lmax, d, num_splits))
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: Optional[torch.Tensor] = None,
+             *, causal: bool = True, rope_base: float = 0.0, scale: float = 0.0,
+             rope_layout: str = "split_half", lse: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out = softmax(RoPE(q) RoPE(k)^T * scale + M) v  (C: csattn_attn_fwd).
+
+    q [B,Hq,T,d], k/v [B,Hkv,T,d] (bf16 or fp32, contiguous, CUDA).  scale <= 0
+    means 1/sqrt(d); rope_base <= 0 means no RoPE.  lse, if given, is an fp32
+    [B,Hq,T] tensor that receives the natural-log log-sum-exp of each row.
+    """
+    _need_cuda(q, k, v)
+    B, Hq, T, d = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda(out)
+    if lse is not None:
+        _need_cuda(lse)
+    need = fwd_workspace_size(B, Hq, Hkv, T, d, q.dtype, rope_base)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    lib = load_library()
+    _check(lib.csattn_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv,
+                               T, d, _dtype_code(q), int(bool(causal)), float(rope_base),
+                               _ROPE_LAYOUT[rope_layout], float(scale),
+                               lse.data_ptr() if lse is not None else None, ws_ptr, ws_bytes,
+                               _stream_handle(stream)))
+    return out
+
+
+def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                seq_lens: torch.Tensor, out: Optional[torch.Tensor] = None, *, scale: float = 0.0,
+                max_seq_len: Optional[int] = None, num_splits: int = 0,
+                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """KV-cache decode (C: csattn_attn_decode).
+
+    q [B,Hq,1,d] already rotated; k_cache/v_cache [B,Hkv,Lmax,d]; seq_lens int32
+    [B] on the device.  max_seq_len defaults to Lmax (always a valid bound).
+    """
+    _need_cuda(q, k_cache, v_cache, seq_lens)
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    B, Hq, _, d = q.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    if max_seq_len is None:
+        max_seq_len = Lmax
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda(out)
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_size(B, Hq, Lmax, d, num_splits),
+                                dtype=torch.uint8, device=q.device)
+    lib = load_library()
+    _check(lib.csattn_attn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                  seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lmax, d,
+                                  _dtype_code(q), float(scale), int(max_seq_len), int(num_splits),
+                                  workspace.data_ptr(), workspace.numel(), _stream_handle(stream)))
+    return out
+
+
+def check_status(stream=None) -> None:
+    """Synchronize the stream and raise if a kernel reported a timeout or a device-side error."""
+    _check(load_library().csattn_check_status(_stream_handle(stream)))
+
+
+def selftest_bounded_wait(limit_us: int, stream=None) -> None:
+    """Launch the kernel whose barrier wait must run out (see csattn_selftest_bounded_wait)."""
+    _check(load_library().csattn_selftest_bounded_wait(int(limit_us), _stream_handle(stream)))

@@ -1,0 +1,345 @@
+// C ABI of libcsattn: argument checks, the per-device status word, TMA
+// descriptor encoding, and dispatch to the kernels.  See include/csattn.h for
+// the contract of every entry point.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/csattn.h"
+#include "internal.h"
+
+namespace csattn {
+
+// One status word per device (a static device variable exists once on every
+// device that loads the library).  Kernels OR bits into it; csattn_check_status
+// reads and clears it.
+__device__ uint32_t g_status_word;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(CSATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+// Device address of the status word and the SM count of the current device.
+int device_info(uint32_t** status, int* num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(CSATTN_ERR_UNSUPPORTED, "device %d", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_status_word);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(status word)");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+    g_status_ptr[dev] = static_cast<uint32_t*>(ptr);
+    g_num_sms[dev] = sms;
+  }
+  *status = g_status_ptr[dev];
+  *num_sms = g_num_sms[dev];
+  return CSATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// theta_p = base^(-2p/d), p < d/2, split into float hi + lo (hi + lo = theta
+// to about 2^-48 relative).
+void rope_table(RopeTable* t, int d, double base) {
+  std::memset(t, 0, sizeof(*t));
+  for (int p = 0; p < d / 2 && p < 64; ++p) {
+    const double th = std::pow(base, -2.0 * p / static_cast<double>(d));
+    const float hi = static_cast<float>(th);
+    t->hi[p] = hi;
+    t->lo[p] = static_cast<float>(th - static_cast<double>(hi));
+  }
+}
+
+// Largest position whose angle the kernels' Cody-Waite reduction keeps exact
+// (|k| < 2^13 multiples of 2 pi for theta_0 = 1).
+constexpr int kMaxRopePositions = 49152;
+
+}  // namespace
+
+void* tensor_map_encoder() {
+  static void* fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return p;
+  }();
+  return fn;
+}
+
+bool make_tmap_bf16_3d(void* tmap_out, const void* base, int d, int rows, int planes,
+                       int box_rows) {
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+  if (encode == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = encode(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                      const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace csattn
+
+using namespace csattn;
+
+extern "C" {
+
+const char* csattn_last_error(void) { return g_last_error.c_str(); }
+
+const char* csattn_status_str(int status) {
+  switch (status) {
+    case CSATTN_OK: return "CSATTN_OK";
+    case CSATTN_ERR_INVALID_ARG: return "CSATTN_ERR_INVALID_ARG";
+    case CSATTN_ERR_UNSUPPORTED: return "CSATTN_ERR_UNSUPPORTED";
+    case CSATTN_ERR_CUDA: return "CSATTN_ERR_CUDA";
+    case CSATTN_ERR_TIMEOUT: return "CSATTN_ERR_TIMEOUT";
+    case CSATTN_ERR_WORKSPACE: return "CSATTN_ERR_WORKSPACE";
+    case CSATTN_ERR_DEVICE_ARG: return "CSATTN_ERR_DEVICE_ARG";
+    default: return "CSATTN_UNKNOWN_STATUS";
+  }
+}
+
+int csattn_version(void) { return 100; }
+
+size_t csattn_fwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,
+                                 float rope_base) {
+  (void)Hq;
+  if (dtype != CSATTN_BF16 || !(rope_base > 0.f) || B < 1 || Hkv < 1 || T < 1 || d < 1) return 0;
+  return static_cast<size_t>(B) * Hkv * T * d * 2;
+}
+
+int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                    int Hkv, int T, int d, int dtype, int causal, float rope_base,
+                    int rope_layout, float scale, float* lse, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: q, k, v and out must be non-null");
+  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: B=%d Hq=%d Hkv=%d T=%d must be >= 1", B, Hq,
+                Hkv, T);
+  if (Hq % Hkv != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (dtype != CSATTN_F32 && dtype != CSATTN_BF16)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: unknown dtype %d", dtype);
+  if (causal != 0 && causal != 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: causal must be 0 or 1");
+  if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: unknown rope_layout %d", rope_layout);
+  if (!std::isfinite(rope_base) || !std::isfinite(scale))
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: rope_base and scale must be finite");
+  if (d != 16 && d != 32 && d != 64 && d != 128)
+    return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: d=%d not in {16,32,64,128}", d);
+  if (dtype == CSATTN_BF16 && d != 64 && d != 128)
+    return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: bf16 supports d in {64,128}, got %d", d);
+  if (T >= (1 << 24)) return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: T=%d >= 2^24", T);
+  if (rope_base > 0.f && T > kMaxRopePositions)
+    return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: RoPE supports T <= %d, got %d",
+                kMaxRopePositions, T);
+  if (static_cast<long long>(B) * Hq > (1LL << 31) - 1)
+    return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: B*Hq too large");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: q, k, v, out must be 16-byte aligned");
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: lse must be 4-byte aligned");
+  const size_t need = csattn_fwd_workspace_size(B, Hq, Hkv, T, d, dtype, rope_base);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return fail(CSATTN_ERR_WORKSPACE,
+                "attn_fwd: needs a 16-byte aligned workspace of %zu bytes (got %zu)", need,
+                workspace_bytes);
+
+  FwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.T = T;
+  a.d = d;
+  a.causal = causal;
+  a.rope = rope_base > 0.f ? (rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2) : 0;
+  a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  if (a.rope) rope_table(&a.theta, d, static_cast<double>(rope_base));
+  int rc = device_info(&a.status, &a.num_sms);
+  if (rc != CSATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  cudaError_t e;
+  if (dtype == CSATTN_F32) {
+    e = launch_fwd_f32(a, st);
+    if (e != cudaSuccess) return fail_cuda(e, "attn_fwd: fp32 kernel launch");
+    return CSATTN_OK;
+  }
+  if (tensor_map_encoder() == nullptr)
+    return fail(CSATTN_ERR_CUDA, "attn_fwd: cuTensorMapEncodeTiled is unavailable");
+  const void* k_eff = k;
+  if (a.rope) {
+    e = launch_rope_rotate_bf16(k, workspace, B, Hkv, T, d, a.rope, a.theta, st);
+    if (e != cudaSuccess) return fail_cuda(e, "attn_fwd: RoPE kernel launch");
+    k_eff = workspace;
+  }
+  e = launch_fwd_sm103a(a, k_eff, st);
+  if (e != cudaSuccess) return fail_cuda(e, "attn_fwd: sm_103a kernel launch");
+  return CSATTN_OK;
+}
+
+size_t csattn_decode_workspace_size(int B, int Hq, int Lmax, int d, int num_splits) {
+  if (B < 1 || Hq < 1 || Lmax < 1 || d < 1 || num_splits < 0) return 0;
+  const size_t splits = num_splits > 0 ? static_cast<size_t>(num_splits)
+                                       : static_cast<size_t>((Lmax + 255) / 256);
+  // part_o [B, Hq, S, d] then part_ml [B, Hq, S, 2], fp32
+  return static_cast<size_t>(B) * Hq * splits * (static_cast<size_t>(d) + 2) * 4;
+}
+
+int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int Lmax,
+                       int d, int dtype, float scale, int max_seq_len, int num_splits,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
+      out == nullptr)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: null pointer argument");
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: B=%d Hq=%d Hkv=%d Lmax=%d must be >= 1",
+                B, Hq, Hkv, Lmax);
+  if (Hq % Hkv != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: Hq=%d is not a multiple of Hkv=%d", Hq,
+                Hkv);
+  if (dtype != CSATTN_BF16)
+    return fail(dtype == CSATTN_F32 ? CSATTN_ERR_UNSUPPORTED : CSATTN_ERR_INVALID_ARG,
+                "attn_decode: only bf16 is implemented (dtype %d)", dtype);
+  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "attn_decode: d=%d", d);
+  if (Hq / Hkv > 16)
+    return fail(CSATTN_ERR_UNSUPPORTED, "attn_decode: group size %d > 16", Hq / Hkv);
+  if (max_seq_len < 1 || max_seq_len > Lmax)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: max_seq_len=%d not in [1, Lmax=%d]",
+                max_seq_len, Lmax);
+  if (num_splits < 0) return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: num_splits < 0");
+  if (!std::isfinite(scale)) return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: scale not finite");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: misaligned pointer");
+
+  int rc;
+  DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Lmax = Lmax;
+  a.d = d;
+  a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  a.max_seq_len = max_seq_len;
+  int num_sms = 0;
+  if (num_splits > 0) {
+    const int per = (max_seq_len + num_splits - 1) / num_splits;
+    a.chunk = ((per + 63) / 64) * 64;
+  } else {
+    rc = device_info(&a.status, &num_sms);
+    if (rc != CSATTN_OK) return rc;
+    // Smallest chunk (>= 256 keys) that keeps the grid near eight CTAs per SM.
+    a.chunk = 256;
+    while (a.chunk < 4096 &&
+           static_cast<long long>(B) * Hkv * ((max_seq_len + a.chunk - 1) / a.chunk) >
+               8LL * num_sms)
+      a.chunk *= 2;
+  }
+  a.n_splits = (max_seq_len + a.chunk - 1) / a.chunk;
+  const size_t need = static_cast<size_t>(B) * Hq * a.n_splits * (static_cast<size_t>(d) + 2) * 4;
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return fail(CSATTN_ERR_WORKSPACE,
+                "attn_decode: needs a 16-byte aligned workspace of %zu bytes (got %zu)", need,
+                workspace_bytes);
+  if (a.status == nullptr) {
+    rc = device_info(&a.status, &num_sms);
+    if (rc != CSATTN_OK) return rc;
+  }
+  a.part_o = static_cast<float*>(workspace);
+  a.part_ml = a.part_o + static_cast<size_t>(B) * Hq * a.n_splits * d;
+  if (tensor_map_encoder() == nullptr)
+    return fail(CSATTN_ERR_CUDA, "attn_decode: cuTensorMapEncodeTiled is unavailable");
+  cudaError_t e = launch_decode_bf16(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "attn_decode: kernel launch");
+  return CSATTN_OK;
+}
+
+int csattn_check_status(void* stream) {
+  uint32_t* status = nullptr;
+  int num_sms = 0;
+  int rc = device_info(&status, &num_sms);
+  if (rc != CSATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail_cuda(e, "check_status: stream synchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e, "check_status: read status word");
+  if (word != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e, "check_status: clear status word");
+  }
+  if (word & kStatusTimeout)
+    return fail(CSATTN_ERR_TIMEOUT, "a kernel wait ran out of time (status 0x%x)", word);
+  if (word & kStatusDeviceArg)
+    return fail(CSATTN_ERR_DEVICE_ARG, "a device-side argument check failed (status 0x%x)", word);
+  return CSATTN_OK;
+}
+
+int csattn_selftest_bounded_wait(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(CSATTN_ERR_INVALID_ARG, "selftest: limit_us=%d not in [1, 1e6]", limit_us);
+  uint32_t* status = nullptr;
+  int num_sms = 0;
+  int rc = device_info(&status, &num_sms);
+  if (rc != CSATTN_OK) return rc;
+  cudaError_t e = launch_selftest_wait(status, static_cast<uint64_t>(limit_us) * 1000ull,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "selftest: launch");
+  return CSATTN_OK;
+}
+
+}  // extern "C"

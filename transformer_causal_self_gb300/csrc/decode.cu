@@ -1,0 +1,402 @@
+// KV-cache decode, bf16, one new query per sequence: split-KV partials plus a
+// log-sum-exp merge.  The query of sequence b sits at position L_b - 1 and
+// attends to cached rows 0..L_b-1 ("The Transformer architecture"
+// (cooking-agi), section "Hands-on": with a cache the query position is
+// cache.pos and the keys run from 0 to cache.pos).  The whole cost is reading
+// K and V once: 2 * n_kv * d_head * L * sizeof(bf16) bytes per sequence, the
+// pages' KV-cache formula with one layer (same page, section "What else the
+// modern decoder-only model changed").
+//
+// Grid (split, kv_head, batch).  One CTA reads a chunk of one sequence's K/V
+// rows once for all the query heads of the KV head's group:
+//   warp 4      TMA producer: 64-row K and V tiles into a 3-stage ring
+//   warps 0-3   16 keys each per tile:  S = Q K^T and O += P V on the tensor
+//               cores (mma.sync m16n8k16; rows = the group's query heads,
+//               padded to 16), online softmax in fp32 between the two.
+// The per-CTA result (running max m, sum l, un-normalised O, log2 units) is
+// written to the workspace; decode_combine_kernel merges the splits:
+//   m = max_s m_s,  l = sum_s l_s 2^(m_s - m),  o = sum_s o_s 2^(m_s - m) / l.
+// Cache rows at or beyond L_b are never used: scores of those keys are set to
+// -inf and the V rows of the final tile are zeroed in shared memory before
+// the second MMA (the cache past L_b may hold anything, NaN included).
+#include "internal.h"
+
+namespace csattn {
+namespace {
+
+constexpr int KT = 64;  // keys per tile
+constexpr int NS = 3;   // ring stages
+constexpr int kComputeWarps = 4;
+constexpr int kThreads = 32 * (kComputeWarps + 1);
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 100000000ull;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct DCfg {
+  static constexpr int KB = D / 64;
+  static constexpr int BLOCK_BYTES = KT * 128;      // one 64-column block of a 64-row tile
+  static constexpr int TILE_BYTES = KT * D * 2;     // K or V tile
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int SMEM_BYTES = NS * STAGE_BYTES + 1024 + 1024;
+};
+
+struct DParams {
+  const __nv_bfloat16* q;
+  const int32_t* seq_lens;
+  float* part_o;
+  float* part_ml;
+  uint32_t* status;
+  int B, Hq, Hkv, Lmax, rep, max_seq_len, chunk, n_splits;
+  float scale_log2;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// shared-memory byte offset of 16-byte chunk `cc` (8 channels) of row r of a
+// 64-row tile stored as 128-byte-swizzled column blocks (TMA SWIZZLE_128B)
+__device__ __forceinline__ uint32_t tile_off(int r, int cc) {
+  return static_cast<uint32_t>((cc >> 3) * (KT * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+    decode_bf16_kernel(const __grid_constant__ DParams p, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v) {
+  using C = DCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * C::STAGE_BYTES);
+  uint64_t* empty = full + NS;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NS);
+  float* s_ml = reinterpret_cast<float*>(smem + NS * C::STAGE_BYTES + 256);  // [4 warps][16][2]
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int L = p.seq_lens[b];
+  if (L < 1 || L > p.max_seq_len) {
+    if (threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(p.status, kStatusDeviceArg);
+    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+  }
+  const int k_begin = split * p.chunk;
+  const int k_end = min(L, k_begin + p.chunk);
+  if (k_begin >= k_end) return;  // the merge reads only splits that hold keys
+  const int ntiles = (k_end - k_begin + KT - 1) / KT;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kComputeWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kComputeWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const int z = b * p.Hkv + kvh;
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % NS, use = t / NS;
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) break;
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        uint8_t* kdst = smem + s * C::STAGE_BYTES;
+        uint8_t* vdst = kdst + C::TILE_BYTES;
+        const int row = k_begin + t * KT;
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &full[s], kb * 64, row, z);
+          tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &full[s], kb * 64, row, z);
+        }
+        ++issued;
+      }
+      if (*abort_flag) {
+        const int first = issued > NS ? issued - NS : 0;
+        for (int t = first; t < issued; ++t)
+          mbar_wait(&full[t % NS], (t / NS) & 1, nullptr, p.status, kDrainNs);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- compute warps
+  const int r0 = lane >> 2;        // fragment rows r0 and r0 + 8 = query heads of the group
+  const int cq = 2 * (lane & 3);   // fragment column pair
+  const __nv_bfloat16* qg = p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.rep) * D;
+  uint32_t qa[D / 16][4];
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qg + static_cast<size_t>(r0) * D);
+    const uint32_t* q8 = reinterpret_cast<const uint32_t*>(qg + static_cast<size_t>(r0 + 8) * D);
+    qa[kk][0] = (r0 < p.rep) ? q0[(16 * kk + cq) >> 1] : 0u;
+    qa[kk][1] = (r0 + 8 < p.rep) ? q8[(16 * kk + cq) >> 1] : 0u;
+    qa[kk][2] = (r0 < p.rep) ? q0[(16 * kk + 8 + cq) >> 1] : 0u;
+    qa[kk][3] = (r0 + 8 < p.rep) ? q8[(16 * kk + 8 + cq) >> 1] : 0u;
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_used[2] = {-INFINITY, -INFINITY};  // rows r0, r0 + 8
+  float l_part[2] = {0.f, 0.f};
+  const float sl2 = p.scale_log2;
+  const uint32_t smem_base = smem_u32(smem);
+
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % NS;
+    if (!mbar_wait(&full[s], (t / NS) & 1, abort_flag, p.status, kWaitNs)) {
+      ok = false;
+      break;
+    }
+    const uint32_t kbase = smem_base + s * C::STAGE_BYTES;
+    const uint32_t vbase = kbase + C::TILE_BYTES;
+    const int key0 = k_begin + t * KT + 16 * warp;  // first key of this warp's slice
+    const int nvalid = k_end - key0;                // keys of the slice that exist (may be <= 0)
+
+    // S = Q K^T for 16 keys (two n-tiles of 8)
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3;  // which 8x8 matrix this lane addresses
+      const int kr = 16 * warp + (lane & 7) + 8 * (mi >> 1);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + tile_off(kr, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+        mma_bf16(sc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+        mma_bf16(sc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+      }
+    }
+    // mask keys past the end of the split, scale to log2 units, row max
+    float x[2][4];
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = 8 * nt + cq + (e & 1);
+        const float v = (key < nvalid) ? sc[nt][e] * sl2 : -INFINITY;
+        x[nt][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+    }
+    float f[2] = {1.f, 1.f};
+    bool need = false;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float m_new = fmaxf(m_used[h], mx[h]);
+      if (m_new > m_used[h] + kRescaleThreshold) {
+        f[h] = ex2_approx(m_used[h] - m_new);  // 0 when m_used was -inf
+        m_used[h] = m_new;
+        need = true;
+      }
+    }
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= f[0];
+        o[n][1] *= f[0];
+        o[n][2] *= f[1];
+        o[n][3] *= f[1];
+      }
+      l_part[0] *= f[0];
+      l_part[1] *= f[1];
+    }
+    float pr[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float mu = m_used[e >> 1];
+        const float v = (mu == -INFINITY) ? 0.f : ex2_approx(x[nt][e] - mu);
+        pr[nt][e] = v;
+        l_part[e >> 1] += v;
+      }
+    const uint32_t pa0 = pack_bf16x2(pr[0][0], pr[0][1]);
+    const uint32_t pa1 = pack_bf16x2(pr[0][2], pr[0][3]);
+    const uint32_t pa2 = pack_bf16x2(pr[1][0], pr[1][1]);
+    const uint32_t pa3 = pack_bf16x2(pr[1][2], pr[1][3]);
+
+    // V rows past the end of the sequence may hold anything: zero them
+    const bool zeroed = nvalid < 16;
+    if (zeroed) {
+      uint8_t* vtile = smem + s * C::STAGE_BYTES + C::TILE_BYTES;
+      const int first = nvalid < 0 ? 0 : nvalid;
+      for (int e = lane; e < 16 * (D / 8); e += 32) {
+        const int rr = e / (D / 8), cc = e % (D / 8);
+        if (rr >= first)
+          *reinterpret_cast<uint4*>(vtile + tile_off(16 * warp + rr, cc)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    // O += P V for 16 keys: 8-channel n-tiles in pairs
+    {
+      const int mi = lane >> 3;
+      const int vr = 16 * warp + (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+      for (int np = 0; np < D / 16; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + tile_off(vr, 2 * np + (mi >> 1)), b0, b1, b2, b3);
+        mma_bf16(o[2 * np], pa0, pa1, pa2, pa3, b0, b1);
+        mma_bf16(o[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
+      }
+    }
+    if (zeroed) fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // sum l over the four lanes of a row
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    l_part[h] += __shfl_xor_sync(0xffffffffu, l_part[h], 1);
+    l_part[h] += __shfl_xor_sync(0xffffffffu, l_part[h], 2);
+  }
+  // all tiles consumed: the ring is free to hold the per-warp results
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
+  if (!ok || *abort_flag) return;
+  float* s_o = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][D]
+  if ((lane & 3) == 0) {
+    s_ml[(warp * 16 + r0) * 2 + 0] = m_used[0];
+    s_ml[(warp * 16 + r0) * 2 + 1] = l_part[0];
+    s_ml[(warp * 16 + r0 + 8) * 2 + 0] = m_used[1];
+    s_ml[(warp * 16 + r0 + 8) * 2 + 1] = l_part[1];
+  }
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    const int c = 8 * n + cq;
+    s_o[(warp * 16 + r0) * D + c] = o[n][0];
+    s_o[(warp * 16 + r0) * D + c + 1] = o[n][1];
+    s_o[(warp * 16 + r0 + 8) * D + c] = o[n][2];
+    s_o[(warp * 16 + r0 + 8) * D + c + 1] = o[n][3];
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
+  // merge the four warps; write this split's partial for each head of the group
+  for (int e = threadIdx.x; e < p.rep * D; e += 32 * kComputeWarps) {
+    const int r = e / D, c = e % D;
+    float m = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kComputeWarps; ++w) m = fmaxf(m, s_ml[(w * 16 + r) * 2]);
+    float acc = 0.f, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kComputeWarps; ++w) {
+      const float mw = s_ml[(w * 16 + r) * 2];
+      const float fw = (mw == -INFINITY) ? 0.f : ex2_approx(mw - m);
+      acc += fw * s_o[(w * 16 + r) * D + c];
+      l += fw * s_ml[(w * 16 + r) * 2 + 1];
+    }
+    const size_t row = (static_cast<size_t>(b) * p.Hq + kvh * p.rep + r) * p.n_splits + split;
+    p.part_o[row * D + c] = acc;
+    if (c == 0) {
+      p.part_ml[row * 2 + 0] = m;
+      p.part_ml[row * 2 + 1] = l;
+    }
+  }
+}
+
+// out[b, h, :] = merge of the splits that hold keys of sequence b.
+__global__ void decode_combine_kernel(const float* __restrict__ part_o,
+                                      const float* __restrict__ part_ml,
+                                      const int32_t* __restrict__ seq_lens,
+                                      __nv_bfloat16* __restrict__ out, int Hq, int n_splits,
+                                      int chunk, int max_seq_len, int D) {
+  const int bh = blockIdx.x;
+  const int b = bh / Hq;
+  int L = seq_lens[b];
+  L = L < 0 ? 0 : (L > max_seq_len ? max_seq_len : L);
+  const int ns = (L + chunk - 1) / chunk;
+  const float* ml = part_ml + static_cast<size_t>(bh) * n_splits * 2;
+  const float* po = part_o + static_cast<size_t>(bh) * n_splits * D;
+  float m = -INFINITY;
+  for (int s = 0; s < ns; ++s) m = fmaxf(m, ml[2 * s]);
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float acc = 0.f, l = 0.f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < ns; ++s) {
+        const float ms = ml[2 * s];
+        const float f = (ms == -INFINITY) ? 0.f : ex2_approx(ms - m);
+        acc += f * po[static_cast<size_t>(s) * D + c];
+        l += f * ml[2 * s + 1];
+      }
+    }
+    out[static_cast<size_t>(bh) * D + c] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
+  using C = DCfg<D>;
+  DParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.seq_lens = a.seq_lens;
+  p.part_o = a.part_o;
+  p.part_ml = a.part_ml;
+  p.status = a.status;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Lmax = a.Lmax;
+  p.rep = a.Hq / a.Hkv;
+  p.max_seq_len = a.max_seq_len;
+  p.chunk = a.chunk;
+  p.n_splits = a.n_splits;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+
+  alignas(64) CUtensorMap tk, tv;
+  if (!make_tmap_bf16_3d(&tk, a.k_cache, D, a.Lmax, a.B * a.Hkv, KT) ||
+      !make_tmap_bf16_3d(&tv, a.v_cache, D, a.Lmax, a.B * a.Hkv, KT))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.n_splits, a.Hkv, a.B);
+  decode_bf16_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tk, tv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_combine_kernel<<<a.B * a.Hq, D, 0, stream>>>(
+      a.part_o, a.part_ml, a.seq_lens, static_cast<__nv_bfloat16*>(a.out), a.Hq, a.n_splits,
+      a.chunk, a.max_seq_len, D);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return launch_d<64>(a, stream);
+    case 128: return launch_d<128>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace csattn

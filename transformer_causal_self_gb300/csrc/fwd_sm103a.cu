@@ -1,0 +1,576 @@
+// Causal GQA attention prefill, bf16 in / bf16 out, fp32 accumulation, for
+// sm_103a: TMA tiles into shared memory, tcgen05 MMAs with TMEM accumulators,
+// online softmax in fp32.  The T x T score matrix never leaves the SM
+// ("Grasping Codes and Math 02", section "Flash Attention: The GPU Does
+// Everything in One Pass": same result without materialising the matrix).
+//
+// Work unit: two 128-row query tiles (A and B) that read the same KV head.
+// With a GQA group of >= 2 query heads, A and B are the same rows of two heads
+// of the group, so every K/V tile is loaded once for both; otherwise they are
+// two consecutive tiles of one head.  The CTA is persistent (one per SM) and
+// walks the units longest-first in a snake order.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax for tile A (TMEM lanes 0-127 = query rows)
+//   warps 4-7  softmax for tile B
+//   warp 8     TMA producer: Q_A, Q_B, then K_0, V_0, K_1, V_1, ... into a ring
+//   warp 9     TMEM allocator and MMA issuer (one thread)
+// TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [256+D,256+2D).
+// P (bf16) overwrites the first 64 columns of its S region and feeds the
+// second MMA straight from TMEM.
+//
+// MMA order per KV tile j (per unit):  PV_A(j) S_A(j+1) PV_B(j) S_B(j+1), so
+// each softmax warpgroup has two MMAs' time to turn S(j+1) into P(j+1) while
+// the tensor core works on the other tile.
+//
+// Online softmax per row (scores in log2 units, x = s * scale * log2 e):
+//   m = running max used for the exponent, l = running sum, O in TMEM.
+//   A new tile raises m only when its max exceeds m by more than 8 (a factor
+//   256); then O and l are rescaled by 2^(m_old - m_new).  P = 2^(x - m) <= 256.
+// Causal mask: score (i, j) = -inf when key j > query i, applied only in the
+// tiles that cross the diagonal; tiles entirely above it are skipped
+// ("Transformer" (ai-notes), section "What is the causal mask?").
+#include "internal.h"
+
+namespace csattn {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile = TMEM lanes
+constexpr int BN = 128;  // keys per KV tile
+constexpr int kThreads = 320;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s: far above any legal wait
+constexpr uint64_t kDrainNs = 100000000ull;     // 100 ms for the teardown after an abort
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
+
+template <int D>
+struct Cfg {
+  static constexpr int KB = D / 64;              // 128-byte column blocks per row
+  static constexpr int BLOCK_BYTES = BM * 128;   // one column block of a 128-row tile
+  static constexpr int TILE_BYTES = BM * D * 2;  // one Q / K / V tile
+  static constexpr int NS = (D == 128) ? 4 : 8;  // K/V ring stages
+  static constexpr int SMEM_TILE_BYTES = (2 + NS) * TILE_BYTES;
+  static constexpr int SMEM_BYTES = SMEM_TILE_BYTES + 1024 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);
+};
+
+struct Params {
+  __nv_bfloat16* out;
+  float* lse;
+  uint32_t* status;
+  int B, Hq, Hkv, T;
+  int rep;      // Hq / Hkv
+  int hp;       // head pairs per group (rep / 2)
+  int n_qt;     // ceil(T / 128), also the number of key tiles
+  int causal;
+  int rope;     // 0 none, 1 split-half, 2 adjacent
+  int nP;       // units made of head pairs
+  int nUnits;   // all units
+  float scale_log2;
+  RopeTable theta;
+};
+
+struct Unit {
+  int b, kvh;
+  int h[2], q0[2], n[2];  // per tile: head, first row, number of key tiles (n[0] <= n[1])
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+  Unit r;
+  if (u < p.nP) {
+    const int per = p.B * p.Hkv * p.hp;
+    int qt = u / per;
+    int rem = u - qt * per;
+    if (p.causal) qt = p.n_qt - 1 - qt;
+    r.b = rem / (p.Hkv * p.hp);
+    rem -= r.b * (p.Hkv * p.hp);
+    r.kvh = rem / p.hp;
+    const int pp = rem - r.kvh * p.hp;
+    r.h[0] = r.kvh * p.rep + 2 * pp;
+    r.h[1] = r.h[0] + 1;
+    r.q0[0] = r.q0[1] = qt * BM;
+    r.n[0] = r.n[1] = p.causal ? qt + 1 : p.n_qt;
+  } else {
+    const int u2 = u - p.nP;
+    const int npairs = (p.n_qt + 1) / 2;
+    const int per = p.B * p.Hkv;
+    int m = u2 / per;
+    const int rem = u2 - m * per;
+    if (p.causal) m = npairs - 1 - m;
+    r.b = rem / p.Hkv;
+    r.kvh = rem - r.b * p.Hkv;
+    r.h[0] = r.h[1] = r.kvh * p.rep + p.rep - 1;
+    const int t0 = 2 * m, t1 = 2 * m + 1;
+    if (t1 < p.n_qt) {
+      r.q0[0] = t0 * BM;
+      r.n[0] = p.causal ? t0 + 1 : p.n_qt;
+      r.q0[1] = t1 * BM;
+      r.n[1] = p.causal ? t1 + 1 : p.n_qt;
+    } else {
+      r.q0[0] = 0;
+      r.n[0] = 0;
+      r.q0[1] = t0 * BM;
+      r.n[1] = p.causal ? t0 + 1 : p.n_qt;
+    }
+  }
+  return r;
+}
+
+// i-th unit of this CTA: rounds of gridDim.x units, alternating direction.
+__device__ __forceinline__ int unit_index(int i) {
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+  return i * G + ((i & 1) ? (G - 1 - c) : c);
+}
+
+// Byte offset of the 8-element (16-byte) chunk holding element e (e % 8 == 0)
+// of row r in a 128-row tile stored as 128-byte-swizzled column blocks.
+__device__ __forceinline__ uint32_t sw128_off(int r, int e) {
+  const int blk = e >> 6;
+  const int chunk = (e >> 3) & 7;
+  return static_cast<uint32_t>(blk * (BM * 128) + r * 128 + ((chunk ^ (r & 7)) << 4));
+}
+
+// Rotate row r of a Q tile in shared memory in place (RoPE at position pos).
+template <int D>
+__device__ __forceinline__ void rotate_q_row(uint8_t* tile, int r, int pos, int layout,
+                                             const RopeTable& th) {
+#pragma unroll 1
+  for (int c = 0; c < D / 16; ++c) {
+    int e0, e1;
+    if (layout == 1) {
+      e0 = 8 * c;
+      e1 = D / 2 + 8 * c;
+    } else {
+      e0 = 16 * c;
+      e1 = 16 * c + 8;
+    }
+    uint4* p0 = reinterpret_cast<uint4*>(tile + sw128_off(r, e0));
+    uint4* p1 = reinterpret_cast<uint4*>(tile + sw128_off(r, e1));
+    const uint4 a = *p0, b = *p1;
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+    float u[8], w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      u[2 * i] = bf16lo_to_f32(wa[i]);
+      u[2 * i + 1] = bf16hi_to_f32(wa[i]);
+      w[2 * i] = bf16lo_to_f32(wb[i]);
+      w[2 * i + 1] = bf16hi_to_f32(wb[i]);
+    }
+    float cs[8], sn[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rope_cos_sin<false>(pos, th.hi[8 * c + i], th.lo[8 * c + i], cs[i], sn[i]);
+    float ou[8], ow[8];
+    if (layout == 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ou[i] = fmaf(u[i], cs[i], -w[i] * sn[i]);
+        ow[i] = fmaf(u[i], sn[i], w[i] * cs[i]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ou[2 * i] = fmaf(u[2 * i], cs[i], -u[2 * i + 1] * sn[i]);
+        ou[2 * i + 1] = fmaf(u[2 * i], sn[i], u[2 * i + 1] * cs[i]);
+        ow[2 * i] = fmaf(w[2 * i], cs[4 + i], -w[2 * i + 1] * sn[4 + i]);
+        ow[2 * i + 1] = fmaf(w[2 * i], sn[4 + i], w[2 * i + 1] * cs[4 + i]);
+      }
+    }
+    uint4 ra, rb;
+    ra.x = pack_bf16x2(ou[0], ou[1]);
+    ra.y = pack_bf16x2(ou[2], ou[3]);
+    ra.z = pack_bf16x2(ou[4], ou[5]);
+    ra.w = pack_bf16x2(ou[6], ou[7]);
+    rb.x = pack_bf16x2(ow[0], ow[1]);
+    rb.y = pack_bf16x2(ow[2], ow[3]);
+    rb.z = pack_bf16x2(ow[4], ow[5]);
+    rb.w = pack_bf16x2(ow[6], ow[7]);
+    *p0 = ra;
+    *p1 = rb;
+  }
+}
+
+// S = Q K^T: M=128 query rows, N=128 keys, K=D; both operands K-major,
+// 128-byte swizzled; one MMA per 16 channels.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>((kk >> 2) * (BM * 128) + (kk & 3) * 32);
+    umma_ss(d_tmem, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024),
+            Cfg<D>::IDESC_S, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V: M=128, N=D, K=128 keys; P from TMEM, V MN-major (rows = keys).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    umma_ts(d_tmem, p_tmem + 8u * kk, smem_desc_sw128(v_smem + 2048u * kk, BM * 128, 1024),
+            Cfg<D>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_sm103a_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ[2] = {smem, smem + C::TILE_BYTES};
+  uint8_t* sKV = smem + 2 * C::TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_TILE_BYTES);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_ready = bars + 2;
+  uint64_t* q_empty = bars + 4;
+  uint64_t* s_full = bars + 6;
+  uint64_t* p_full = bars + 8;
+  uint64_t* o_full = bars + 10;
+  uint64_t* o_empty = bars + 12;
+  uint64_t* teardown = bars + 14;
+  uint64_t* kv_full = bars + 16;
+  uint64_t* kv_empty = kv_full + C::NS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kv_empty + C::NS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&q_full[x], 1);
+      mbar_init(&q_ready[x], 4);
+      mbar_init(&q_empty[x], 1);
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 4);
+      mbar_init(&o_full[x], 1);
+      mbar_init(&o_empty[x], 4);
+    }
+    mbar_init(teardown, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t fill = 0;
+      uint32_t nq[2] = {0, 0};
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        const int u = unit_index(i);
+        if (u >= p.nUnits) break;
+        const Unit un = decode_unit(p, u);
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (un.n[x] == 0) continue;
+          if (nq[x] > 0 && !mbar_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, p.status, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&q_full[x], C::TILE_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(sQ[x] + kb * C::BLOCK_BYTES, &tm_q, &q_full[x], kb * 64, un.q0[x],
+                        un.b * p.Hq + un.h[x]);
+          ++nq[x];
+        }
+        for (int j = 0; j < un.n[1] && ok; ++j) {
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t s = fill % C::NS, use = fill / C::NS;
+            if (use > 0 && !mbar_wait(&kv_empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
+            uint8_t* dst = sKV + s * C::TILE_BYTES;
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_3d(dst + kb * C::BLOCK_BYTES, t == 0 ? &tm_k : &tm_v, &kv_full[s], kb * 64,
+                          j * BN, un.b * p.Hkv + un.kvh);
+            ++fill;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // Let every copy still in flight land before the CTA's shared memory is released.
+        const uint32_t first = fill > static_cast<uint32_t>(C::NS) ? fill - C::NS : 0u;
+        for (uint32_t f = first; f < fill; ++f)
+          mbar_wait(&kv_full[f % C::NS], (f / C::NS) & 1, nullptr, p.status, kDrainNs);
+        for (int x = 0; x < 2; ++x)
+          if (nq[x] > 0) mbar_wait(&q_full[x], (nq[x] - 1) & 1, nullptr, p.status, kDrainNs);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sKV0 = smem_u32(sKV);
+      const uint32_t sQa[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
+      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t tO[2] = {tmem + 256u, tmem + 256u + static_cast<uint32_t>(D)};
+      uint32_t fill = 0;
+      uint32_t cq[2] = {0, 0}, cp[2] = {0, 0}, cu[2] = {0, 0};
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!ok) return false;
+        ok = mbar_wait(bar, parity, abort_flag, p.status, kWaitNs);
+        tc_fence_after();
+        return ok;
+      };
+      for (int i = 0; ok; ++i) {
+        const int u = unit_index(i);
+        if (u >= p.nUnits) break;
+        const Unit un = decode_unit(p, u);
+        // first score tiles: S_X(0) = Q_X K_0^T
+        const uint32_t s0 = fill % C::NS;
+        bool k0_ready = false;
+        for (int x = 0; x < 2; ++x) {
+          if (un.n[x] == 0) continue;
+          if (!wait(&q_ready[x], cq[x] & 1)) break;
+          ++cq[x];
+          if (!k0_ready) {
+            if (!wait(&kv_full[s0], (fill / C::NS) & 1)) break;
+            k0_ready = true;
+          }
+          issue_qk<D>(tS[x], sQa[x], sKV0 + s0 * C::TILE_BYTES);
+          tc_commit(&s_full[x]);
+          if (un.n[x] == 1) tc_commit(&q_empty[x]);
+        }
+        if (!ok) break;
+        tc_commit(&kv_empty[s0]);
+        for (int j = 0; j < un.n[1] && ok; ++j) {
+          const uint32_t fV = fill + 2 * j + 1, fK = fill + 2 * j + 2;
+          const uint32_t sV = fV % C::NS, sK = fK % C::NS;
+          bool v_ready = false, k_ready = false;
+          for (int x = 0; x < 2; ++x) {
+            if (j >= un.n[x]) continue;
+            if (!wait(&p_full[x], cp[x] & 1)) break;
+            ++cp[x];
+            if (!v_ready) {
+              if (!wait(&kv_full[sV], (fV / C::NS) & 1)) break;
+              v_ready = true;
+            }
+            if (j == 0 && cu[x] > 0) {
+              if (!wait(&o_empty[x], (cu[x] - 1) & 1)) break;
+            }
+            issue_pv<D>(tO[x], tS[x], sKV0 + sV * C::TILE_BYTES, j > 0);
+            if (x == 1) tc_commit(&kv_empty[sV]);
+            if (j == un.n[x] - 1) tc_commit(&o_full[x]);
+            if (j + 1 < un.n[x]) {
+              if (!k_ready) {
+                if (!wait(&kv_full[sK], (fK / C::NS) & 1)) break;
+                k_ready = true;
+              }
+              issue_qk<D>(tS[x], sQa[x], sKV0 + sK * C::TILE_BYTES);
+              tc_commit(&s_full[x]);
+              if (j + 1 == un.n[x] - 1) tc_commit(&q_empty[x]);
+              if (x == 1) tc_commit(&kv_empty[sK]);
+            }
+          }
+        }
+        for (int x = 0; x < 2; ++x)
+          if (un.n[x] > 0) ++cu[x];
+        fill += 2 * un.n[1];
+      }
+      // every MMA issued above has completed once this barrier flips
+      tc_commit(teardown);
+      mbar_wait(teardown, 0, nullptr, p.status, kDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (A: warps 0-3, B: 4-7)
+    const int x = warp >> 2;
+    const int row = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (x == 0 ? 0u : 128u);
+    const uint32_t tO = tmem + lane_off + 256u + (x == 0 ? 0u : static_cast<uint32_t>(D));
+    const float sl2 = p.scale_log2;
+    uint32_t cq = 0, cs = 0, co = 0;
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+      const int u = unit_index(i);
+      if (u >= p.nUnits) break;
+      const Unit un = decode_unit(p, u);
+      const int n = un.n[x];
+      if (n == 0) continue;
+      const int qpos = un.q0[x] + row;
+      if (!mbar_wait(&q_full[x], cq & 1, abort_flag, p.status, kWaitNs)) break;
+      ++cq;
+      if (p.rope) {
+        rotate_q_row<D>(sQ[x], row, qpos, p.rope, p.theta);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready[x]);
+
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        if (!mbar_wait(&s_full[x], cs & 1, abort_flag, p.status, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        ++cs;
+        tc_fence_after();
+        float s[BN];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            tmem_ld32_sync(tS + 32u * c, r);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) s[32 * c + t] = __uint_as_float(r[t]);
+          }
+        }
+        // causal diagonal and ragged tail: keys beyond the row's limit get -inf
+        int lim = BN - 1;
+        if (p.causal) lim = min(lim, qpos - j * BN);
+        lim = min(lim, p.T - 1 - j * BN);
+        if (lim < BN - 1) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+        }
+        float mx = fmax3(s[0], s[1], s[2]);
+#pragma unroll
+        for (int c = 3; c + 1 < BN; c += 2) mx = fmax3(mx, s[c], s[c + 1]);
+        mx = fmaxf(mx, s[BN - 1]);
+        const float m_new = fmaxf(m_used, mx * sl2);
+        if (j == 0) {
+          m_used = m_new;
+        } else if (m_new > m_used + kRescaleThreshold) {
+          const float f = ex2_approx(m_used - m_new);
+          l *= f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32_sync(tO + 32u * c, r);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * f);
+            tmem_st32(tO + 32u * c, r);
+          }
+          tmem_st_wait();
+          m_used = m_new;
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            const float p0 = ex2_approx(fmaf(s[64 * c + 2 * t], sl2, -m_used));
+            const float p1 = ex2_approx(fmaf(s[64 * c + 2 * t + 1], sl2, -m_used));
+            sum += p0 + p1;
+            pk[t] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + 32u * c, pk);
+        }
+        l += sum;
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[x]);
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16 rows of out; optional natural-log LSE
+      if (!mbar_wait(&o_full[x], co & 1, abort_flag, p.status, kWaitNs)) break;
+      ++co;
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool live = qpos < p.T;
+      __nv_bfloat16* orow =
+          p.out + ((static_cast<size_t>(un.b) * p.Hq + un.h[x]) * p.T + (live ? qpos : 0)) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32_sync(tO + 32u * c, r);
+        uint32_t w[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+          w[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * inv, __uint_as_float(r[2 * t + 1]) * inv);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        }
+      }
+      if (live && p.lse != nullptr)
+        p.lse[(static_cast<size_t>(un.b) * p.Hq + un.h[x]) * p.T + qpos] =
+            (m_used + log2f(l)) * 0.69314718055994531f;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_empty[x]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
+  using C = Cfg<D>;
+  Params p{};
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.status = a.status;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.T = a.T;
+  p.rep = a.Hq / a.Hkv;
+  p.hp = p.rep / 2;
+  p.n_qt = (a.T + BM - 1) / BM;
+  p.causal = a.causal;
+  p.rope = a.rope;
+  p.nP = p.n_qt * a.B * a.Hkv * p.hp;
+  const int nC = (p.rep & 1) ? ((p.n_qt + 1) / 2) * a.B * a.Hkv : 0;
+  p.nUnits = p.nP + nC;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.theta = a.theta;
+
+  alignas(64) CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16_3d(&tq, a.q, D, a.T, a.B * a.Hq, BM) ||
+      !make_tmap_bf16_3d(&tk, k_eff, D, a.T, a.B * a.Hkv, BN) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.T, a.B * a.Hkv, BN))
+    return cudaErrorInvalidValue;
+
+  cudaError_t e = cudaFuncSetAttribute(fwd_sm103a_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int grid = p.nUnits < a.num_sms ? p.nUnits : a.num_sms;
+  fwd_sm103a_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_sm103a(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return launch_d<64>(a, k_eff, stream);
+    case 128: return launch_d<128>(a, k_eff, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace csattn

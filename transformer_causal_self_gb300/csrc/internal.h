@@ -1,0 +1,67 @@
+// Host-side interfaces between the C-ABI layer (csattn_api.cu) and the kernel
+// translation units.  Launchers validate nothing: csattn_api.cu has already
+// checked every argument.  They return a cudaError_t from the launch.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace csattn {
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  int B, Hq, Hkv, T, d;
+  int causal;
+  int rope;          // 0 none, 1 split-half, 2 adjacent
+  float scale;       // > 0
+  RopeTable theta;   // valid when rope != 0
+  uint32_t* status;  // device status word
+  int num_sms;
+};
+
+// fp32 SIMT path (any d in {16,32,64,128}).
+cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t stream);
+
+// bf16 path: x_rot = RoPE(x) for x [B, H, T, d] bf16 (rope 1 split-half, 2 adjacent).
+cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, int T, int d,
+                                    int rope, const RopeTable& theta, cudaStream_t stream);
+
+// bf16 tcgen05 prefill; `k_eff` is k itself or its rotated copy.
+cudaError_t launch_fwd_sm103a(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* seq_lens;
+  void* out;
+  int B, Hq, Hkv, Lmax, d;
+  float scale;
+  int max_seq_len;
+  int chunk;       // keys per split, multiple of 64
+  int n_splits;    // ceil(max_seq_len / chunk)
+  float* part_o;   // [B, Hq, n_splits, d]
+  float* part_ml;  // [B, Hq, n_splits, 2]
+  uint32_t* status;
+};
+
+cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+// Driver entry point for cuTensorMapEncodeTiled (nullptr if unavailable).
+void* tensor_map_encoder();
+
+// 3-D bf16 tensor map over rows of `d` elements: dims {d, rows, planes},
+// box {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
+bool make_tmap_bf16_3d(void* tmap_out, const void* base, int d, int rows, int planes,
+                       int box_rows);
+
+}  // namespace csattn
