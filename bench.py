@@ -1,0 +1,459 @@
+"""Benchmark of the causal GQA attention hot path on GB300.
+
+One step = the whole hot path once:
+  * prefill of the Llama-style GQA workload (B=4, Hq=32, Hkv=8, T=4096,
+    d=128, RoPE base 1e4, bf16): RoPE pass over the keys, then the tcgen05
+    attention kernel (q rotated in-kernel);
+  * KV-cache decode of the decode workload (B=64, Hq=32, Hkv=8, d=128,
+    L ~ U[512, 8192], Lmax=8192, bf16): split-KV kernel plus merge.
+value = prefill TFLOP/s with causal FLOPs 2*B*Hq*T^2*d; the decode GB/s
+(K+V bytes actually visible, 2*Hkv*L_b*d*2 per sequence) is reported beside
+it.  Inputs are resident in HBM; every step streams > 1.4 GB, far more than
+the 129 MB L2, so no flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 run under torch.distributed.run: every rank runs the same single-GPU
+replica (the path needs no exchange step), value = sum over ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd TFLOP/s (bf16 GQA T=4096) & decode HBM GB/s, % roofline"
+PREFILL = "llama_gqa_bf16"
+DECODE = "decode_bf16"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"csattn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv",
+                                          "-lms", "200", "-i", str(self.gpu)], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        with open(self.path) as f:
+            rows = list(csv.reader(io.StringIO(f.read())))
+        if len(rows) < 2:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        hdr = [h.strip() for h in rows[0]]
+        data = [dict(zip(hdr, [c.strip() for c in r])) for r in rows[1:] if len(r) == len(hdr)]
+
+        def num(s):
+            try:
+                return float(s.split()[0])
+            except (ValueError, IndexError):
+                return None
+        sm = [num(r.get("clocks.current.sm [MHz]", r.get("clocks.sm [MHz]", ""))) for r in data]
+        mx = [num(r.get("clocks.max.sm [MHz]", "")) for r in data]
+        pw = [num(r.get("power.draw [W]", "")) for r in data]
+        sm = [x for x in sm if x is not None]
+        mx = [x for x in mx if x is not None]
+        pw = [x for x in pw if x is not None]
+        reasons = set()
+        for r in data:
+            for key, name in (("clocks_event_reasons.hw_slowdown", "hw_slowdown"),
+                              ("clocks_event_reasons.hw_thermal_slowdown", "hw_thermal_slowdown"),
+                              ("clocks_event_reasons.sw_thermal_slowdown", "sw_thermal_slowdown"),
+                              ("clocks_event_reasons.sw_power_cap", "sw_power_cap")):
+                if r.get(key, "").lower().startswith("active"):
+                    reasons.add(name)
+        loaded = [x for x, p in zip(sm, pw) if p is not None and p > 200] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons)}
+
+
+def _source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "transformer_causal_self_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if it is for this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[kernel_file]
+        if e.get("source_sha") == _source_hash(kernel_file, "common.cuh"):
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
+        pass
+    return None
+
+
+def _decode_bytes(seq_lens, w):
+    return float(sum(2 * w.Hkv * int(L) * w.d * 2 for L in seq_lens))
+
+
+# ------------------------------------------------------------------------ CPU oracle legs
+
+def _oracle_prefill_sample(q, k, v, w, budget_s):
+    """Time the oracle on whole (b, h) heads of the prefill until budget_s; TFLOP/s."""
+    from oracle import attn as OA
+    import numpy as np
+    flops = 0.0
+    heads = 0
+    t0 = time.perf_counter()
+    rows = np.arange(w.T)
+    for b in range(w.B):
+        for h in range(w.Hq):
+            OA.attention_rows(q, k, v, b, h, rows, causal=True, rope_base=w.rope_base,
+                              scale=w.scale, operand_dtype="bf16")
+            flops += 2.0 * w.T * w.T * w.d
+            heads += 1
+            if time.perf_counter() - t0 >= budget_s:
+                dt = time.perf_counter() - t0
+                return flops / dt / 1e12, heads, dt
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, heads, dt
+
+
+def _cores():
+    n = os.cpu_count() or 1
+    try:
+        from threadpoolctl import threadpool_info
+        th = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if th:
+            return int(th[0])
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return n
+
+
+def run_reference(args):
+    """The reference arm: the float64 CPU oracle, timed on this host's cores."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import attn_workloads as W
+    w = W.WORKLOADS[PREFILL]
+    q, k, v = W.make_prefill_inputs(w)
+    budget = 3.0
+    for _ in range(args.warmup):
+        _oracle_prefill_sample(q, k, v, w, budget_s=0.1)
+    vals, times = [], []
+    heads_total = 0
+    for _ in range(args.steps):
+        tf, heads, dt = _oracle_prefill_sample(q, k, v, w, budget_s=budget)
+        vals.append(tf)
+        times.append(dt)
+        heads_total += heads
+    value = statistics.median(vals)
+    cores = _cores()
+    sample = (f"{heads_total} whole (b, h) heads of {PREFILL} over {args.steps} steps "
+              f"(~{budget:.0f} s each), float64 numpy, causal FLOPs 2*T^2*d per head")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1000 * statistics.mean(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{PREFILL} (B=4, Hq=32, Hkv=8, T=4096, d=128, RoPE 1e4) "
+                                   "sampled by whole heads", "parallelism": "none"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import attn_workloads as W
+    import transformer_causal_self_gb300 as csattn
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hbm_peak, tf_burst, tf_sust, peak_kind = _peaks()
+
+    wp = W.WORKLOADS[PREFILL]
+    wd = W.WORKLOADS[DECODE]
+    q_h, k_h, v_h = W.make_prefill_inputs(wp)
+    qd_h, kc_h, vc_h, lens_h = W.make_decode_inputs(wd)
+    max_len = int(lens_h.max())
+
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    out = torch.empty_like(q)
+    k_rot = torch.empty_like(k)
+    qd, kc, vc, lens = qd_h.to(dev), kc_h.to(dev), vc_h.to(dev), lens_h.to(dev)
+    outd = torch.empty_like(qd)
+    ws_dec = torch.empty(csattn.decode_workspace_size(wd.B, wd.Hq, wd.Lmax, wd.d, 0),
+                         dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        csattn.rope_rotate(k, k_rot, rope_base=wp.rope_base, stream=stream)
+        if evs:
+            evs[1].record(stream)
+        csattn.attn_fwd(q, k_rot, v, out, causal=True, rope_base=wp.rope_base, scale=wp.scale,
+                        k_prerotated=True, stream=stream)
+        if evs:
+            evs[2].record(stream)
+        csattn.attn_decode(qd, kc, vc, lens, outd, scale=wd.scale, max_seq_len=max_len,
+                           workspace=ws_dec, stream=stream)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    csattn.check_status(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        _barrier(world)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            step(evs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        _barrier(world)
+    csattn.check_status(stream)
+    launches = 4 * args.steps  # rope, attention, decode split, decode merge
+
+    rope_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    total_ms = _max_over_ranks(sum(step_ms), world)
+    pre_ms = _max_over_ranks(sum(r + f for r, f in zip(rope_ms, fwd_ms)), world) / args.steps
+    fwd_avg = _max_over_ranks(sum(fwd_ms), world) / args.steps
+    dec_avg = _max_over_ranks(sum(dec_ms), world) / args.steps
+
+    flops = wp.flops()
+    dbytes = _decode_bytes(lens_h.tolist(), wd)
+    value = world * flops / (pre_ms * 1e-3) / 1e12
+    fwd_tflops = flops / (fwd_avg * 1e-3) / 1e12
+    dec_gbs = world * dbytes / (dec_avg * 1e-3) / 1e9
+    dec_gbs_one = dbytes / (dec_avg * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    e2e = None
+    if rank == 0 or world > 1:
+        pin = lambda t: t.pin_memory()  # noqa: E731
+        hq, hk, hv = pin(q_h), pin(k_h), pin(v_h)
+        hqd, hkc, hvc, hl = pin(qd_h), pin(kc_h), pin(vc_h), pin(lens_h)
+        ho, hod = torch.empty_like(hq).pin_memory(), torch.empty_like(hqd).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hkc, hvc, hl))
+        d2h = ho.numel() * ho.element_size() + hod.numel() * hod.element_size()
+        e_steps = max(1, min(args.steps, 5))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e_steps)]
+        torch.cuda.synchronize()
+        for i in range(e_steps):
+            ev[i][0].record(stream)
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            csattn.attn_fwd(q, k, v, out, causal=True, rope_base=wp.rope_base, scale=wp.scale,
+                            workspace=k_rot.view(torch.uint8).view(-1), stream=stream)
+            ho.copy_(out, non_blocking=True)
+            ev[i][1].record(stream)
+            qd.copy_(hqd, non_blocking=True)
+            kc.copy_(hkc, non_blocking=True)
+            vc.copy_(hvc, non_blocking=True)
+            lens.copy_(hl, non_blocking=True)
+            csattn.attn_decode(qd, kc, vc, lens, outd, scale=wd.scale, max_seq_len=max_len,
+                               workspace=ws_dec, stream=stream)
+            hod.copy_(outd, non_blocking=True)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        csattn.check_status(stream)
+        e_pre = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        e_dec = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        e2e = {"value": round(world * flops / (e_pre * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_pre + e_dec, 3),
+               "decode": {"value": round(world * dbytes / (e_dec * 1e-3) / 1e9, 1),
+                          "unit": "GB/s"},
+               "note": "pinned host buffers; H2D of q,k,v (+ decode q, K/V cache, seq_lens) "
+                       "and D2H of both outputs inside each timed step"}
+
+    if rank != 0:
+        return 0
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        tf, heads, dt = _oracle_prefill_sample(q_h, k_h, v_h, wp, budget_s=args.cpu_budget)
+        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+               "sample": f"{heads} whole (b, h) heads of {PREFILL}, float64 numpy, "
+                         f"{dt:.1f} s, causal FLOPs 2*T^2*d per head"}
+
+    roof = {"bound": "tensor", "achieved": round(fwd_tflops, 2), "peak": tf_burst,
+            "unit": "TFLOP/s", "frac": round(fwd_tflops / tf_burst, 4),
+            "traffic": _traffic("fwd_sm103a.cu"),
+            "kernel": "fwd_sm103a_kernel<128>",
+            "peak_kind": f"{peak_kind} bf16 dense burst (cuBLAS)",
+            "frac_of_sustained": round(fwd_tflops / tf_sust, 4),
+            "frac_of_spec_2250": round(fwd_tflops / 2250.0, 4)}
+    dec_roof = {"bound": "hbm", "achieved": round(dec_gbs_one, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(dec_gbs_one / hbm_peak, 4), "traffic": _traffic("decode.cu"),
+                "kernel": "decode_bf16_kernel<128> + decode_combine_kernel",
+                "peak_kind": f"{peak_kind} HBM copy", "frac_of_spec_8000": round(dec_gbs_one / 8000.0, 4)}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs, decode lengths U[512,8192])",
+        "config": {"workload": f"{PREFILL} prefill (B=4, Hq=32, Hkv=8, T=4096, d=128, RoPE 1e4) + "
+                               f"{DECODE} (B=64, Hq=32, Hkv=8, d=128, Lmax=8192)",
+                   "l2": "inputs larger than L2: each step streams > 1.4 GB (no flush)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "prefill_ms": round(pre_ms, 4), "rope_ms": round(statistics.mean(rope_ms), 4),
+        "attn_kernel_ms": round(fwd_avg, 4),
+        "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "ms": round(dec_avg, 4),
+                   "bytes_per_step": dbytes, "roofline": dec_roof},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clocks.summary(), "wall_s_timed": round(t_wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_profile_case(args):
+    """A short program for ncu: one warm-up and one timed launch of one kernel group.
+
+    fwd:    the llama_gqa_bf16 prefill (RoPE pass + attention kernel), full size.
+    decode: the decode_bf16 workload with B=16 sequences (0.5 GB of cache).
+    """
+    import torch
+
+    import attn_workloads as W
+    import transformer_causal_self_gb300 as csattn
+    dev = torch.device("cuda", 0)
+    if args.profile == "fwd":
+        w = W.WORKLOADS[PREFILL]
+        q, k, v = (t.to(dev) for t in W.make_prefill_inputs(w))
+        k_rot = torch.empty_like(k)
+        out = torch.empty_like(q)
+        for _ in range(2):
+            csattn.rope_rotate(k, k_rot, rope_base=w.rope_base)
+            csattn.attn_fwd(q, k_rot, v, out, causal=True, rope_base=w.rope_base, scale=w.scale,
+                            k_prerotated=True)
+    else:
+        w = W.WORKLOADS[DECODE].with_(B=16)
+        qd, kc, vc, lens = W.make_decode_inputs(w)
+        qd, kc, vc, lens_d = qd.to(dev), kc.to(dev), vc.to(dev), lens.to(dev)
+        for _ in range(2):
+            csattn.attn_decode(qd, kc, vc, lens_d, scale=w.scale, max_seq_len=int(lens.max()))
+    csattn.check_status()
+    print(json.dumps({"profile_case": args.profile, "ok": True}))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="csattn", choices=["csattn", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["fwd", "decode"], default=None,
+                    help="run a short single-kernel case for ncu instead of the benchmark")
+    args = ap.parse_args()
+    if args.profile:
+        return run_profile_case(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

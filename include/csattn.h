@@ -59,6 +59,10 @@ typedef enum { CSATTN_F32 = 0, CSATTN_BF16 = 1 } csattn_dtype;
 
 typedef enum { CSATTN_ROPE_SPLIT_HALF = 0, CSATTN_ROPE_ADJACENT = 1 } csattn_rope_layout;
 
+/* OR into rope_layout of csattn_attn_fwd: k is already rotated (for instance
+ * by csattn_rope_rotate, as a KV cache stores it); only q is rotated. */
+#define CSATTN_ROPE_K_PREROTATED 0x100
+
 /*
  * Bytes of device workspace csattn_attn_fwd needs for these arguments.
  * Non-zero only for bf16 with RoPE (rope_base > 0): the rotated keys,
@@ -78,7 +82,8 @@ size_t csattn_fwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype
  *   rope_base    > 0: RoPE with theta_p = rope_base^(-2p/d) at positions
  *                0..T-1 on q and k; <= 0: no RoPE.
  *   rope_layout  CSATTN_ROPE_SPLIT_HALF (channel p with p + d/2) or
- *                CSATTN_ROPE_ADJACENT (channel 2p with 2p+1).
+ *                CSATTN_ROPE_ADJACENT (channel 2p with 2p+1), optionally OR
+ *                CSATTN_ROPE_K_PREROTATED (k given rotated; no workspace needed).
  *   scale        > 0: logit scale; <= 0: 1/sqrt(d).
  *   lse          NULL, or fp32 [B, Hq, T]: natural-log log-sum-exp of each
  *                scaled, masked score row.
@@ -92,6 +97,16 @@ int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int 
                     int Hkv, int T, int d, int dtype, int causal, float rope_base,
                     int rope_layout, float scale, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream);
+
+/*
+ * RoPE of x [B, H, T, d] into x_rot (same shape; must not overlap x), at
+ * positions 0..T-1 with theta_p = rope_base^(-2p/d), rounded to the input
+ * dtype.  This is the rotation csattn_attn_fwd applies to its keys, exposed to
+ * build a rotated KV cache for csattn_attn_decode.  dtype must be CSATTN_BF16;
+ * d in {64, 128}; rope_base > 0; T <= 49152.
+ */
+int csattn_rope_rotate(const void* x, void* x_rot, int B, int H, int T, int d, int dtype,
+                       float rope_base, int rope_layout, void* stream);
 
 /*
  * Bytes of device workspace csattn_attn_decode needs: fp32 partial results

@@ -40,13 +40,25 @@ def test_decode_groups_and_lengths(Hq, Hkv, d):
 
 
 def test_decode_split_count_invariance():
+    """Results agree across split counts within bf16 rounding.
+
+    Each split rounds its P = 2^(x - m_s) to bf16 against its own running max
+    m_s, so two split counts see independent P rounding: about 2^-9/sqrt(3)
+    relative noise per weight, which reaches the output at ~1e-3 relative and
+    at sqrt(2) times that between two runs.  The bound is therefore the bf16
+    parity bound (max-abs 2e-2, rel-L2 5e-3), and each result is also held to
+    the oracle.
+    """
     w = W.WORKLOADS["decode_bf16"].with_(B=8, Lmax=4096, Lmin=512)
     q, kc, vc, sl = W.make_decode_inputs(w)
+    ref = OA.decode(q, kc, vc, sl.numpy(), scale=w.scale)
     outs = [to_np(_decode(q, kc, vc, sl, scale=w.scale, max_seq_len=4096, num_splits=s))
             for s in (1, 4, 7, 64)]
-    for o in outs[1:]:
-        assert np.max(np.abs(o - outs[0])) <= 1e-2
-        assert np.linalg.norm(o - outs[0]) / np.linalg.norm(outs[0]) <= 1e-3
+    for s, o in zip((1, 4, 7, 64), outs):
+        assert_bf16_close(o, ref, f"splits={s}")
+        err = np.max(np.abs(o - outs[0]))
+        rl2 = np.linalg.norm(o - outs[0]) / np.linalg.norm(outs[0])
+        assert err <= 2e-2 and rl2 <= 5e-3, (s, err, rl2)
 
 
 def test_decode_matches_prefill_last_row():

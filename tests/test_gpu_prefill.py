@@ -31,10 +31,17 @@ def test_tiny_fp32_workload(layout):
     assert_f32_close(to_np(out), ref, f"tiny fp32 {layout}")
 
 
-@pytest.mark.parametrize("d", [16, 32, 64, 128])
-@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 1), (6, 2)])
-@pytest.mark.parametrize("T", [1, 37, 200])
-@pytest.mark.parametrize("causal", [True, False])
+FP32_CASES = [
+    # (d, Hq, Hkv, T, causal)
+    (16, 2, 2, 1, True), (16, 4, 1, 37, True), (16, 6, 2, 200, False),
+    (32, 2, 2, 37, True), (32, 6, 2, 200, True), (32, 4, 1, 1, False),
+    (64, 4, 1, 200, True), (64, 2, 2, 37, False), (64, 6, 2, 129, True),
+    (128, 2, 2, 200, True), (128, 6, 2, 37, False), (128, 4, 1, 1, True),
+    (128, 4, 4, 97, True),
+]
+
+
+@pytest.mark.parametrize("d,hq,hkv,T,causal", FP32_CASES)
 def test_fp32_shapes(d, hq, hkv, T, causal):
     base = 10000.0 if (d + T) % 2 == 0 else 0.0
     w = W.PrefillWorkload("f32case", B=2, Hq=hq, Hkv=hkv, T=T, d=d, dtype="f32", rope_base=base,

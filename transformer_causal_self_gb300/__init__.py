@@ -14,7 +14,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "CsattnError", "library_path", "load_library", "attn_fwd", "attn_decode",
+    "CsattnError", "library_path", "load_library", "attn_fwd", "attn_decode", "rope_rotate",
     "fwd_workspace_size", "decode_workspace_size", "check_status",
     "selftest_bounded_wait", "EXPORTED_SYMBOLS",
 ]
@@ -23,6 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB: Optional[ctypes.CDLL] = None
 
 CSATTN_F32, CSATTN_BF16 = 0, 1
+K_PREROTATED = 0x100
 _ROPE_LAYOUT = {"split_half": 0, "adjacent": 1}
 _STATUS = {0: "CSATTN_OK", -1: "CSATTN_ERR_INVALID_ARG", -2: "CSATTN_ERR_UNSUPPORTED",
            -3: "CSATTN_ERR_CUDA", -4: "CSATTN_ERR_TIMEOUT", -5: "CSATTN_ERR_WORKSPACE",
@@ -35,6 +36,7 @@ _SIGNATURES = {
     "csattn_fwd_workspace_size": (_c_size, [_c_int] * 6 + [_c_float]),
     "csattn_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _c_float,
                                                                         _vp, _vp, _c_size, _vp]),
+    "csattn_rope_rotate": (_c_int, [_vp, _vp] + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "csattn_decode_workspace_size": (_c_size, [_c_int] * 5),
     "csattn_attn_decode": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp,
                                                                 _c_size, _vp]),
@@ -111,10 +113,25 @@ def decode_workspace_size(B, Hq, Lmax, d, num_splits: int = 0) -> int:
     return int(load_library().csattn_decode_workspace_size(B, Hq, Lmax, d, num_splits))
 
 
+def rope_rotate(x: torch.Tensor, out: Optional[torch.Tensor] = None, *, rope_base: float,
+                rope_layout: str = "split_half", stream=None) -> torch.Tensor:
+    """RoPE of x [B,H,T,d] (bf16) at positions 0..T-1 (C: csattn_rope_rotate)."""
+    _need_cuda(x)
+    B, H, T, d = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _need_cuda(out)
+    _check(load_library().csattn_rope_rotate(x.data_ptr(), out.data_ptr(), B, H, T, d,
+                                             _dtype_code(x), float(rope_base),
+                                             _ROPE_LAYOUT[rope_layout], _stream_handle(stream)))
+    return out
+
+
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: Optional[torch.Tensor] = None,
              *, causal: bool = True, rope_base: float = 0.0, scale: float = 0.0,
              rope_layout: str = "split_half", lse: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+             workspace: Optional[torch.Tensor] = None, k_prerotated: bool = False,
+             stream=None) -> torch.Tensor:
     """out = softmax(RoPE(q) RoPE(k)^T * scale + M) v  (C: csattn_attn_fwd).
 
     q [B,Hq,T,d], k/v [B,Hkv,T,d] (bf16 or fp32, contiguous, CUDA).  scale <= 0
@@ -129,7 +146,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: Optional[to
     _need_cuda(out)
     if lse is not None:
         _need_cuda(lse)
-    need = fwd_workspace_size(B, Hq, Hkv, T, d, q.dtype, rope_base)
+    need = 0 if k_prerotated else fwd_workspace_size(B, Hq, Hkv, T, d, q.dtype, rope_base)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
@@ -137,7 +154,8 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: Optional[to
     lib = load_library()
     _check(lib.csattn_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv,
                                T, d, _dtype_code(q), int(bool(causal)), float(rope_base),
-                               _ROPE_LAYOUT[rope_layout], float(scale),
+                               _ROPE_LAYOUT[rope_layout] | (K_PREROTATED if k_prerotated else 0),
+                               float(scale),
                                lse.data_ptr() if lse is not None else None, ws_ptr, ws_bytes,
                                _stream_handle(stream)))
     return out

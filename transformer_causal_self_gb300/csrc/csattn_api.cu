@@ -161,6 +161,8 @@ int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int 
     return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: unknown dtype %d", dtype);
   if (causal != 0 && causal != 1)
     return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: causal must be 0 or 1");
+  const bool k_prerotated = (rope_layout & CSATTN_ROPE_K_PREROTATED) != 0;
+  rope_layout &= ~CSATTN_ROPE_K_PREROTATED;
   if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
     return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: unknown rope_layout %d", rope_layout);
   if (!std::isfinite(rope_base) || !std::isfinite(scale))
@@ -179,7 +181,8 @@ int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int 
     return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: q, k, v, out must be 16-byte aligned");
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: lse must be 4-byte aligned");
-  const size_t need = csattn_fwd_workspace_size(B, Hq, Hkv, T, d, dtype, rope_base);
+  const size_t need =
+      k_prerotated ? 0 : csattn_fwd_workspace_size(B, Hq, Hkv, T, d, dtype, rope_base);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
     return fail(CSATTN_ERR_WORKSPACE,
                 "attn_fwd: needs a 16-byte aligned workspace of %zu bytes (got %zu)", need,
@@ -198,6 +201,7 @@ int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int 
   a.d = d;
   a.causal = causal;
   a.rope = rope_base > 0.f ? (rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2) : 0;
+  a.rope_k = (a.rope != 0 && !k_prerotated) ? 1 : 0;
   a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   if (a.rope) rope_table(&a.theta, d, static_cast<double>(rope_base));
   int rc = device_info(&a.status, &a.num_sms);
@@ -213,13 +217,44 @@ int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int 
   if (tensor_map_encoder() == nullptr)
     return fail(CSATTN_ERR_CUDA, "attn_fwd: cuTensorMapEncodeTiled is unavailable");
   const void* k_eff = k;
-  if (a.rope) {
+  if (a.rope_k) {
     e = launch_rope_rotate_bf16(k, workspace, B, Hkv, T, d, a.rope, a.theta, st);
     if (e != cudaSuccess) return fail_cuda(e, "attn_fwd: RoPE kernel launch");
     k_eff = workspace;
   }
   e = launch_fwd_sm103a(a, k_eff, st);
   if (e != cudaSuccess) return fail_cuda(e, "attn_fwd: sm_103a kernel launch");
+  return CSATTN_OK;
+}
+
+int csattn_rope_rotate(const void* x, void* x_rot, int B, int H, int T, int d, int dtype,
+                       float rope_base, int rope_layout, void* stream) {
+  if (x == nullptr || x_rot == nullptr)
+    return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: null pointer argument");
+  if (B < 1 || H < 1 || T < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: B=%d H=%d T=%d must be >= 1", B, H, T);
+  if (dtype != CSATTN_BF16)
+    return fail(dtype == CSATTN_F32 ? CSATTN_ERR_UNSUPPORTED : CSATTN_ERR_INVALID_ARG,
+                "rope_rotate: only bf16 is implemented (dtype %d)", dtype);
+  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "rope_rotate: d=%d", d);
+  if (!(rope_base > 0.f) || !std::isfinite(rope_base))
+    return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: rope_base must be finite and > 0");
+  if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
+    return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: unknown rope_layout %d", rope_layout);
+  if (T > kMaxRopePositions)
+    return fail(CSATTN_ERR_UNSUPPORTED, "rope_rotate: T <= %d, got %d", kMaxRopePositions, T);
+  if (!aligned16(x) || !aligned16(x_rot))
+    return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: x, x_rot must be 16-byte aligned");
+  const size_t bytes = static_cast<size_t>(B) * H * T * d * 2;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(x), b0 = reinterpret_cast<uintptr_t>(x_rot);
+  if (a0 < b0 + bytes && b0 < a0 + bytes)
+    return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: x and x_rot overlap");
+  RopeTable th;
+  rope_table(&th, d, static_cast<double>(rope_base));
+  cudaError_t e = launch_rope_rotate_bf16(x, x_rot, B, H, T, d,
+                                          rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2, th,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "rope_rotate: kernel launch");
   return CSATTN_OK;
 }
 

@@ -47,7 +47,8 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const float* __restri
                                                            float* __restrict__ out,
                                                            float* __restrict__ lse, int Hq,
                                                            int Hkv, int T, int causal, int rope,
-                                                           float scale, RopeTable theta) {
+                                                           int rope_k, float scale,
+                                                           RopeTable theta) {
   using C = F32Cfg<D>;
   __shared__ float sq[C::ROWS * D];
   __shared__ float sk[C::KT * D];
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const float* __restri
       sv[e] = ok ? vh[(size_t)(k0 + r) * D + (e % D)] : 0.f;
     }
     __syncthreads();
-    if (rope) {
+    if (rope_k) {
       for (int e = tid; e < nk * (D / 2); e += kThreads) {
         const int r = e / (D / 2);
         rotate_row_f32(sk + r * D, D, e % (D / 2), rope, k0 + r, theta);
@@ -144,7 +145,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   fwd_f32_kernel<D><<<grid, kThreads, 0, stream>>>(
       static_cast<const float*>(a.q), static_cast<const float*>(a.k),
       static_cast<const float*>(a.v), static_cast<float*>(a.out), a.lse, a.Hq, a.Hkv, a.T,
-      a.causal, a.rope, a.scale, a.theta);
+      a.causal, a.rope, a.rope_k, a.scale, a.theta);
   return cudaGetLastError();
 }
 

@@ -282,17 +282,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = unit_index(i);
         if (u >= p.nUnits) break;
         const Unit un = decode_unit(p, u);
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (un.n[x] == 0) continue;
-          if (nq[x] > 0 && !mbar_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, p.status, kWaitNs)) {
-            ok = false;
-            break;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (ok && un.n[x] > 0) {
+            if (nq[x] > 0 &&
+                !mbar_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, p.status, kWaitNs)) {
+              ok = false;
+            } else {
+              mbar_arrive_expect_tx(&q_full[x], C::TILE_BYTES);
+#pragma unroll
+              for (int kb = 0; kb < C::KB; ++kb)
+                tma_load_3d(sQ[x] + kb * C::BLOCK_BYTES, &tm_q, &q_full[x], kb * 64, un.q0[x],
+                            un.b * p.Hq + un.h[x]);
+              ++nq[x];
+            }
           }
-          mbar_arrive_expect_tx(&q_full[x], C::TILE_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(sQ[x] + kb * C::BLOCK_BYTES, &tm_q, &q_full[x], kb * 64, un.q0[x],
-                        un.b * p.Hq + un.h[x]);
-          ++nq[x];
         }
         for (int j = 0; j < un.n[1] && ok; ++j) {
           for (int t = 0; t < 2; ++t) {
@@ -342,17 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // first score tiles: S_X(0) = Q_X K_0^T
         const uint32_t s0 = fill % C::NS;
         bool k0_ready = false;
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (un.n[x] == 0) continue;
-          if (!wait(&q_ready[x], cq[x] & 1)) break;
-          ++cq[x];
-          if (!k0_ready) {
-            if (!wait(&kv_full[s0], (fill / C::NS) & 1)) break;
-            k0_ready = true;
+          if (un.n[x] > 0 && wait(&q_ready[x], cq[x] & 1)) {
+            ++cq[x];
+            if (!k0_ready) k0_ready = wait(&kv_full[s0], (fill / C::NS) & 1);
+            if (k0_ready) {
+              issue_qk<D>(tS[x], sQa[x], sKV0 + s0 * C::TILE_BYTES);
+              tc_commit(&s_full[x]);
+              if (un.n[x] == 1) tc_commit(&q_empty[x]);
+            }
           }
-          issue_qk<D>(tS[x], sQa[x], sKV0 + s0 * C::TILE_BYTES);
-          tc_commit(&s_full[x]);
-          if (un.n[x] == 1) tc_commit(&q_empty[x]);
         }
         if (!ok) break;
         tc_commit(&kv_empty[s0]);
@@ -360,32 +364,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fV = fill + 2 * j + 1, fK = fill + 2 * j + 2;
           const uint32_t sV = fV % C::NS, sK = fK % C::NS;
           bool v_ready = false, k_ready = false;
+#pragma unroll
           for (int x = 0; x < 2; ++x) {
-            if (j >= un.n[x]) continue;
-            if (!wait(&p_full[x], cp[x] & 1)) break;
-            ++cp[x];
-            if (!v_ready) {
-              if (!wait(&kv_full[sV], (fV / C::NS) & 1)) break;
-              v_ready = true;
-            }
-            if (j == 0 && cu[x] > 0) {
-              if (!wait(&o_empty[x], (cu[x] - 1) & 1)) break;
-            }
-            issue_pv<D>(tO[x], tS[x], sKV0 + sV * C::TILE_BYTES, j > 0);
-            if (x == 1) tc_commit(&kv_empty[sV]);
-            if (j == un.n[x] - 1) tc_commit(&o_full[x]);
-            if (j + 1 < un.n[x]) {
-              if (!k_ready) {
-                if (!wait(&kv_full[sK], (fK / C::NS) & 1)) break;
-                k_ready = true;
+            if (j < un.n[x] && wait(&p_full[x], cp[x] & 1)) {
+              ++cp[x];
+              if (!v_ready) v_ready = wait(&kv_full[sV], (fV / C::NS) & 1);
+              if (v_ready && (j > 0 || cu[x] == 0 || wait(&o_empty[x], (cu[x] - 1) & 1))) {
+                issue_pv<D>(tO[x], tS[x], sKV0 + sV * C::TILE_BYTES, j > 0);
+                if (x == 1) tc_commit(&kv_empty[sV]);
+                if (j == un.n[x] - 1) tc_commit(&o_full[x]);
+                if (j + 1 < un.n[x]) {
+                  if (!k_ready) k_ready = wait(&kv_full[sK], (fK / C::NS) & 1);
+                  if (k_ready) {
+                    issue_qk<D>(tS[x], sQa[x], sKV0 + sK * C::TILE_BYTES);
+                    tc_commit(&s_full[x]);
+                    if (j + 1 == un.n[x] - 1) tc_commit(&q_empty[x]);
+                    if (x == 1) tc_commit(&kv_empty[sK]);
+                  }
+                }
               }
-              issue_qk<D>(tS[x], sQa[x], sKV0 + sK * C::TILE_BYTES);
-              tc_commit(&s_full[x]);
-              if (j + 1 == un.n[x] - 1) tc_commit(&q_empty[x]);
-              if (x == 1) tc_commit(&kv_empty[sK]);
             }
           }
         }
+#pragma unroll
         for (int x = 0; x < 2; ++x)
           if (un.n[x] > 0) ++cu[x];
         fill += 2 * un.n[1];
@@ -409,13 +410,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = unit_index(i);
       if (u >= p.nUnits) break;
       const Unit un = decode_unit(p, u);
-      const int n = un.n[x];
+      const int n = x ? un.n[1] : un.n[0];
       if (n == 0) continue;
-      const int qpos = un.q0[x] + row;
+      const int hx = x ? un.h[1] : un.h[0];
+      const int qpos = (x ? un.q0[1] : un.q0[0]) + row;
       if (!mbar_wait(&q_full[x], cq & 1, abort_flag, p.status, kWaitNs)) break;
       ++cq;
       if (p.rope) {
-        rotate_q_row<D>(sQ[x], row, qpos, p.rope, p.theta);
+        rotate_q_row<D>(x ? sQ[1] : sQ[0], row, qpos, p.rope, p.theta);
         fence_proxy_async_smem();
       }
       __syncwarp();
@@ -431,13 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         float s[BN];
         {
-          uint32_t r[32];
+          uint32_t r[BN];
+          tmem_ld128_sync(tS, r);
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) {
-            tmem_ld32_sync(tS + 32u * c, r);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) s[32 * c + t] = __uint_as_float(r[t]);
-          }
+          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(r[c]);
         }
         // causal diagonal and ragged tail: keys beyond the row's limit get -inf
         int lim = BN - 1;
@@ -447,10 +446,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
         }
-        float mx = fmax3(s[0], s[1], s[2]);
+        // row max as four independent chains (latency), then combined
+        float mq[4];
 #pragma unroll
-        for (int c = 3; c + 1 < BN; c += 2) mx = fmax3(mx, s[c], s[c + 1]);
-        mx = fmaxf(mx, s[BN - 1]);
+        for (int t = 0; t < 4; ++t) mq[t] = fmaxf(s[t], s[4 + t]);
+#pragma unroll
+        for (int c = 8; c < BN; c += 8) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) mq[t] = fmax3(mq[t], s[c + t], s[c + 4 + t]);
+        }
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         const float m_new = fmaxf(m_used, mx * sl2);
         if (j == 0) {
           m_used = m_new;
@@ -468,20 +473,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
           m_used = m_new;
         }
-        float sum = 0.f;
+        float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;  // two independent pair sums
+        const float neg_m = -m_used;
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c) {
           uint32_t pk[32];
 #pragma unroll
           for (int t = 0; t < 32; ++t) {
-            const float p0 = ex2_approx(fmaf(s[64 * c + 2 * t], sl2, -m_used));
-            const float p1 = ex2_approx(fmaf(s[64 * c + 2 * t + 1], sl2, -m_used));
-            sum += p0 + p1;
+            float x0, x1;
+            ffma2(x0, x1, s[64 * c + 2 * t], s[64 * c + 2 * t + 1], sl2, sl2, neg_m, neg_m);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            if (t & 1)
+              fadd2(sb0, sb1, sb0, sb1, p0, p1);
+            else
+              fadd2(sa0, sa1, sa0, sa1, p0, p1);
             pk[t] = pack_bf16x2(p0, p1);
           }
           tmem_st32(tS + 32u * c, pk);
         }
-        l += sum;
+        l += (sa0 + sa1) + (sb0 + sb1);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -495,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = 1.f / l;
       const bool live = qpos < p.T;
       __nv_bfloat16* orow =
-          p.out + ((static_cast<size_t>(un.b) * p.Hq + un.h[x]) * p.T + (live ? qpos : 0)) * D;
+          p.out + ((static_cast<size_t>(un.b) * p.Hq + hx) * p.T + (live ? qpos : 0)) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -511,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (live && p.lse != nullptr)
-        p.lse[(static_cast<size_t>(un.b) * p.Hq + un.h[x]) * p.T + qpos] =
+        p.lse[(static_cast<size_t>(un.b) * p.Hq + hx) * p.T + qpos] =
             (m_used + log2f(l)) * 0.69314718055994531f;
       tc_fence_before();
       __syncwarp();

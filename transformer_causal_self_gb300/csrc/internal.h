@@ -19,7 +19,8 @@ struct FwdArgs {
   float* lse;
   int B, Hq, Hkv, T, d;
   int causal;
-  int rope;          // 0 none, 1 split-half, 2 adjacent
+  int rope;          // 0 none, 1 split-half, 2 adjacent (applied to q)
+  int rope_k;        // 1: rotate k as well; 0: k is used as given
   float scale;       // > 0
   RopeTable theta;   // valid when rope != 0
   uint32_t* status;  // device status word
