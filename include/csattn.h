@@ -24,8 +24,9 @@
  * Conventions for every call:
  *   - All tensors are dense, row-major, contiguous, in device memory, and
  *     16-byte aligned (they are read by TMA).  The caller owns every buffer;
- *     the library never allocates device memory of its own except one status
- *     word per device (a static device variable).
+ *     the library allocates no device memory at run time: its only device
+ *     memory is static (one status word per device, and the scratch buffer
+ *     of csattn_attn_decode_noalloc).
  *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
  *     stream) and never synchronize.  Argument errors are detected on the host
  *     before any launch and returned; nothing is launched then.
@@ -137,6 +138,36 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int Lmax,
                        int d, int dtype, float scale, int max_seq_len, int num_splits,
                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * csattn_attn_decode for callers that cannot allocate device memory (for
+ * example a plugin in a framework that owns all device memory and hands out
+ * no allocator, or a latency-critical loop where cudaMalloc would synchronise
+ * the device or could fail mid-batch).  The source pages have no counterpart
+ * of this entry point; it changes only where the scratch lives.
+ *
+ * Same arguments and results as csattn_attn_decode, without the workspace:
+ * the split partials go to a static device buffer of
+ * CSATTN_DECODE_STATIC_SCRATCH_BYTES bytes that the library defines and that
+ * every GPU loading the library keeps until the process exits.  The call
+ * allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
+ *   - Arguments whose partials (B*Hq*splits*(d+2)*4 bytes for the split
+ *     count actually used) exceed the buffer are rejected with
+ *     CSATTN_ERR_WORKSPACE and a message naming both sizes; nothing is
+ *     launched.  Use fewer splits, or csattn_attn_decode with a workspace.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture on the device.
+ *   - All calls on a device share the one buffer, which keeps the previous
+ *     call's contents (nothing in it has to start at zero).  Calls whose
+ *     kernels overlap on the GPU (other streams, other threads) race on it:
+ *     serialise them.
+ */
+#define CSATTN_DECODE_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int csattn_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* seq_lens, void* out, int B, int Hq, int Hkv,
+                               int Lmax, int d, int dtype, float scale, int max_seq_len,
+                               int num_splits, void* stream);
 
 /*
  * Synchronize `stream`, then read and clear this device's status word.

@@ -40,6 +40,8 @@ _SIGNATURES = {
     "csattn_decode_workspace_size": (_c_size, [_c_int] * 5),
     "csattn_attn_decode": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp,
                                                                 _c_size, _vp]),
+    "csattn_attn_decode_noalloc": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int,
+                                                                        _vp]),
     "csattn_check_status": (_c_int, [_vp]),
     "csattn_selftest_bounded_wait": (_c_int, [_c_int, _vp]),
     "csattn_last_error": (ctypes.c_char_p, []),

@@ -10,7 +10,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/csattn.h"
+#include "csattn.h"
 #include "internal.h"
 
 namespace csattn {
@@ -85,6 +85,8 @@ void rope_table(RopeTable* t, int d, double base) {
 constexpr int kMaxRopePositions = 49152;
 
 }  // namespace
+
+void set_last_error(const char* msg) { g_last_error = msg; }
 
 void* tensor_map_encoder() {
   static void* fn = [] {

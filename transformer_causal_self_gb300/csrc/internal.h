@@ -57,6 +57,9 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
+// Replace the calling thread's csattn_last_error() message.
+void set_last_error(const char* msg);
+
 // Driver entry point for cuTensorMapEncodeTiled (nullptr if unavailable).
 void* tensor_map_encoder();
 
