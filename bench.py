@@ -61,13 +61,20 @@ def _barrier(world):
 
 
 def _max_over_ranks(x, world):
+    """Largest x over all ranks (the slowest replica's time decides the step)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _job_throughput(units_per_rank, seconds_per_rank, world):
+    """Whole-job throughput of `world` replicas: all units / the slowest rank's time."""
+    return world * units_per_rank / _max_over_ranks(seconds_per_rank, world)
 
 
 class ClockSampler:

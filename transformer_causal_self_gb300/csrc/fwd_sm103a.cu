@@ -10,11 +10,17 @@
 // two consecutive tiles of one head.  The CTA is persistent (one per SM) and
 // walks the units longest-first in a snake order.
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax for tile A (TMEM lanes 0-127 = query rows)
-//   warps 4-7  softmax for tile B
-//   warp 8     TMA producer: Q_A, Q_B, then K_0, V_0, K_1, V_1, ... into a ring
-//   warp 9     TMEM allocator and MMA issuer (one thread)
+// Warp roles (384 threads = three warpgroups; setmaxnreg gives the softmax
+// warpgroups 200 registers and the third 104: 2*128*200 + 128*104 = 384*168):
+//   warps 0-3   softmax for tile A (TMEM lanes 0-127 = query rows); also the
+//               RoPE of tile A's next Q and tile A's epilogue
+//   warps 4-7   the same for tile B
+//   warp 8      TMA producer: Q_A, Q_B, then K_0, V_0, K_1, V_1, ... into a ring
+//   warp 9      TMEM allocator and MMA issuer (one thread)
+//   warps 10-11 idle (they complete the third warpgroup)
+// At the end of a unit a softmax warpgroup rotates the next unit's Q (which
+// has landed by then) before its epilogue, so the MMA warp can start the next
+// unit's S = Q K^T while the epilogue stores O.
 // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [256+D,256+2D).
 // P (bf16) overwrites the first 64 columns of its S region and feeds the
 // second MMA straight from TMEM.
@@ -37,9 +43,11 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile = TMEM lanes
 constexpr int BN = 128;  // keys per KV tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
+constexpr int kRegsSoftmax = 200;  // 2*128*200 + 128*104 = 64512 = 384 * 168
+constexpr int kRegsCtl = 104;
 constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s: far above any legal wait
 constexpr uint64_t kDrainNs = 100000000ull;     // 100 ms for the teardown after an abort
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
@@ -117,6 +125,21 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     }
   }
   return r;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status, uint64_t limit_ns) {
+  const bool ok = mbar_wait(bar, parity, abort, status, limit_ns);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // i-th unit of this CTA: rounds of gridDim.x units, alternating direction.
@@ -269,7 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kWarpProducer) {
+  if (warp >= 8) {
+   regs_dec<kRegsCtl>();
+   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -396,8 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(teardown, 0, nullptr, p.status, kDrainNs);
     }
     __syncwarp();
+   }
   } else {
     // ------------------------------------------------------------ softmax (A: warps 0-3, B: 4-7)
+    regs_inc<kRegsSoftmax>();
     const int x = warp >> 2;
     const int row = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -406,6 +433,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t cq = 0, cs = 0, co = 0;
     bool ok = true;
+    // Q of the next unit this warpgroup serves: wait for the tile, rotate row
+    // `row`, hand it to the MMA warp.  Done right after a unit's last P and
+    // before its epilogue, so the MMA warp can start the next unit's first
+    // S = Q K^T while the epilogue runs.
+    auto prep_q = [&](int i_from) {
+      for (int i2 = i_from;; ++i2) {
+        const int u2 = unit_index(i2);
+        if (u2 >= p.nUnits) return;
+        const Unit un2 = decode_unit(p, u2);
+        if ((x ? un2.n[1] : un2.n[0]) == 0) continue;
+        if (!warp_wait(&q_full[x], cq & 1, abort_flag, p.status, kWaitNs)) {
+          ok = false;
+          return;
+        }
+        ++cq;
+        if (p.rope) {
+          rotate_q_row<D>(x ? sQ[1] : sQ[0], row, (x ? un2.q0[1] : un2.q0[0]) + row, p.rope,
+                          p.theta);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_ready[x]);
+        return;
+      }
+    };
+    prep_q(0);
     for (int i = 0; ok; ++i) {
       const int u = unit_index(i);
       if (u >= p.nUnits) break;
@@ -414,18 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n == 0) continue;
       const int hx = x ? un.h[1] : un.h[0];
       const int qpos = (x ? un.q0[1] : un.q0[0]) + row;
-      if (!mbar_wait(&q_full[x], cq & 1, abort_flag, p.status, kWaitNs)) break;
-      ++cq;
-      if (p.rope) {
-        rotate_q_row<D>(x ? sQ[1] : sQ[0], row, qpos, p.rope, p.theta);
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_ready[x]);
 
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
-        if (!mbar_wait(&s_full[x], cs & 1, abort_flag, p.status, kWaitNs)) {
+        if (!warp_wait(&s_full[x], cs & 1, abort_flag, p.status, kWaitNs)) {
           ok = false;
           break;
         }
@@ -459,19 +504,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = fmaxf(m_used, mx * sl2);
         if (j == 0) {
           m_used = m_new;
-        } else if (m_new > m_used + kRescaleThreshold) {
-          const float f = ex2_approx(m_used - m_new);
-          l *= f;
+        } else {
+          const bool mine = m_new > m_used + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, mine)) {
+            const float f = mine ? ex2_approx(m_used - m_new) : 1.0f;
+            l *= f;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32_sync(tO + 32u * c, r);
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32_sync(tO + 32u * c, r);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * f);
-            tmem_st32(tO + 32u * c, r);
+              for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * f);
+              tmem_st32(tO + 32u * c, r);
+            }
+            tmem_st_wait();
+            if (mine) m_used = m_new;
           }
-          tmem_st_wait();
-          m_used = m_new;
         }
         float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;  // two independent pair sums
         const float neg_m = -m_used;
@@ -499,8 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&p_full[x]);
       }
       if (!ok) break;
+      prep_q(i + 1);
+      if (!ok) break;
       // epilogue: O / l -> bf16 rows of out; optional natural-log LSE
-      if (!mbar_wait(&o_full[x], co & 1, abort_flag, p.status, kWaitNs)) break;
+      if (!warp_wait(&o_full[x], co & 1, abort_flag, p.status, kWaitNs)) break;
       ++co;
       tc_fence_after();
       const float inv = 1.f / l;
