@@ -317,11 +317,12 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   } else {
     rc = device_info(&a.status, &num_sms);
     if (rc != CSATTN_OK) return rc;
-    // Smallest chunk (>= 256 keys) that keeps the grid near eight CTAs per SM.
+    // Smallest chunk (>= 256 keys) that keeps the grid at most ~32 CTAs per SM
+    // (measured on the B=64, L~U[512,8192] workload: 1024-key chunks).
     a.chunk = 256;
     while (a.chunk < 4096 &&
            static_cast<long long>(B) * Hkv * ((max_seq_len + a.chunk - 1) / a.chunk) >
-               8LL * num_sms)
+               32LL * num_sms)
       a.chunk *= 2;
   }
   a.n_splits = (max_seq_len + a.chunk - 1) / a.chunk;

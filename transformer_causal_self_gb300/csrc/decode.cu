@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(kThreads)
     if (threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(p.status, kStatusDeviceArg);
     L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
   }
+  // let the merge kernel (launched with programmatic dependent launch) be
+  // scheduled as soon as every CTA of this grid has started; it still waits
+  // for this grid to finish before it reads the partials
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int k_begin = split * p.chunk;
   const int k_end = min(L, k_begin + p.chunk);
   if (k_begin >= k_end) return;  // the merge reads only splits that hold keys
@@ -330,6 +334,8 @@ __global__ void decode_combine_kernel(const float* __restrict__ part_o,
                                       const int32_t* __restrict__ seq_lens,
                                       __nv_bfloat16* __restrict__ out, int Hq, int n_splits,
                                       int chunk, int max_seq_len, int D) {
+  // wait until the split kernel has finished and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bh = blockIdx.x;
   const int b = bh / Hq;
   int L = seq_lens[b];
@@ -383,10 +389,19 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   decode_bf16_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<a.B * a.Hq, D, 0, stream>>>(
-      a.part_o, a.part_ml, a.seq_lens, static_cast<__nv_bfloat16*>(a.out), a.Hq, a.n_splits,
-      a.chunk, a.max_seq_len, D);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * a.Hq, 1, 1);
+  cfg.blockDim = dim3(D, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float*>(a.part_o),
+                            static_cast<const float*>(a.part_ml), a.seq_lens,
+                            static_cast<__nv_bfloat16*>(a.out), a.Hq, a.n_splits, a.chunk,
+                            a.max_seq_len, D);
 }
 
 }  // namespace
