@@ -152,14 +152,15 @@ def _source_hash(*names):
     return h.hexdigest()[:16]
 
 
-def _traffic(kernel_file):
-    """DRAM bytes per launch from the committed ncu summary, if it is for this source."""
+def _traffic(kernel_file, *deps):
+    """DRAM bytes per launch from the committed ncu summary, if it is for this source
+    (the kernel's file plus the headers it includes)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
         e = t[kernel_file]
-        if e.get("source_sha") == _source_hash(kernel_file, "common.cuh"):
+        if e.get("source_sha") == _source_hash(kernel_file, *deps):
             return float(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError, TypeError):
         pass
@@ -379,13 +380,13 @@ def run_gpu(args):
 
     roof = {"bound": "tensor", "achieved": round(fwd_tflops, 2), "peak": tf_burst,
             "unit": "TFLOP/s", "frac": round(fwd_tflops / tf_burst, 4),
-            "traffic": _traffic("fwd_sm103a.cu"),
-            "kernel": "fwd_sm103a_kernel<128>",
+            "traffic": _traffic("fwd_sm103a_d128.cu", "fwd_units.cuh", "common.cuh"),
+            "kernel": "fwd_d128_kernel",
             "peak_kind": f"{peak_kind} bf16 dense burst (cuBLAS)",
             "frac_of_sustained": round(fwd_tflops / tf_sust, 4),
             "frac_of_spec_2250": round(fwd_tflops / 2250.0, 4)}
     dec_roof = {"bound": "hbm", "achieved": round(dec_gbs_one, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(dec_gbs_one / hbm_peak, 4), "traffic": _traffic("decode.cu"),
+                "frac": round(dec_gbs_one / hbm_peak, 4), "traffic": _traffic("decode.cu", "common.cuh"),
                 "kernel": "decode_bf16_kernel<128> + decode_combine_kernel",
                 "peak_kind": f"{peak_kind} HBM copy", "frac_of_spec_8000": round(dec_gbs_one / 8000.0, 4)}
     line = {

@@ -34,8 +34,10 @@ cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, int T, int d,
                                     int rope, const RopeTable& theta, cudaStream_t stream);
 
-// bf16 tcgen05 prefill; `k_eff` is k itself or its rotated copy.
+// bf16 tcgen05 prefill; `k_eff` is k itself or its rotated copy.  d = 64 runs
+// the kernel in fwd_sm103a.cu, d = 128 the one in fwd_sm103a_d128.cu.
 cudaError_t launch_fwd_sm103a(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
+cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
 
 struct DecodeArgs {
   const void* q;
