@@ -23,7 +23,12 @@ Sources (page title, then section):
   * "The Transformer architecture", "What else the modern decoder-only model
     changed": each group of n_rep query heads shares one K/V head.
   * "The Transformer architecture", "Hands-on": with a cache, the query at
-    position p sees keys 0..p, the current token included.
+    position p sees keys 0..p, the current token included.  The same holds for
+    a chunk of Tq new queries after a cache prefix of length q_offset: query i
+    sits at position q_offset + i, is rotated at that position, and sees keys
+    0..q_offset+i (the cache plus the chunk's own causal part).
+  * "Transformer Math and Implementation Deep Dive", "Attention Equation"
+    (cross-attention): with no causal mask, Tq and Tk need not be equal.
 
 Readings where the pages leave a step open (each one also listed in the design doc):
   * RoPE frequencies theta_i = base^(-2i/d), i = 0..d/2-1, positions from 0.
@@ -168,12 +173,14 @@ def _rotated(x, base, layout, operand_dtype, positions):
 
 
 def attention(q, k, v, *, causal=True, rope_base=0.0, scale=None,
-              rope_layout="split_half", operand_dtype=None):
-    """Full prefill output [B, Hq, T, d] in float64.
+              rope_layout="split_half", operand_dtype=None, q_offset=0):
+    """Full prefill output [B, Hq, Tq, d] in float64.
 
-    Steps: upcast; RoPE on q and k (positions 0..T-1), rounded to
-    ``operand_dtype``; GQA repetition of K/V; S = Q K^T * scale; S + M;
-    row softmax; P V.  Loops over (b, h) to bound memory.
+    q [B, Hq, Tq, d]; k, v [B, Hkv, Tk, d].  Query i sits at position
+    q_offset + i, key j at position j.  Steps: upcast; RoPE on q and k at
+    those positions, rounded to ``operand_dtype``; GQA repetition of K/V;
+    S = Q K^T * scale; S + M (key j visible iff j <= q_offset + i when
+    causal); row softmax; P V.  Loops over (b, h) to bound memory.
     """
     q = np.asarray(_as_np(q), dtype=np.float64)
     k = np.asarray(_as_np(k), dtype=np.float64)
@@ -181,11 +188,11 @@ def attention(q, k, v, *, causal=True, rope_base=0.0, scale=None,
     B, Hq, T, d = q.shape
     Tk = k.shape[2]
     sc = _default_scale(d, scale)
-    qr = _rotated(q, rope_base, rope_layout, operand_dtype, np.arange(T))
+    qr = _rotated(q, rope_base, rope_layout, operand_dtype, int(q_offset) + np.arange(T))
     kr = _rotated(k, rope_base, rope_layout, operand_dtype, np.arange(Tk))
     kf = expand_kv_heads(kr, Hq)
     vf = expand_kv_heads(v, Hq)
-    mask = causal_additive_mask(T, Tk) if causal else np.zeros((T, Tk))
+    mask = causal_additive_mask(T, Tk, q_offset) if causal else np.zeros((T, Tk))
     out = np.empty((B, Hq, T, v.shape[-1]), dtype=np.float64)
     for b in range(B):
         for h in range(Hq):
@@ -195,16 +202,16 @@ def attention(q, k, v, *, causal=True, rope_base=0.0, scale=None,
 
 
 def attention_lse(q, k, *, causal=True, rope_base=0.0, scale=None,
-                  rope_layout="split_half", operand_dtype=None):
-    """Natural-log log-sum-exp of each masked score row, [B, Hq, T]."""
+                  rope_layout="split_half", operand_dtype=None, q_offset=0):
+    """Natural-log log-sum-exp of each masked score row, [B, Hq, Tq]."""
     q = np.asarray(_as_np(q), dtype=np.float64)
     k = np.asarray(_as_np(k), dtype=np.float64)
     B, Hq, T, d = q.shape
     Tk = k.shape[2]
     sc = _default_scale(d, scale)
-    qr = _rotated(q, rope_base, rope_layout, operand_dtype, np.arange(T))
+    qr = _rotated(q, rope_base, rope_layout, operand_dtype, int(q_offset) + np.arange(T))
     kf = expand_kv_heads(_rotated(k, rope_base, rope_layout, operand_dtype, np.arange(Tk)), Hq)
-    mask = causal_additive_mask(T, Tk) if causal else np.zeros((T, Tk))
+    mask = causal_additive_mask(T, Tk, q_offset) if causal else np.zeros((T, Tk))
     out = np.empty((B, Hq, T), dtype=np.float64)
     for b in range(B):
         for h in range(Hq):
@@ -215,7 +222,7 @@ def attention_lse(q, k, *, causal=True, rope_base=0.0, scale=None,
 
 
 def attention_rows(q, k, v, b: int, h: int, rows, *, causal=True, rope_base=0.0,
-                   scale=None, rope_layout="split_half", operand_dtype=None):
+                   scale=None, rope_layout="split_half", operand_dtype=None, q_offset=0):
     """Output rows ``rows`` of head h, batch b: [len(rows), d] float64.
 
     Same definition as ``attention`` restricted to a subset of query rows, for
@@ -230,11 +237,12 @@ def attention_rows(q, k, v, b: int, h: int, rows, *, causal=True, rope_base=0.0,
     kb = np.asarray(_as_np(k[b, g]), dtype=np.float64)
     vb = np.asarray(_as_np(v[b, g]), dtype=np.float64)
     sc = _default_scale(d, scale)
-    qr = _rotated(qb, rope_base, rope_layout, operand_dtype, rows)
+    pos = int(q_offset) + rows
+    qr = _rotated(qb, rope_base, rope_layout, operand_dtype, pos)
     kr = _rotated(kb, rope_base, rope_layout, operand_dtype, np.arange(Tk))
     s = attention_scores(qr, kr, sc)
     if causal:
-        s = s + np.where(np.arange(Tk)[None, :] > rows[:, None], -np.inf, 0.0)
+        s = s + np.where(np.arange(Tk)[None, :] > pos[:, None], -np.inf, 0.0)
     return softmax_rows(s) @ vb
 
 

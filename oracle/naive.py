@@ -57,8 +57,10 @@ def _rot(vec, pos, base, layout, rnd):
 
 
 def naive_attention(q, k, v, causal=True, rope_base=0.0, scale=None,
-                    rope_layout="split_half", round_bf16=False):
-    """q [B][Hq][T][d], k/v [B][Hkv][T][d] as nested lists; returns nested lists."""
+                    rope_layout="split_half", round_bf16=False, q_offset=0):
+    """q [B][Hq][Tq][d], k/v [B][Hkv][Tk][d] as nested lists; returns nested lists.
+
+    Query i sits at position q_offset + i (RoPE angle and causal limit)."""
     B, Hq, T, d = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
     Hkv = len(k[0])
     Tk = len(k[0][0])
@@ -71,7 +73,8 @@ def naive_attention(q, k, v, causal=True, rope_base=0.0, scale=None,
         for h in range(Hq):
             g = h // rep
             if rope_base > 0:
-                qs = [_rot(q[b][h][t], t, rope_base, rope_layout, rnd) for t in range(T)]
+                qs = [_rot(q[b][h][t], q_offset + t, rope_base, rope_layout, rnd)
+                      for t in range(T)]
                 ks = [_rot(k[b][g][t], t, rope_base, rope_layout, rnd) for t in range(Tk)]
             else:
                 qs = [list(map(float, q[b][h][t])) for t in range(T)]
@@ -81,7 +84,7 @@ def naive_attention(q, k, v, causal=True, rope_base=0.0, scale=None,
             for i in range(T):
                 scores = {}
                 for j in range(Tk):
-                    if causal and j > i:
+                    if causal and j > q_offset + i:
                         continue
                     dot = 0.0
                     for c in range(d):

@@ -252,11 +252,77 @@ def pin_bf16_rounding(o):
     assert np.array_equal(o.round_to_bf16(x64), naive)
 
 
+def pin_chunk_equals_full_rows(o):
+    """A chunk of queries after a cache prefix (q_offset) gives the same rows as the
+    full causal prefill ("The Transformer architecture", "Hands-on": the query at
+    position p sees keys 0..p, rotated at p)."""
+    B, Hkv, rep, T, d = 1, 2, 2, 40, 16
+    q = _rand((B, Hkv * rep, T, d), 130, 2.0)
+    k = _rand((B, Hkv, T, d), 131, 2.0)
+    v = _rand((B, Hkv, T, d), 132)
+    for dt in (None, "bf16"):
+        full = o.attention(q, k, v, causal=True, rope_base=10000.0, operand_dtype=dt)
+        for off in (0, 7, 23, 39):
+            chunk = o.attention(q[:, :, off:], k, v, causal=True, rope_base=10000.0,
+                                operand_dtype=dt, q_offset=off)
+            assert chunk.shape == (B, Hkv * rep, T - off, d)
+            assert np.max(np.abs(chunk - full[:, :, off:])) < 1e-12, (dt, off)
+        # a chunk that stops early: keys past the chunk's last position are never visible
+        mid = o.attention(q[:, :, 10:20], k, v, causal=True, rope_base=10000.0, operand_dtype=dt,
+                          q_offset=10)
+        assert np.max(np.abs(mid - full[:, :, 10:20])) < 1e-12
+
+
+def pin_chunk_naive(o):
+    """Query offset and rectangular shapes against the scalar-loop oracle."""
+    cases = [dict(Tq=4, Tk=9, off=5, causal=True, base=10000.0, layout="split_half"),
+             dict(Tq=3, Tk=12, off=2, causal=True, base=10000.0, layout="adjacent"),
+             dict(Tq=5, Tk=11, off=0, causal=False, base=0.0, layout="split_half"),
+             dict(Tq=7, Tk=3, off=4, causal=False, base=10000.0, layout="split_half")]
+    for i, c in enumerate(cases):
+        q = _rand((1, 4, c["Tq"], 8), 140 + i, 2.0)
+        k = _rand((1, 2, c["Tk"], 8), 150 + i, 2.0)
+        v = _rand((1, 2, c["Tk"], 8), 160 + i)
+        for rnd in (False, True):
+            a = o.attention(q, k, v, causal=c["causal"], rope_base=c["base"], scale=0.41,
+                            rope_layout=c["layout"], operand_dtype="bf16" if rnd else None,
+                            q_offset=c["off"])
+            b = np.array(ON.naive_attention(_to_list(q), _to_list(k), _to_list(v), c["causal"],
+                                            c["base"], 0.41, c["layout"], round_bf16=rnd,
+                                            q_offset=c["off"]))
+            assert np.max(np.abs(a - b)) < 1e-12, (i, rnd)
+            rows = np.arange(c["Tq"])[::2]
+            r = o.attention_rows(q, k, v, 0, 3, rows, causal=c["causal"], rope_base=c["base"],
+                                 scale=0.41, rope_layout=c["layout"],
+                                 operand_dtype="bf16" if rnd else None, q_offset=c["off"])
+            assert np.max(np.abs(r - a[0, 3, rows])) < 1e-12
+    # one key: every query returns that key's value exactly
+    q = _rand((1, 2, 6, 8), 170)
+    k = _rand((1, 1, 1, 8), 171)
+    v = _rand((1, 1, 1, 8), 172)
+    out = o.attention(q, k, v, causal=False, rope_base=10000.0, q_offset=3)
+    assert np.array_equal(out, np.broadcast_to(v, (1, 2, 6, 8)))
+
+
+def pin_decode_is_chunk_of_one(o):
+    """Decode at length L equals a one-query chunk at q_offset = L - 1."""
+    B, Hkv, rep, d, L = 1, 2, 4, 16, 23
+    q = _rand((B, Hkv * rep, L, d), 180)
+    k = _rand((B, Hkv, L, d), 181)
+    v = _rand((B, Hkv, L, d), 182)
+    one = o.attention(q[:, :, L - 1:], k, v, causal=True, rope_base=10000.0, q_offset=L - 1)
+    qd = o.rope_rotate(q[:, :, L - 1:], np.array([L - 1]), 10000.0)
+    kr = o.rope_rotate(k, np.arange(L), 10000.0)
+    dec = o.decode(qd, kr, v, [L])
+    assert np.max(np.abs(one - dec)) < 1e-12
+
+
 ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exactly_zero,
             pin_mask_variants_differ, pin_gqa_equals_mha_repeated, pin_basis_invariance,
             pin_qq_symmetric, pin_rope_relative, pin_rope_orthogonal, pin_rope_layouts_permute,
             pin_rope_angle_formula, pin_naive_agreement, pin_degenerate_cases,
-            pin_decode_equals_prefill_last_row, pin_merge_partials, pin_bf16_rounding]
+            pin_decode_equals_prefill_last_row, pin_merge_partials, pin_bf16_rounding,
+            pin_chunk_equals_full_rows, pin_chunk_naive, pin_decode_is_chunk_of_one]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -415,3 +481,43 @@ def test_planted_bf16_truncation():
         m, e = np.frexp(x)
         return np.ldexp(np.trunc(np.ldexp(m, 8)), e - 8)
     assert _fails(_Mutant(round_to=bad_round), [pin_naive_agreement])
+
+
+
+def _chunk_attention(q, k, v, mask_offset, rope_offset, causal=True, rope_base=0.0, scale=None,
+                     rope_layout="split_half", operand_dtype=None):
+    """The oracle's chunk definition with the mask and the RoPE positions offset separately."""
+    q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+    B, Hq, Tq, d = q.shape
+    Tk = k.shape[2]
+    sc = 1 / math.sqrt(d) if (scale is None or scale <= 0) else scale
+    if rope_base > 0:
+        q = OA.round_to(OA.rope_rotate(q, rope_offset + np.arange(Tq), rope_base, rope_layout),
+                        operand_dtype)
+        k = OA.round_to(OA.rope_rotate(k, np.arange(Tk), rope_base, rope_layout), operand_dtype)
+    kf, vf = OA.expand_kv_heads(k, Hq), OA.expand_kv_heads(v, Hq)
+    mask = OA.causal_additive_mask(Tq, Tk, mask_offset) if causal else 0.0
+    out = np.empty((B, Hq, Tq, v.shape[-1]))
+    for b in range(B):
+        for h in range(Hq):
+            out[b, h] = OA.softmax_rows(OA.attention_scores(q[b, h], kf[b, h], sc) + mask) @ vf[b, h]
+    return out
+
+
+def test_chunk_helper_is_faithful():
+    def good(q, k, v, *, q_offset=0, **kw):
+        return _chunk_attention(q, k, v, q_offset, q_offset, **kw)
+    assert _fails(_Mutant(attention=good), [pin_chunk_equals_full_rows, pin_chunk_naive,
+                                            pin_decode_is_chunk_of_one]) == []
+
+
+def test_planted_offset_ignored_by_mask():
+    def bad(q, k, v, *, q_offset=0, **kw):
+        return _chunk_attention(q, k, v, 0, q_offset, **kw)
+    assert _fails(_Mutant(attention=bad), [pin_chunk_equals_full_rows])
+
+
+def test_planted_offset_ignored_by_rope():
+    def bad(q, k, v, *, q_offset=0, **kw):
+        return _chunk_attention(q, k, v, q_offset, 0, **kw)
+    assert _fails(_Mutant(attention=bad), [pin_chunk_equals_full_rows, pin_decode_is_chunk_of_one])
