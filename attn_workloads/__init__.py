@@ -81,6 +81,40 @@ class DecodeWorkload:
         return replace(self, **kw)
 
 
+@dataclass(frozen=True)
+class ChunkWorkload:
+    """A chunk of Tq queries at positions q_offset.. against Tk keys (a cached prefix
+    plus the chunk's own keys when Tk = q_offset + Tq), or rectangular attention."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Tq: int
+    Tk: int
+    q_offset: int
+    d: int
+    dtype: str
+    rope_base: float
+    scale: float
+    causal: bool = True
+    seed: int = 0
+
+    def visible_keys(self) -> int:
+        """Sum over query rows of the keys each one sees (row i: min(Tk, q_offset + i + 1))."""
+        if not self.causal:
+            return self.Tq * self.Tk
+        rows_short = max(0, min(self.Tq, self.Tk - self.q_offset))  # rows seeing < all keys
+        seen = rows_short * (2 * self.q_offset + rows_short + 1) // 2
+        return seen + (self.Tq - rows_short) * self.Tk
+
+    def flops(self) -> float:
+        """QK^T and PV over the visible (query, key) pairs: 4*d per pair."""
+        return 4.0 * self.B * self.Hq * self.d * self.visible_keys()
+
+    def with_(self, **kw) -> "ChunkWorkload":
+        return replace(self, **kw)
+
+
 WORKLOADS = {
     "tiny_f32": PrefillWorkload("tiny_f32", B=1, Hq=2, Hkv=2, T=64, d=16, dtype="f32",
                                 rope_base=10000.0, scale=1.0 / math.sqrt(16)),
@@ -95,6 +129,10 @@ WORKLOADS = {
     "long_gqa_bf16": PrefillWorkload("long_gqa_bf16", B=1, Hq=32, Hkv=8, T=32768, d=128,
                                      dtype="bf16", rope_base=500000.0,
                                      scale=1.0 / math.sqrt(128)),
+    # the last quarter of the llama_gqa_bf16 sequence as one chunk after a 3072-token cache
+    "llama_chunk_bf16": ChunkWorkload("llama_chunk_bf16", B=4, Hq=32, Hkv=8, Tq=1024, Tk=4096,
+                                      q_offset=3072, d=128, dtype="bf16", rope_base=10000.0,
+                                      scale=1.0 / math.sqrt(128)),
     "decode_bf16": DecodeWorkload("decode_bf16", B=64, Hq=32, Hkv=8, d=128, Lmax=8192,
                                   Lmin=512, dtype="bf16", scale=1.0 / math.sqrt(128)),
 }
@@ -122,6 +160,16 @@ def make_prefill_inputs(w: PrefillWorkload, seed: Optional[int] = None):
         assert math.log2(m).is_integer(), "qk_mult must be a power of two (exact scaling)"
         q = q * m
         k = k * m
+    return q.contiguous(), k.contiguous(), v.contiguous()
+
+
+def make_chunk_inputs(w: ChunkWorkload, seed: Optional[int] = None):
+    """Return CPU tensors q [B,Hq,Tq,d], k, v [B,Hkv,Tk,d] in the workload dtype."""
+    g = _gen(w.seed if seed is None else seed)
+    dt = torch_dtype(w.dtype)
+    q = torch.randn(w.B, w.Hq, w.Tq, w.d, generator=g, dtype=torch.float32).to(dt)
+    k = torch.randn(w.B, w.Hkv, w.Tk, w.d, generator=g, dtype=torch.float32).to(dt)
+    v = torch.randn(w.B, w.Hkv, w.Tk, w.d, generator=g, dtype=torch.float32).to(dt)
     return q.contiguous(), k.contiguous(), v.contiguous()
 
 

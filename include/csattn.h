@@ -91,13 +91,46 @@ size_t csattn_fwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype
  *   workspace    device buffer of at least csattn_fwd_workspace_size() bytes
  *                (may be NULL when that size is 0), owned by the caller.
  * Requirements: B, Hq, Hkv, T >= 1; Hq % Hkv == 0; d in {64, 128} for bf16,
- * d in {16, 32, 64, 128} for fp32; T < 2^24.  The rotated q and k are rounded
+ * d in {16, 32, 64, 128} for fp32; T < 2^24, and T <= 49152 with RoPE (the
+ * range in which the angles are reduced exactly).  The rotated q and k are rounded
  * to the input dtype before the dot products; accumulation is fp32.
  */
 int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
                     int Hkv, int T, int d, int dtype, int causal, float rope_base,
                     int rope_layout, float scale, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of device workspace csattn_attn_fwd_ext needs: the rotated keys,
+ * B*Hkv*Tk*d*2, for bf16 with RoPE (unless k is given rotated); 0 otherwise.
+ */
+size_t csattn_fwd_ext_workspace_size(int B, int Hq, int Hkv, int Tq, int Tk, int d, int dtype,
+                                     float rope_base);
+
+/*
+ * Prefill of a chunk of queries after a cache prefix, or rectangular
+ * (cross-)attention ("The Transformer architecture", "Hands-on": the query at
+ * position p sees cached keys 0..p; "Transformer Math and Implementation Deep
+ * Dive", "Attention Equation": Tq and Tk need not match without a mask).
+ *   q    [B, Hq,  Tq, d];  k, v [B, Hkv, Tk, d];  out [B, Hq, Tq, d]
+ *   q_offset     position of query row 0: row i sits at q_offset + i; keys sit
+ *                at 0..Tk-1.  With causal = 1, row i sees keys j <= q_offset + i
+ *                (a chunked prefill passes Tk = q_offset + Tq: the cached prefix
+ *                followed by the chunk's own keys).  With causal = 0 every key
+ *                is visible.
+ *   rope_base    > 0: q is rotated at positions q_offset + i and k at 0..Tk-1
+ *                (unless CSATTN_ROPE_K_PREROTATED is set in rope_layout).
+ *   lse          NULL or fp32 [B, Hq, Tq].
+ *   workspace    at least csattn_fwd_ext_workspace_size() bytes.
+ * Other arguments, ownership and errors as csattn_attn_fwd, which is this call
+ * with Tq = Tk = T and q_offset = 0.  Additional requirements: Tq, Tk >= 1,
+ * 0 <= q_offset < 2^24; with RoPE, q_offset + Tq <= 49152 and Tk <= 49152
+ * (CSATTN_ERR_UNSUPPORTED otherwise).
+ */
+int csattn_attn_fwd_ext(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                        int Hkv, int Tq, int Tk, int q_offset, int d, int dtype, int causal,
+                        float rope_base, int rope_layout, float scale, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * RoPE of x [B, H, T, d] into x_rot (same shape; must not overlap x), at

@@ -63,6 +63,8 @@ def test_workspace_sizes(lib):
     assert lib.csattn_fwd_workspace_size(4, 32, 8, 4096, 128, 1, 0.0) == 0
     assert lib.csattn_fwd_workspace_size(1, 2, 2, 64, 16, 0, 10000.0) == 0
     # decode partials: B*Hq*splits*(d+2) fp32, automatic splits cover Lmax/256
+    assert lib.csattn_fwd_ext_workspace_size(4, 32, 8, 1024, 4096, 128, 1, 10000.0) == 4 * 8 * 4096 * 128 * 2
+    assert lib.csattn_fwd_ext_workspace_size(4, 32, 8, 1024, 4096, 128, 0, 10000.0) == 0
     assert lib.csattn_decode_workspace_size(64, 32, 8192, 128, 0) == 64 * 32 * 32 * 130 * 4
     assert lib.csattn_decode_workspace_size(2, 4, 100, 64, 5) == 2 * 4 * 5 * 66 * 4
 
@@ -98,6 +100,29 @@ def test_fwd_rejects_invalid_arguments(lib, kw, status):
                              a["scale"], a["lse"], a["ws"], a["ws_bytes"], None)
     assert rc == status, lib.csattn_last_error()
     assert len(lib.csattn_last_error()) > 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q_offset=-1), -1),
+    (dict(Tk=0), -1),
+    (dict(Tq=0), -1),
+    (dict(q_offset=1 << 24), -2),
+    (dict(dtype=1, rope_base=10000.0, q_offset=49000, Tq=200), -2),
+    (dict(dtype=1, rope_base=10000.0, Tk=50000), -2),
+    (dict(dtype=1, rope_base=10000.0, ws=None, ws_bytes=0), -5),
+    (dict(dtype=1, rope_base=10000.0, Tk=512, ws=FAKE, ws_bytes=1 * 2 * 256 * 64 * 2), -5),
+])
+def test_fwd_ext_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, Hq=4, Hkv=2, Tq=64, Tk=256, q_offset=192,
+             d=64, dtype=0, causal=1, rope_base=0.0, rope_layout=0, scale=0.0, lse=None, ws=None,
+             ws_bytes=0)
+    a.update(kw)
+    rc = lib.csattn_attn_fwd_ext(a["q"], a["k"], a["v"], a["out"], a["B"], a["Hq"], a["Hkv"],
+                                 a["Tq"], a["Tk"], a["q_offset"], a["d"], a["dtype"], a["causal"],
+                                 a["rope_base"], a["rope_layout"], a["scale"], a["lse"], a["ws"],
+                                 a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"attn_fwd_ext" in lib.csattn_last_error()
 
 
 @pytest.mark.parametrize("kw,status", [

@@ -36,6 +36,10 @@ _SIGNATURES = {
     "csattn_fwd_workspace_size": (_c_size, [_c_int] * 6 + [_c_float]),
     "csattn_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _c_float,
                                                                         _vp, _vp, _c_size, _vp]),
+    "csattn_fwd_ext_workspace_size": (_c_size, [_c_int] * 7 + [_c_float]),
+    "csattn_attn_fwd_ext": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 9 + [_c_float, _c_int,
+                                                                            _c_float, _vp, _vp,
+                                                                            _c_size, _vp]),
     "csattn_rope_rotate": (_c_int, [_vp, _vp] + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "csattn_decode_workspace_size": (_c_size, [_c_int] * 5),
     "csattn_attn_decode": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp,
@@ -111,6 +115,12 @@ def fwd_workspace_size(B, Hq, Hkv, T, d, dtype: torch.dtype, rope_base: float) -
     return int(load_library().csattn_fwd_workspace_size(B, Hq, Hkv, T, d, code, float(rope_base)))
 
 
+def fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, dtype: torch.dtype, rope_base: float) -> int:
+    code = CSATTN_BF16 if dtype == torch.bfloat16 else CSATTN_F32
+    return int(load_library().csattn_fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, code,
+                                                            float(rope_base)))
+
+
 def decode_workspace_size(B, Hq, Lmax, d, num_splits: int = 0) -> int:
     return int(load_library().csattn_decode_workspace_size(B, Hq, Lmax, d, num_splits))
 
@@ -160,6 +170,40 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: Optional[to
                                float(scale),
                                lse.data_ptr() if lse is not None else None, ws_ptr, ws_bytes,
                                _stream_handle(stream)))
+    return out
+
+
+def attn_fwd_ext(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                 out: Optional[torch.Tensor] = None, *, q_offset: int = 0, causal: bool = True,
+                 rope_base: float = 0.0, scale: float = 0.0, rope_layout: str = "split_half",
+                 lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 k_prerotated: bool = False, stream=None) -> torch.Tensor:
+    """Chunked / rectangular prefill (C: csattn_attn_fwd_ext).
+
+    q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d].  Query row i sits at position q_offset + i;
+    with causal it sees keys j <= q_offset + i.  RoPE rotates q at q_offset + i
+    and k at 0..Tk-1 (unless k_prerotated).  lse, if given, is fp32 [B,Hq,Tq].
+    """
+    _need_cuda(q, k, v)
+    B, Hq, Tq, d = q.shape
+    Hkv, Tk = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda(out)
+    if lse is not None:
+        _need_cuda(lse)
+    need = 0 if k_prerotated else fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, q.dtype, rope_base)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    lib = load_library()
+    _check(lib.csattn_attn_fwd_ext(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq,
+                                   Hkv, Tq, Tk, int(q_offset), d, _dtype_code(q),
+                                   int(bool(causal)), float(rope_base),
+                                   _ROPE_LAYOUT[rope_layout] | (K_PREROTATED if k_prerotated else 0),
+                                   float(scale), lse.data_ptr() if lse is not None else None,
+                                   ws_ptr, ws_bytes, _stream_handle(stream)))
     return out
 
 

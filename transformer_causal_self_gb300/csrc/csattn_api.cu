@@ -143,51 +143,66 @@ int csattn_version(void) { return 100; }
 
 size_t csattn_fwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,
                                  float rope_base) {
-  (void)Hq;
-  if (dtype != CSATTN_BF16 || !(rope_base > 0.f) || B < 1 || Hkv < 1 || T < 1 || d < 1) return 0;
-  return static_cast<size_t>(B) * Hkv * T * d * 2;
+  return csattn_fwd_ext_workspace_size(B, Hq, Hkv, T, T, d, dtype, rope_base);
 }
 
-int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
-                    int Hkv, int T, int d, int dtype, int causal, float rope_base,
-                    int rope_layout, float scale, float* lse, void* workspace,
-                    size_t workspace_bytes, void* stream) {
+size_t csattn_fwd_ext_workspace_size(int B, int Hq, int Hkv, int Tq, int Tk, int d, int dtype,
+                                     float rope_base) {
+  (void)Hq;
+  (void)Tq;
+  if (dtype != CSATTN_BF16 || !(rope_base > 0.f) || B < 1 || Hkv < 1 || Tk < 1 || d < 1) return 0;
+  return static_cast<size_t>(B) * Hkv * Tk * d * 2;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared by csattn_attn_fwd (Tq = Tk = T, q_offset = 0) and csattn_attn_fwd_ext.
+int attn_fwd_impl(const char* fn, const void* q, const void* k, const void* v, void* out, int B,
+                  int Hq, int Hkv, int Tq, int Tk, int q_offset, int d, int dtype, int causal,
+                  float rope_base, int rope_layout, float scale, float* lse, void* workspace,
+                  size_t workspace_bytes, void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: q, k, v and out must be non-null");
-  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: B=%d Hq=%d Hkv=%d T=%d must be >= 1", B, Hq,
-                Hkv, T);
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: q, k, v and out must be non-null", fn);
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: B=%d Hq=%d Hkv=%d Tq=%d Tk=%d must be >= 1", fn, B,
+                Hq, Hkv, Tq, Tk);
+  if (q_offset < 0) return fail(CSATTN_ERR_INVALID_ARG, "%s: q_offset=%d < 0", fn, q_offset);
   if (Hq % Hkv != 0)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: Hq=%d is not a multiple of Hkv=%d", fn, Hq, Hkv);
   if (dtype != CSATTN_F32 && dtype != CSATTN_BF16)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: unknown dtype %d", dtype);
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, dtype);
   if (causal != 0 && causal != 1)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: causal must be 0 or 1");
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
   const bool k_prerotated = (rope_layout & CSATTN_ROPE_K_PREROTATED) != 0;
   rope_layout &= ~CSATTN_ROPE_K_PREROTATED;
   if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: unknown rope_layout %d", rope_layout);
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown rope_layout %d", fn, rope_layout);
   if (!std::isfinite(rope_base) || !std::isfinite(scale))
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: rope_base and scale must be finite");
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: rope_base and scale must be finite", fn);
   if (d != 16 && d != 32 && d != 64 && d != 128)
-    return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: d=%d not in {16,32,64,128}", d);
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d not in {16,32,64,128}", fn, d);
   if (dtype == CSATTN_BF16 && d != 64 && d != 128)
-    return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: bf16 supports d in {64,128}, got %d", d);
-  if (T >= (1 << 24)) return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: T=%d >= 2^24", T);
-  if (rope_base > 0.f && T > kMaxRopePositions)
-    return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: RoPE supports T <= %d, got %d",
-                kMaxRopePositions, T);
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: bf16 supports d in {64,128}, got %d", fn, d);
+  if (Tq >= (1 << 24) || Tk >= (1 << 24) || q_offset >= (1 << 24))
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: Tq=%d, Tk=%d and q_offset=%d must be < 2^24", fn, Tq,
+                Tk, q_offset);
+  if (rope_base > 0.f && (q_offset + Tq > kMaxRopePositions || Tk > kMaxRopePositions))
+    return fail(CSATTN_ERR_UNSUPPORTED,
+                "%s: RoPE supports positions < %d (q_offset + Tq = %d, Tk = %d)", fn,
+                kMaxRopePositions, q_offset + Tq, Tk);
   if (static_cast<long long>(B) * Hq > (1LL << 31) - 1)
-    return fail(CSATTN_ERR_UNSUPPORTED, "attn_fwd: B*Hq too large");
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: B*Hq too large", fn);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: q, k, v, out must be 16-byte aligned");
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: q, k, v, out must be 16-byte aligned", fn);
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_fwd: lse must be 4-byte aligned");
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: lse must be 4-byte aligned", fn);
   const size_t need =
-      k_prerotated ? 0 : csattn_fwd_workspace_size(B, Hq, Hkv, T, d, dtype, rope_base);
+      k_prerotated ? 0 : csattn_fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, dtype, rope_base);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
     return fail(CSATTN_ERR_WORKSPACE,
-                "attn_fwd: needs a 16-byte aligned workspace of %zu bytes (got %zu)", need,
+                "%s: needs a 16-byte aligned workspace of %zu bytes (got %zu)", fn, need,
                 workspace_bytes);
 
   FwdArgs a{};
@@ -199,7 +214,9 @@ int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int 
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
-  a.T = T;
+  a.Tq = Tq;
+  a.Tk = Tk;
+  a.q_off = q_offset;
   a.d = d;
   a.causal = causal;
   a.rope = rope_base > 0.f ? (rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2) : 0;
@@ -217,16 +234,37 @@ int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int 
     return CSATTN_OK;
   }
   if (tensor_map_encoder() == nullptr)
-    return fail(CSATTN_ERR_CUDA, "attn_fwd: cuTensorMapEncodeTiled is unavailable");
+    return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
   const void* k_eff = k;
   if (a.rope_k) {
-    e = launch_rope_rotate_bf16(k, workspace, B, Hkv, T, d, a.rope, a.theta, st);
+    e = launch_rope_rotate_bf16(k, workspace, B, Hkv, Tk, d, a.rope, a.theta, st);
     if (e != cudaSuccess) return fail_cuda(e, "attn_fwd: RoPE kernel launch");
     k_eff = workspace;
   }
   e = launch_fwd_sm103a(a, k_eff, st);
   if (e != cudaSuccess) return fail_cuda(e, "attn_fwd: sm_103a kernel launch");
   return CSATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                    int Hkv, int T, int d, int dtype, int causal, float rope_base,
+                    int rope_layout, float scale, float* lse, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  return attn_fwd_impl("attn_fwd", q, k, v, out, B, Hq, Hkv, T, T, 0, d, dtype, causal, rope_base,
+                       rope_layout, scale, lse, workspace, workspace_bytes, stream);
+}
+
+int csattn_attn_fwd_ext(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                        int Hkv, int Tq, int Tk, int q_offset, int d, int dtype, int causal,
+                        float rope_base, int rope_layout, float scale, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_fwd_impl("attn_fwd_ext", q, k, v, out, B, Hq, Hkv, Tq, Tk, q_offset, d, dtype,
+                       causal, rope_base, rope_layout, scale, lse, workspace, workspace_bytes,
+                       stream);
 }
 
 int csattn_rope_rotate(const void* x, void* x_rot, int B, int H, int T, int d, int dtype,

@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const float* __restri
                                                            const float* __restrict__ v,
                                                            float* __restrict__ out,
                                                            float* __restrict__ lse, int Hq,
-                                                           int Hkv, int T, int causal, int rope,
+                                                           int Hkv, int Tq, int Tk, int q_off,
+                                                           int causal, int rope,
                                                            int rope_k, float scale,
                                                            RopeTable theta) {
   using C = F32Cfg<D>;
@@ -61,21 +62,22 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const float* __restri
   const int b = blockIdx.z;
   const int g = h / (Hq / Hkv);
   const int q0 = blockIdx.x * C::ROWS;
-  const int qpos = q0 + row;
+  const int qpos = q0 + row;      // row of q / out
+  const int qabs = q_off + qpos;  // its position
 
-  const float* qh = q + ((size_t)b * Hq + h) * (size_t)T * D;
-  const float* kh = k + ((size_t)b * Hkv + g) * (size_t)T * D;
-  const float* vh = v + ((size_t)b * Hkv + g) * (size_t)T * D;
+  const float* qh = q + ((size_t)b * Hq + h) * (size_t)Tq * D;
+  const float* kh = k + ((size_t)b * Hkv + g) * (size_t)Tk * D;
+  const float* vh = v + ((size_t)b * Hkv + g) * (size_t)Tk * D;
 
   for (int e = tid; e < C::ROWS * D; e += kThreads) {
     const int r = e / D;
-    sq[e] = (q0 + r < T) ? qh[(size_t)(q0 + r) * D + (e % D)] : 0.f;
+    sq[e] = (q0 + r < Tq) ? qh[(size_t)(q0 + r) * D + (e % D)] : 0.f;
   }
   __syncthreads();
   if (rope) {
     for (int e = tid; e < C::ROWS * (D / 2); e += kThreads) {
       const int r = e / (D / 2);
-      rotate_row_f32(sq + r * D, D, e % (D / 2), rope, q0 + r, theta);
+      rotate_row_f32(sq + r * D, D, e % (D / 2), rope, q_off + q0 + r, theta);
     }
     __syncthreads();
   }
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const float* __restri
 #pragma unroll
   for (int c = 0; c < 16; ++c) acc[c] = 0.f;
 
-  const int kv_end = causal ? min(T, q0 + C::ROWS) : T;
+  const int kv_end = causal ? min(Tk, q_off + q0 + C::ROWS) : Tk;
   for (int k0 = 0; k0 < kv_end; k0 += C::KT) {
     const int nk = min(C::KT, kv_end - k0);
     __syncthreads();
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const float* __restri
 #pragma unroll
       for (int off = 1; off < C::TPR; off <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
       const int key = k0 + j;
-      if (causal && key > qpos) continue;
+      if (causal && key > qabs) continue;
       const float s = dot * scale;
       if (s > m) {
         const float corr = expf(m - s);
@@ -129,23 +131,23 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const float* __restri
     }
   }
 
-  if (qpos < T) {
+  if (qpos < Tq) {
     const float inv = 1.f / l;
-    float* o = out + (((size_t)b * Hq + h) * (size_t)T + qpos) * D + part * 16;
+    float* o = out + (((size_t)b * Hq + h) * (size_t)Tq + qpos) * D + part * 16;
 #pragma unroll
     for (int c = 0; c < 16; ++c) o[c] = acc[c] * inv;
-    if (lse != nullptr && part == 0) lse[((size_t)b * Hq + h) * (size_t)T + qpos] = m + logf(l);
+    if (lse != nullptr && part == 0) lse[((size_t)b * Hq + h) * (size_t)Tq + qpos] = m + logf(l);
   }
 }
 
 template <int D>
 cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   using C = F32Cfg<D>;
-  dim3 grid((a.T + C::ROWS - 1) / C::ROWS, a.Hq, a.B);
+  dim3 grid((a.Tq + C::ROWS - 1) / C::ROWS, a.Hq, a.B);
   fwd_f32_kernel<D><<<grid, kThreads, 0, stream>>>(
       static_cast<const float*>(a.q), static_cast<const float*>(a.k),
-      static_cast<const float*>(a.v), static_cast<float*>(a.out), a.lse, a.Hq, a.Hkv, a.T,
-      a.causal, a.rope, a.rope_k, a.scale, a.theta);
+      static_cast<const float*>(a.v), static_cast<float*>(a.out), a.lse, a.Hq, a.Hkv, a.Tq, a.Tk,
+      a.q_off, a.causal, a.rope, a.rope_k, a.scale, a.theta);
   return cudaGetLastError();
 }
 

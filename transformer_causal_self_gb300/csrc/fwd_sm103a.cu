@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++cq;
         if (p.rope) {
-          rotate_q_row<D>(x ? sQ[1] : sQ[0], row, (x ? un2.q0[1] : un2.q0[0]) + row, p.rope,
+          rotate_q_row<D>(x ? sQ[1] : sQ[0], row, p.q_off + (x ? un2.q0[1] : un2.q0[0]) + row, p.rope,
                           p.theta);
           fence_proxy_async_smem();
         }
@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // causal diagonal and ragged tail: keys beyond the row's limit get -inf
         int lim = BN - 1;
-        if (p.causal) lim = min(lim, qpos - j * BN);
-        lim = min(lim, p.T - 1 - j * BN);
+        if (p.causal) lim = min(lim, p.q_off + qpos - j * BN);
+        lim = min(lim, p.Tk - 1 - j * BN);
         if (lim < BN - 1) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
@@ -376,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++co;
       tc_fence_after();
       const float inv = 1.f / l;
-      const bool live = qpos < p.T;
+      const bool live = qpos < p.Tq;
       __nv_bfloat16* orow =
-          p.out + ((static_cast<size_t>(un.b) * p.Hq + hx) * p.T + (live ? qpos : 0)) * D;
+          p.out + ((static_cast<size_t>(un.b) * p.Hq + hx) * p.Tq + (live ? qpos : 0)) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (live && p.lse != nullptr)
-        p.lse[(static_cast<size_t>(un.b) * p.Hq + hx) * p.T + qpos] =
+        p.lse[(static_cast<size_t>(un.b) * p.Hq + hx) * p.Tq + qpos] =
             (m_used + log2f(l)) * 0.69314718055994531f;
       tc_fence_before();
       __syncwarp();
@@ -415,9 +415,9 @@ cudaError_t launch_d64(const FwdArgs& a, const void* k_eff, cudaStream_t stream)
   using C = Cfg<D>;
   const Params p = make_params(a);
   alignas(64) CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16_3d(&tq, a.q, D, a.T, a.B * a.Hq, BM) ||
-      !make_tmap_bf16_3d(&tk, k_eff, D, a.T, a.B * a.Hkv, BN) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.T, a.B * a.Hkv, BN))
+  if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, a.B * a.Hq, BM) ||
+      !make_tmap_bf16_3d(&tk, k_eff, D, a.Tk, a.B * a.Hkv, BN) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BN))
     return cudaErrorInvalidValue;
 
   cudaError_t e = cudaFuncSetAttribute(fwd_sm103a_kernel<D>,

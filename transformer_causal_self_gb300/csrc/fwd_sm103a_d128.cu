@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++cqa;
           ++cqb;
           if (p.rope) {
-            rotate_chunks(sQ[0], sQ[1], row, un2.q0[0] + row, p.rope, p.theta, x * (D / 32),
+            rotate_chunks(sQ[0], sQ[1], row, p.q_off + un2.q0[0] + row, p.rope, p.theta, x * (D / 32),
                           (x + 1) * (D / 32));
             fence_proxy_async_smem();
           }
@@ -472,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++cq;
         if (p.rope) {
-          rotate_chunks(x ? sQ[1] : sQ[0], nullptr, row, (x ? un2.q0[1] : un2.q0[0]) + row, p.rope, p.theta,
+          rotate_chunks(x ? sQ[1] : sQ[0], nullptr, row, p.q_off + (x ? un2.q0[1] : un2.q0[0]) + row,
+                        p.rope, p.theta,
                         0, D / 16);
           fence_proxy_async_smem();
         }
@@ -517,8 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_free[x]);
           int lim = BN - 1;
-          if (p.causal) lim = min(lim, qpos - j * BN);
-          lim = min(lim, p.T - 1 - j * BN);
+          if (p.causal) lim = min(lim, p.q_off + qpos - j * BN);
+          lim = min(lim, p.Tk - 1 - j * BN);
           if (!present) lim = -1;
           if (lim < BN - 1) {
 #pragma unroll
@@ -657,8 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_store_3d(&tm_o, sP + 2 * BM * 128 + x * (BM * 128), 64, q0x, z);
           bulk_commit();
         }
-        if (p.lse != nullptr && qpos < p.T)
-          p.lse[(static_cast<size_t>(un.b) * p.Hq + hx) * p.T + qpos] =
+        if (p.lse != nullptr && qpos < p.Tq)
+          p.lse[(static_cast<size_t>(un.b) * p.Hq + hx) * p.Tq + qpos] =
               (m_used + log2f(l)) * 0.69314718055994531f;
       }
       __syncwarp();
@@ -681,10 +682,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
   const Params p = make_params(a);
   alignas(64) CUtensorMap tq, tk, tv, to;
-  if (!make_tmap_bf16_3d(&tq, a.q, D, a.T, a.B * a.Hq, BM) ||
-      !make_tmap_bf16_3d(&tk, k_eff, D, a.T, a.B * a.Hkv, BN) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.T, a.B * a.Hkv, BN) ||
-      !make_tmap_bf16_3d(&to, a.out, D, a.T, a.B * a.Hq, BM))
+  if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, a.B * a.Hq, BM) ||
+      !make_tmap_bf16_3d(&tk, k_eff, D, a.Tk, a.B * a.Hkv, BN) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BN) ||
+      !make_tmap_bf16_3d(&to, a.out, D, a.Tq, a.B * a.Hq, BM))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);

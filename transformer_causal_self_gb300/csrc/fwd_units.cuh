@@ -30,11 +30,14 @@ struct Params {
   __nv_bfloat16* out;
   float* lse;
   uint32_t* status;
-  int B, Hq, Hkv, T;
+  int B, Hq, Hkv;
+  int Tq, Tk;   // query rows, key rows
+  int q_off;    // position of query row 0; keys sit at 0..Tk-1
   int rep;      // Hq / Hkv
   int hp;       // head pairs per group (rep / 2)
-  int n_qt;     // ceil(T / 128), also the number of key tiles
-  int causal;
+  int n_qt;     // ceil(Tq / 128) query tiles
+  int n_kt;     // ceil(Tk / 128) key tiles
+  int causal;   // key j visible to query row i iff j <= q_off + i
   int rope;     // 0 none, 1 split-half, 2 adjacent
   int nP;       // units made of head pairs
   int nUnits;   // all units
@@ -46,6 +49,14 @@ struct Unit {
   int b, kvh;
   int h[2], q0[2], n[2];  // per tile: head, first row, number of key tiles (n[0] <= n[1])
 };
+
+// Key tiles query tile qt reads: all of them, or (causal) up to the tile that holds
+// the position of its last row.  Never 0 (key 0 is visible to every query).
+__device__ __forceinline__ int key_tiles(const Params& p, int qt) {
+  if (!p.causal) return p.n_kt;
+  const int last = min(qt * BM + BM, p.Tq) - 1 + p.q_off;
+  return min(p.n_kt, last / BN + 1);
+}
 
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   Unit r;
@@ -61,7 +72,7 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     r.h[0] = r.kvh * p.rep + 2 * pp;
     r.h[1] = r.h[0] + 1;
     r.q0[0] = r.q0[1] = qt * BM;
-    r.n[0] = r.n[1] = p.causal ? qt + 1 : p.n_qt;
+    r.n[0] = r.n[1] = key_tiles(p, qt);
   } else {
     const int u2 = u - p.nP;
     const int npairs = (p.n_qt + 1) / 2;
@@ -75,14 +86,14 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     const int t0 = 2 * m, t1 = 2 * m + 1;
     if (t1 < p.n_qt) {
       r.q0[0] = t0 * BM;
-      r.n[0] = p.causal ? t0 + 1 : p.n_qt;
+      r.n[0] = key_tiles(p, t0);
       r.q0[1] = t1 * BM;
-      r.n[1] = p.causal ? t1 + 1 : p.n_qt;
+      r.n[1] = key_tiles(p, t1);
     } else {
       r.q0[0] = 0;
       r.n[0] = 0;
       r.q0[1] = t0 * BM;
-      r.n[1] = p.causal ? t0 + 1 : p.n_qt;
+      r.n[1] = key_tiles(p, t0);
     }
   }
   return r;
@@ -199,10 +210,13 @@ inline Params make_params(const FwdArgs& a) {
   p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
-  p.T = a.T;
+  p.Tq = a.Tq;
+  p.Tk = a.Tk;
+  p.q_off = a.q_off;
   p.rep = a.Hq / a.Hkv;
   p.hp = p.rep / 2;
-  p.n_qt = (a.T + BM - 1) / BM;
+  p.n_qt = (a.Tq + BM - 1) / BM;
+  p.n_kt = (a.Tk + BN - 1) / BN;
   p.causal = a.causal;
   p.rope = a.rope;
   p.nP = p.n_qt * a.B * a.Hkv * p.hp;

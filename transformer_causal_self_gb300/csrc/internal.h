@@ -17,8 +17,10 @@ struct FwdArgs {
   const void* v;
   void* out;
   float* lse;
-  int B, Hq, Hkv, T, d;
-  int causal;
+  int B, Hq, Hkv, d;
+  int Tq, Tk;        // query rows, key rows
+  int q_off;         // position of query row 0 (keys sit at 0..Tk-1)
+  int causal;        // 1: key j visible to query i iff j <= q_off + i
   int rope;          // 0 none, 1 split-half, 2 adjacent (applied to q)
   int rope_k;        // 1: rotate k as well; 0: k is used as given
   float scale;       // > 0
