@@ -48,7 +48,7 @@ import numpy as np
 __all__ = [
     "softmax_rows", "rope_inv_freq", "rope_cos_sin", "rope_rotate", "round_to",
     "round_to_bf16", "expand_kv_heads", "causal_additive_mask", "attention_scores",
-    "attention", "attention_rows", "attention_lse", "decode", "merge_partials",
+    "attention", "attention_rows", "attention_lse", "decode", "decode_step", "merge_partials",
     "split_partials",
 ]
 
@@ -266,6 +266,36 @@ def decode(q, k_cache, v_cache, seq_lens, scale=None):
         s = np.einsum("hd,hld->hl", qb, kb) * sc
         out[b, :, 0] = np.einsum("hl,hld->hd", softmax_rows(s), vb)
     return out
+
+
+def decode_step(q_new, k_new, v_new, k_cache, v_cache, cache_lens, *, rope_base=0.0,
+                rope_layout="split_half", scale=None, operand_dtype=None):
+    """One decode step with the new token's K/V appended to the cache first.
+
+    q_new [B, Hq, 1, d], k_new / v_new [B, Hkv, 1, d] are the new token's
+    projections, not rotated; the cache [B, Hkv, Lmax, d] holds rotated keys.
+    For sequence b the new token sits at position p = cache_lens[b] ("The
+    Transformer architecture", "Hands-on": the cache grows by one row per
+    generated token and the query at cache.pos sees keys 0..cache.pos): q and k
+    are rotated at p and rounded to ``operand_dtype``, k and v are written to
+    cache row p, and the query attends to rows 0..p.  Returns (out, k_cache',
+    v_cache') with the caches as new float64 arrays.
+    """
+    q_new = np.asarray(_as_np(q_new), dtype=np.float64)
+    k_new = np.asarray(_as_np(k_new), dtype=np.float64)
+    v_new = np.asarray(_as_np(v_new), dtype=np.float64)
+    kc = np.array(_as_np(k_cache), dtype=np.float64)
+    vc = np.array(_as_np(v_cache), dtype=np.float64)
+    B, Hq, _, d = q_new.shape
+    qr = np.empty_like(q_new)
+    lens = [int(x) for x in np.asarray(_as_np(cache_lens)).reshape(-1)]
+    for b, pos in enumerate(lens):
+        at = np.array([pos])
+        qr[b] = _rotated(q_new[b], rope_base, rope_layout, operand_dtype, at)
+        kc[b, :, pos] = _rotated(k_new[b], rope_base, rope_layout, operand_dtype, at)[:, 0]
+        vc[b, :, pos] = v_new[b, :, 0]
+    out = decode(qr, kc, vc, [L + 1 for L in lens], scale=scale)
+    return out, kc, vc
 
 
 def split_partials(s, v, bounds):

@@ -317,12 +317,46 @@ def pin_decode_is_chunk_of_one(o):
     assert np.max(np.abs(one - dec)) < 1e-12
 
 
+def pin_decode_step_appends_then_attends(o):
+    """Appending the new token's rotated key and value at row cache_len and attending
+    over rows 0..cache_len equals a one-query chunk over the whole unrotated sequence."""
+    B, Hkv, rep, d, Lmax = 3, 2, 2, 16, 40
+    lens = [0, 17, 38]
+    for dt in (None, "bf16"):
+        kc = np.full((B, Hkv, Lmax, d), np.nan)
+        vc = np.full((B, Hkv, Lmax, d), np.nan)
+        seqs = []
+        for b, L in enumerate(lens):
+            K = _rand((1, Hkv, L + 1, d), 190 + b, 2.0)
+            V = _rand((1, Hkv, L + 1, d), 195 + b)
+            Q = _rand((1, Hkv * rep, 1, d), 200 + b, 2.0)
+            kc[b, :, :L] = o.round_to(o.rope_rotate(K[0, :, :L], np.arange(L), 10000.0), dt)
+            vc[b, :, :L] = V[0, :, :L]
+            seqs.append((K, V, Q))
+        qn = np.concatenate([s_[2] for s_ in seqs])
+        kn = np.concatenate([s_[0][:, :, -1:] for s_ in seqs])
+        vn = np.concatenate([s_[1][:, :, -1:] for s_ in seqs])
+        out, kc2, vc2 = o.decode_step(qn, kn, vn, kc, vc, lens, rope_base=10000.0,
+                                      operand_dtype=dt)
+        for b, L in enumerate(lens):
+            K, V, Q = seqs[b]
+            ref = o.attention(Q, K, V, causal=True, rope_base=10000.0, operand_dtype=dt,
+                              q_offset=L)
+            assert np.max(np.abs(out[b] - ref[0])) < 1e-12, (dt, b)
+            assert np.array_equal(vc2[b, :, L], V[0, :, L])
+            rk = o.round_to(o.rope_rotate(K[0, :, L:L + 1], np.array([L]), 10000.0), dt)
+            assert np.array_equal(kc2[b, :, L], rk[:, 0])
+            assert np.all(np.isnan(kc2[b, :, L + 1:])) and np.all(np.isnan(vc2[b, :, L + 1:]))
+            assert np.array_equal(kc2[b, :, :L], kc[b, :, :L])
+
+
 ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exactly_zero,
             pin_mask_variants_differ, pin_gqa_equals_mha_repeated, pin_basis_invariance,
             pin_qq_symmetric, pin_rope_relative, pin_rope_orthogonal, pin_rope_layouts_permute,
             pin_rope_angle_formula, pin_naive_agreement, pin_degenerate_cases,
             pin_decode_equals_prefill_last_row, pin_merge_partials, pin_bf16_rounding,
-            pin_chunk_equals_full_rows, pin_chunk_naive, pin_decode_is_chunk_of_one]
+            pin_chunk_equals_full_rows, pin_chunk_naive, pin_decode_is_chunk_of_one,
+            pin_decode_step_appends_then_attends]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -362,20 +396,23 @@ class _Mutant:
         me = self
 
         def attention(q, k, v, *, causal=True, rope_base=0.0, scale=None,
-                      rope_layout="split_half", operand_dtype=None):
+                      rope_layout="split_half", operand_dtype=None, q_offset=0):
             q = np.asarray(q, np.float64)
             k = np.asarray(k, np.float64)
             v = np.asarray(v, np.float64)
             B, Hq, T, d = q.shape
+            Tk = k.shape[2]
             sc = 1 / math.sqrt(d) if (scale is None or scale <= 0) else scale
             if rope_base > 0:
-                q = me.round_to(me.rope_rotate(q, np.arange(T), rope_base, rope_layout), operand_dtype)
-                k = me.round_to(me.rope_rotate(k, np.arange(T), rope_base, rope_layout), operand_dtype)
+                q = me.round_to(me.rope_rotate(q, q_offset + np.arange(T), rope_base, rope_layout),
+                                operand_dtype)
+                k = me.round_to(me.rope_rotate(k, np.arange(Tk), rope_base, rope_layout),
+                                operand_dtype)
                 if "rope_on_v" in repl:
-                    v = me.rope_rotate(v, np.arange(T), rope_base, rope_layout)
+                    v = me.rope_rotate(v, np.arange(Tk), rope_base, rope_layout)
             kf, vf = me.expand_kv_heads(k, Hq), me.expand_kv_heads(v, Hq)
-            mask = me.causal_additive_mask(T, T) if causal else 0.0
-            out = np.empty_like(q)
+            mask = me.causal_additive_mask(T, Tk, q_offset) if causal else 0.0
+            out = np.empty((B, Hq, T, v.shape[-1]))
             for b in range(B):
                 for h in range(Hq):
                     out[b, h] = me.softmax_rows(me.attention_scores(q[b, h], kf[b, h], sc) + mask) @ vf[b, h]
@@ -521,3 +558,22 @@ def test_planted_offset_ignored_by_rope():
     def bad(q, k, v, *, q_offset=0, **kw):
         return _chunk_attention(q, k, v, q_offset, 0, **kw)
     assert _fails(_Mutant(attention=bad), [pin_chunk_equals_full_rows, pin_decode_is_chunk_of_one])
+
+
+def test_planted_decode_step_rotates_key_at_wrong_position():
+    def bad(q_new, k_new, v_new, k_cache, v_cache, cache_lens, *, rope_base=0.0,
+            rope_layout="split_half", scale=None, operand_dtype=None):
+        # the new key rotated at position cache_len + 1 instead of cache_len
+        kc = np.array(k_cache, dtype=np.float64)
+        vc = np.array(v_cache, dtype=np.float64)
+        qr = np.empty(np.shape(q_new))
+        lens = [int(x) for x in cache_lens]
+        for b, pos in enumerate(lens):
+            qr[b] = OA.round_to(OA.rope_rotate(np.asarray(q_new[b], np.float64), np.array([pos]),
+                                               rope_base, rope_layout), operand_dtype)
+            kr = OA.rope_rotate(np.asarray(k_new[b], np.float64), np.array([pos + 1]), rope_base,
+                                rope_layout)
+            kc[b, :, pos] = OA.round_to(kr, operand_dtype)[:, 0]
+            vc[b, :, pos] = np.asarray(v_new[b], np.float64)[:, 0]
+        return OA.decode(qr, kc, vc, [L + 1 for L in lens], scale=scale), kc, vc
+    assert _fails(_Mutant(decode_step=bad), [pin_decode_step_appends_then_attends])
