@@ -368,6 +368,11 @@ def run_gpu(args):
                "note": "pinned host buffers; H2D of q,k,v (+ decode q, K/V cache, seq_lens) "
                        "and D2H of both outputs inside each timed step"}
 
+    rows = None
+    if rank == 0 and not args.no_rows:
+        rows = _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_len,
+                             tf_burst, hbm_peak)
+
     if rank != 0:
         return 0
 
@@ -404,6 +409,7 @@ def run_gpu(args):
         "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "ms": round(dec_avg, 4),
                    "bytes_per_step": dbytes, "roofline": dec_roof},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "rows": rows,
         "clocks": clocks.summary(), "wall_s_timed": round(t_wall, 3),
     }
     print(json.dumps(line), flush=True)
@@ -411,6 +417,82 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_len, tf_burst,
+                  hbm_peak, reps=30):
+    """The other rows of the path, timed after (outside) the headline step.
+
+    chunked_prefill: llama_chunk_bf16 (1024 queries after a 3072-token cache) through
+    csattn_attn_fwd_ext, L2 flushed before each launch (its inputs are ~L2-sized).
+    decode_step: the decode_bf16 batch with the new token appended at row L_b - 1 and
+    rotated inside the call (csattn_attn_decode_step), attending over the same L_b rows
+    as the headline decode; its cache is > 2 GB, so no flush.
+    Each: 3 warm-up launches, then `reps` launches, each bracketed by CUDA events on the
+    launching stream; the mean is reported."""
+    out = {}
+    wc = W.WORKLOADS["llama_chunk_bf16"]
+    q, k, v = (t.to(dev) for t in W.make_chunk_inputs(wc))
+    k_rot = csattn.rope_rotate(k, rope_base=wc.rope_base, stream=stream)
+    o = torch.empty_like(q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(3 + reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csattn.attn_fwd_ext(q, k_rot, v, o, q_offset=wc.q_offset, causal=True,
+                            rope_base=wc.rope_base, scale=wc.scale, k_prerotated=True,
+                            stream=stream)
+        e1.record(stream)
+        if i >= 3:
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    csattn.check_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    tf = wc.flops() / (ms * 1e-3) / 1e12
+    out["chunked_prefill"] = {
+        "workload": "llama_chunk_bf16 (B=4, Hq=32, Hkv=8, Tq=1024 at q_offset=3072, Tk=4096, "
+                    "d=128, RoPE 1e4, keys pre-rotated)",
+        "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+        "flops": wc.flops(), "l2": "flushed before each launch",
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
+                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                     "kernel": "fwd_d128_kernel"}}
+    del q, k, v, k_rot, o, flush
+
+    g = torch.Generator()
+    g.manual_seed(7)
+    qn = torch.randn(wd.B, wd.Hq, 1, wd.d, generator=g).to(torch.bfloat16).to(dev)
+    kn = torch.randn(wd.B, wd.Hkv, 1, wd.d, generator=g).to(torch.bfloat16).to(dev)
+    vn = torch.randn(wd.B, wd.Hkv, 1, wd.d, generator=g).to(torch.bfloat16).to(dev)
+    pos = (lens - 1).to(torch.int32)
+    od = torch.empty_like(qn)
+    ws = torch.empty(csattn.decode_step_workspace_size(wd.B, wd.Hq, wd.Lmax, wd.d, 0),
+                     dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(3 + reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csattn.attn_decode_step(qn, kn, vn, kc, vc, pos, od, rope_base=10000.0, scale=wd.scale,
+                                max_seq_len=max_len, workspace=ws, stream=stream)
+        e1.record(stream)
+        if i >= 3:
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    csattn.check_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    dbytes = _decode_bytes(lens_h.tolist(), wd)
+    gbs = dbytes / (ms * 1e-3) / 1e9
+    out["decode_step"] = {
+        "workload": "decode_bf16 (B=64, Hq=32, Hkv=8, d=128, L~U[512,8192]) with the new "
+                    "token's q, k rotated (RoPE 1e4) and k, v written at row L_b - 1 in the call",
+        "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": dbytes,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "kernel": "decode_append_kernel + decode_bf16_kernel<128> + "
+                               "decode_combine_kernel"}}
+    return out
 
 
 def run_profile_case(args):
@@ -454,6 +536,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="skip the timing of the chunked-prefill and decode-step rows")
     ap.add_argument("--profile", choices=["fwd", "decode"], default=None,
                     help="run a short single-kernel case for ncu instead of the benchmark")
     args = ap.parse_args()

@@ -173,6 +173,43 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of device workspace csattn_attn_decode_step needs: the decode
+ * partials of csattn_decode_workspace_size (rounded up to 256 bytes) followed
+ * by the rotated queries, B*Hq*d*2 bytes.
+ */
+size_t csattn_decode_step_workspace_size(int B, int Hq, int Lmax, int d, int num_splits);
+
+/*
+ * One generation step with the cache append fused in ("The Transformer
+ * architecture", section "Hands-on": the cache grows by one row per
+ * generated token; the query at cache.pos sees keys 0..cache.pos; section
+ * "Now: RoPE": q and k are rotated, v is not).
+ *   q_new      [B, Hq, 1, d]   bf16, the new token's queries, NOT rotated
+ *   k_new      [B, Hkv, 1, d]  bf16, its keys, NOT rotated
+ *   v_new      [B, Hkv, 1, d]  bf16, its values
+ *   k_cache, v_cache [B, Hkv, Lmax, d] bf16, caller-owned, written in place:
+ *              row p_b = cache_lens[b] of every KV head receives RoPE_{p_b}(k_new)
+ *              (rounded to bf16) and v_new; no other row is written
+ *   cache_lens device int32 [B]: rows already cached = position of the new
+ *              token; not modified (the caller advances it)
+ *   out        [B, Hq, 1, d] bf16: attention of RoPE_{p_b}(q_new) over rows
+ *              0..p_b, the new row included
+ *   rope_base, rope_layout  as csattn_attn_fwd (rope_base <= 0: no rotation)
+ *   scale, max_seq_len, num_splits  as csattn_attn_decode, where max_seq_len
+ *              bounds cache_lens[b] + 1 (<= Lmax; <= 49152 with RoPE)
+ *   workspace  >= csattn_decode_step_workspace_size(B, Hq, Lmax, d, num_splits)
+ * Errors as csattn_attn_decode; all host-side checks run before the cache is
+ * written.  A cache_lens[b] outside [0, max_seq_len - 1] raises
+ * CSATTN_ERR_DEVICE_ARG in the status word and leaves that sequence's cache
+ * unwritten (its output is then zero).
+ */
+int csattn_attn_decode_step(const void* q_new, const void* k_new, const void* v_new,
+                            void* k_cache, void* v_cache, const int32_t* cache_lens, void* out,
+                            int B, int Hq, int Hkv, int Lmax, int d, int dtype, float rope_base,
+                            int rope_layout, float scale, int max_seq_len, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * csattn_attn_decode for callers that cannot allocate device memory (for
  * example a plugin in a framework that owns all device memory and hands out
  * no allocator, or a latency-critical loop where cudaMalloc would synchronise

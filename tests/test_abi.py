@@ -67,6 +67,9 @@ def test_workspace_sizes(lib):
     assert lib.csattn_fwd_ext_workspace_size(4, 32, 8, 1024, 4096, 128, 0, 10000.0) == 0
     assert lib.csattn_decode_workspace_size(64, 32, 8192, 128, 0) == 64 * 32 * 32 * 130 * 4
     assert lib.csattn_decode_workspace_size(2, 4, 100, 64, 5) == 2 * 4 * 5 * 66 * 4
+    # decode step: partials rounded up to 256 bytes, then the rotated queries
+    part = 2 * 4 * 5 * 66 * 4
+    assert lib.csattn_decode_step_workspace_size(2, 4, 100, 64, 5) == ((part + 255) // 256) * 256 + 2 * 4 * 64 * 2
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case below fails before any CUDA call
@@ -148,6 +151,30 @@ def test_decode_rejects_invalid_arguments(lib, kw, status):
                                 a["Hkv"], a["Lmax"], a["d"], a["dtype"], a["scale"], a["max_len"],
                                 a["splits"], a["ws"], a["ws_bytes"], None)
     assert rc == status, lib.csattn_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q_new=None), -1),
+    (dict(k_new=FAKE + 8), -1),
+    (dict(rope_layout=7), -1),
+    (dict(rope_base=float("inf")), -1),
+    (dict(max_seq_len=0), -1),
+    (dict(dtype=0), -2),
+    (dict(rope_base=10000.0, Lmax=60000, max_seq_len=50000), -2),
+    (dict(ws=FAKE, ws_bytes=64), -5),
+])
+def test_decode_step_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q_new=FAKE, k_new=FAKE, v_new=FAKE, kc=FAKE, vc=FAKE, lens=FAKE, out=FAKE, B=2, Hq=8,
+             Hkv=2, Lmax=256, d=128, dtype=1, rope_base=0.0, rope_layout=0, scale=0.0,
+             max_seq_len=256, splits=0, ws=FAKE, ws_bytes=1 << 24)
+    a.update(kw)
+    rc = lib.csattn_attn_decode_step(a["q_new"], a["k_new"], a["v_new"], a["kc"], a["vc"],
+                                     a["lens"], a["out"], a["B"], a["Hq"], a["Hkv"], a["Lmax"],
+                                     a["d"], a["dtype"], a["rope_base"], a["rope_layout"],
+                                     a["scale"], a["max_seq_len"], a["splits"], a["ws"],
+                                     a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"attn_decode_step" in lib.csattn_last_error()
 
 
 def test_selftest_rejects_bad_limit(lib):

@@ -46,6 +46,10 @@ _SIGNATURES = {
                                                                 _c_size, _vp]),
     "csattn_attn_decode_noalloc": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int,
                                                                         _vp]),
+    "csattn_decode_step_workspace_size": (_c_size, [_c_int] * 5),
+    "csattn_attn_decode_step": (_c_int, [_vp] * 7 + [_c_int] * 6 + [_c_float, _c_int, _c_float,
+                                                                    _c_int, _c_int, _vp, _c_size,
+                                                                    _vp]),
     "csattn_check_status": (_c_int, [_vp]),
     "csattn_selftest_bounded_wait": (_c_int, [_c_int, _vp]),
     "csattn_last_error": (ctypes.c_char_p, []),
@@ -119,6 +123,10 @@ def fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, dtype: torch.dtype, rope_base:
     code = CSATTN_BF16 if dtype == torch.bfloat16 else CSATTN_F32
     return int(load_library().csattn_fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, code,
                                                             float(rope_base)))
+
+
+def decode_step_workspace_size(B, Hq, Lmax, d, num_splits: int = 0) -> int:
+    return int(load_library().csattn_decode_step_workspace_size(B, Hq, Lmax, d, num_splits))
 
 
 def decode_workspace_size(B, Hq, Lmax, d, num_splits: int = 0) -> int:
@@ -234,6 +242,42 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                                   seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lmax, d,
                                   _dtype_code(q), float(scale), int(max_seq_len), int(num_splits),
                                   workspace.data_ptr(), workspace.numel(), _stream_handle(stream)))
+    return out
+
+
+def attn_decode_step(q_new: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                     k_cache: torch.Tensor, v_cache: torch.Tensor, cache_lens: torch.Tensor,
+                     out: Optional[torch.Tensor] = None, *, rope_base: float = 0.0,
+                     rope_layout: str = "split_half", scale: float = 0.0,
+                     max_seq_len: Optional[int] = None, num_splits: int = 0,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode step with the cache append fused in (C: csattn_attn_decode_step).
+
+    q_new [B,Hq,1,d], k_new/v_new [B,Hkv,1,d] not rotated; the caches are written at
+    row cache_lens[b] (int32 [B] on the device, not modified); the query attends to
+    rows 0..cache_lens[b].  max_seq_len bounds cache_lens + 1 (default Lmax).
+    """
+    _need_cuda(q_new, k_new, v_new, k_cache, v_cache, cache_lens)
+    if cache_lens.dtype != torch.int32:
+        raise TypeError("cache_lens must be int32")
+    B, Hq, _, d = q_new.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    if max_seq_len is None:
+        max_seq_len = Lmax
+    if out is None:
+        out = torch.empty_like(q_new)
+    _need_cuda(out)
+    if workspace is None:
+        workspace = torch.empty(decode_step_workspace_size(B, Hq, Lmax, d, num_splits),
+                                dtype=torch.uint8, device=q_new.device)
+    lib = load_library()
+    _check(lib.csattn_attn_decode_step(q_new.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                       k_cache.data_ptr(), v_cache.data_ptr(),
+                                       cache_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lmax, d,
+                                       _dtype_code(q_new), float(rope_base),
+                                       _ROPE_LAYOUT[rope_layout], float(scale), int(max_seq_len),
+                                       int(num_splits), workspace.data_ptr(), workspace.numel(),
+                                       _stream_handle(stream)))
     return out
 
 

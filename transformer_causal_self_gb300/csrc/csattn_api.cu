@@ -306,40 +306,56 @@ size_t csattn_decode_workspace_size(int B, int Hq, int Lmax, int d, int num_spli
   return static_cast<size_t>(B) * Hq * splits * (static_cast<size_t>(d) + 2) * 4;
 }
 
-int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
-                       const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int Lmax,
-                       int d, int dtype, float scale, int max_seq_len, int num_splits,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Host-side checks shared by both decode entry points (q may be any non-null
+// placeholder when the queries are produced on the device).
+int decode_check(const char* fn, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* seq_lens, const void* out, int B, int Hq, int Hkv, int Lmax, int d,
+                 int dtype, float scale, int max_seq_len, int num_splits) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
       out == nullptr)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: null pointer argument");
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: null pointer argument", fn);
   if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: B=%d Hq=%d Hkv=%d Lmax=%d must be >= 1",
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: B=%d Hq=%d Hkv=%d Lmax=%d must be >= 1", fn,
                 B, Hq, Hkv, Lmax);
   if (Hq % Hkv != 0)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: Hq=%d is not a multiple of Hkv=%d", Hq,
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: Hq=%d is not a multiple of Hkv=%d", fn, Hq,
                 Hkv);
   if (dtype != CSATTN_BF16)
     return fail(dtype == CSATTN_F32 ? CSATTN_ERR_UNSUPPORTED : CSATTN_ERR_INVALID_ARG,
-                "attn_decode: only bf16 is implemented (dtype %d)", dtype);
-  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "attn_decode: d=%d", d);
+                "%s: only bf16 is implemented (dtype %d)", fn, dtype);
+  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d", fn, d);
   if (Hq / Hkv > 16)
-    return fail(CSATTN_ERR_UNSUPPORTED, "attn_decode: group size %d > 16", Hq / Hkv);
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: group size %d > 16", fn, Hq / Hkv);
   if (max_seq_len < 1 || max_seq_len > Lmax)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: max_seq_len=%d not in [1, Lmax=%d]",
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: max_seq_len=%d not in [1, Lmax=%d]", fn,
                 max_seq_len, Lmax);
-  if (num_splits < 0) return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: num_splits < 0");
-  if (!std::isfinite(scale)) return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: scale not finite");
+  if (num_splits < 0) return fail(CSATTN_ERR_INVALID_ARG, "%s: num_splits < 0", fn);
+  if (!std::isfinite(scale)) return fail(CSATTN_ERR_INVALID_ARG, "%s: scale not finite", fn);
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0)
-    return fail(CSATTN_ERR_INVALID_ARG, "attn_decode: misaligned pointer");
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  return CSATTN_OK;
+}
 
-  int rc;
+// Shared by csattn_attn_decode (len_add 0) and csattn_attn_decode_step (len_add 1:
+// the appended row).
+int decode_impl(const char* fn, const void* q, const void* k_cache, const void* v_cache,
+                const int32_t* seq_lens, int len_add, void* out, int B, int Hq, int Hkv, int Lmax,
+                int d, int dtype, float scale, int max_seq_len, int num_splits, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  int rc = decode_check(fn, q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, Lmax, d, dtype, scale,
+                        max_seq_len, num_splits);
+  if (rc != CSATTN_OK) return rc;
   DecodeArgs a{};
   a.q = q;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.seq_lens = seq_lens;
+  a.len_add = len_add;
   a.out = out;
   a.B = B;
   a.Hq = Hq;
@@ -367,7 +383,7 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   const size_t need = static_cast<size_t>(B) * Hq * a.n_splits * (static_cast<size_t>(d) + 2) * 4;
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
     return fail(CSATTN_ERR_WORKSPACE,
-                "attn_decode: needs a 16-byte aligned workspace of %zu bytes (got %zu)", need,
+                "%s: needs a 16-byte aligned workspace of %zu bytes (got %zu)", fn, need,
                 workspace_bytes);
   if (a.status == nullptr) {
     rc = device_info(&a.status, &num_sms);
@@ -376,10 +392,73 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   a.part_o = static_cast<float*>(workspace);
   a.part_ml = a.part_o + static_cast<size_t>(B) * Hq * a.n_splits * d;
   if (tensor_map_encoder() == nullptr)
-    return fail(CSATTN_ERR_CUDA, "attn_decode: cuTensorMapEncodeTiled is unavailable");
+    return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
   cudaError_t e = launch_decode_bf16(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "attn_decode: kernel launch");
   return CSATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int Lmax,
+                       int d, int dtype, float scale, int max_seq_len, int num_splits,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl("attn_decode", q, k_cache, v_cache, seq_lens, 0, out, B, Hq, Hkv, Lmax, d,
+                     dtype, scale, max_seq_len, num_splits, workspace, workspace_bytes, stream);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t csattn_decode_step_workspace_size(int B, int Hq, int Lmax, int d, int num_splits) {
+  const size_t part = csattn_decode_workspace_size(B, Hq, Lmax, d, num_splits);
+  if (part == 0) return 0;
+  return align256(part) + static_cast<size_t>(B) * Hq * d * 2;  // + the rotated queries
+}
+
+int csattn_attn_decode_step(const void* q_new, const void* k_new, const void* v_new,
+                            void* k_cache, void* v_cache, const int32_t* cache_lens, void* out,
+                            int B, int Hq, int Hkv, int Lmax, int d, int dtype, float rope_base,
+                            int rope_layout, float scale, int max_seq_len, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  const char* fn = "attn_decode_step";
+  if (q_new == nullptr || k_new == nullptr || v_new == nullptr)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: q_new, k_new and v_new must be non-null", fn);
+  if (!aligned16(q_new) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown rope_layout %d", fn, rope_layout);
+  if (!std::isfinite(rope_base))
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: rope_base must be finite", fn);
+  if (rope_base > 0.f && max_seq_len > kMaxRopePositions)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: RoPE supports positions < %d, max_seq_len=%d", fn,
+                kMaxRopePositions, max_seq_len);
+  const size_t need = csattn_decode_step_workspace_size(B, Hq, Lmax, d, num_splits);
+  if (need == 0 || workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return fail(CSATTN_ERR_WORKSPACE,
+                "%s: needs a 16-byte aligned workspace of %zu bytes (got %zu)", fn, need,
+                workspace_bytes);
+  const size_t q_at = need - static_cast<size_t>(B) * Hq * d * 2;
+  void* q_rot = static_cast<uint8_t*>(workspace) + q_at;
+  // every check of the decode runs before the cache is written
+  int rc = decode_check(fn, q_rot, k_cache, v_cache, cache_lens, out, B, Hq, Hkv, Lmax, d, dtype,
+                        scale, max_seq_len, num_splits);
+  if (rc != CSATTN_OK) return rc;
+  RopeTable th{};
+  const int rope = rope_base > 0.f ? (rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2) : 0;
+  if (rope) rope_table(&th, d, static_cast<double>(rope_base));
+  uint32_t* status = nullptr;
+  int num_sms = 0;
+  rc = device_info(&status, &num_sms);
+  if (rc != CSATTN_OK) return rc;
+  cudaError_t e = launch_decode_append_bf16(q_new, k_new, v_new, k_cache, v_cache, cache_lens,
+                                            q_rot, B, Hq, Hkv, Lmax, d, max_seq_len, rope, th,
+                                            status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "attn_decode_step: append kernel launch");
+  return decode_impl(fn, q_rot, k_cache, v_cache, cache_lens, 1, out, B, Hq, Hkv, Lmax, d, dtype,
+                     scale, max_seq_len, num_splits, workspace, q_at, stream);
 }
 
 int csattn_check_status(void* stream) {

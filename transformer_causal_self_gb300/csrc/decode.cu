@@ -44,6 +44,7 @@ struct DCfg {
 struct DParams {
   const __nv_bfloat16* q;
   const int32_t* seq_lens;
+  int len_add;
   float* part_o;
   float* part_ml;
   uint32_t* status;
@@ -96,7 +97,8 @@ __global__ void __launch_bounds__(kThreads)
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  int L = p.seq_lens[b];
+  const int raw = p.seq_lens[b];  // (no overflow in raw + len_add past max_seq_len)
+  int L = raw > p.max_seq_len ? p.max_seq_len + 1 : raw + p.len_add;
   if (L < 1 || L > p.max_seq_len) {
     if (threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(p.status, kStatusDeviceArg);
     L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
@@ -331,14 +333,15 @@ __global__ void __launch_bounds__(kThreads)
 // out[b, h, :] = merge of the splits that hold keys of sequence b.
 __global__ void decode_combine_kernel(const float* __restrict__ part_o,
                                       const float* __restrict__ part_ml,
-                                      const int32_t* __restrict__ seq_lens,
+                                      const int32_t* __restrict__ seq_lens, int len_add,
                                       __nv_bfloat16* __restrict__ out, int Hq, int n_splits,
                                       int chunk, int max_seq_len, int D) {
   // wait until the split kernel has finished and its partials are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bh = blockIdx.x;
   const int b = bh / Hq;
-  int L = seq_lens[b];
+  const int raw = seq_lens[b];
+  int L = raw > max_seq_len ? max_seq_len : raw + len_add;
   L = L < 0 ? 0 : (L > max_seq_len ? max_seq_len : L);
   const int ns = (L + chunk - 1) / chunk;
   const float* ml = part_ml + static_cast<size_t>(bh) * n_splits * 2;
@@ -365,6 +368,7 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   DParams p{};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.seq_lens = a.seq_lens;
+  p.len_add = a.len_add;
   p.part_o = a.part_o;
   p.part_ml = a.part_ml;
   p.status = a.status;
@@ -399,7 +403,7 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float*>(a.part_o),
-                            static_cast<const float*>(a.part_ml), a.seq_lens,
+                            static_cast<const float*>(a.part_ml), a.seq_lens, a.len_add,
                             static_cast<__nv_bfloat16*>(a.out), a.Hq, a.n_splits, a.chunk,
                             a.max_seq_len, D);
 }

@@ -46,6 +46,7 @@ struct DecodeArgs {
   const void* k_cache;
   const void* v_cache;
   const int32_t* seq_lens;
+  int len_add;     // sequence b has seq_lens[b] + len_add cached rows
   void* out;
   int B, Hq, Hkv, Lmax, d;
   float scale;
@@ -58,6 +59,17 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream);
+
+// One decode step's cache append: for sequence b at position p = cache_lens[b],
+// q_rot[b,h] = RoPE_p(q_new[b,h]) for every query head, k_cache[b,g,p] =
+// RoPE_p(k_new[b,g]) and v_cache[b,g,p] = v_new[b,g] for every KV head (rope
+// 0: no rotation).  A position outside [0, max_pos) sets kStatusDeviceArg in
+// *status and writes nothing for that sequence.
+cudaError_t launch_decode_append_bf16(const void* q_new, const void* k_new, const void* v_new,
+                                      void* k_cache, void* v_cache, const int32_t* cache_lens,
+                                      void* q_rot, int B, int Hq, int Hkv, int Lmax, int d,
+                                      int max_pos, int rope, const RopeTable& theta,
+                                      uint32_t* status, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
