@@ -48,8 +48,8 @@ import numpy as np
 __all__ = [
     "softmax_rows", "rope_inv_freq", "rope_cos_sin", "rope_rotate", "round_to",
     "round_to_bf16", "expand_kv_heads", "causal_additive_mask", "attention_scores",
-    "attention", "attention_rows", "attention_lse", "decode", "decode_step", "merge_partials",
-    "split_partials",
+    "attention", "attention_rows", "attention_lse", "attention_backward", "decode",
+    "decode_step", "merge_partials", "split_partials", "rope_rotate_transpose",
 ]
 
 _BF16_MAX = float.fromhex("0x1.fep127")
@@ -296,6 +296,78 @@ def decode_step(q_new, k_new, v_new, k_cache, v_cache, cache_lens, *, rope_base=
         vc[b, :, pos] = v_new[b, :, 0]
     out = decode(qr, kc, vc, [L + 1 for L in lens], scale=scale)
     return out, kc, vc
+
+
+def rope_rotate_transpose(x, positions, base: float, layout: str = "split_half"):
+    """R_pos^T x, the transpose (= inverse) of ``rope_rotate``'s rotation: the
+    chain rule applies it to a gradient flowing back through RoPE.
+
+    Pair (a, b) becomes (a cos + b sin, -a sin + b cos).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    c, s = rope_cos_sin(positions, d, base)
+    out = np.empty_like(x)
+    if layout == "split_half":
+        a, b = x[..., : d // 2], x[..., d // 2:]
+        out[..., : d // 2] = a * c + b * s
+        out[..., d // 2:] = -a * s + b * c
+    elif layout == "adjacent":
+        a, b = x[..., 0::2], x[..., 1::2]
+        out[..., 0::2] = a * c + b * s
+        out[..., 1::2] = -a * s + b * c
+    else:
+        raise ValueError(f"unknown RoPE layout {layout!r}")
+    return out
+
+
+def attention_backward(q, k, v, dout, *, causal=True, rope_base=0.0, scale=None,
+                       rope_layout="split_half", operand_dtype=None, q_offset=0):
+    """Gradients (dq, dk, dv) of sum(out * dout) for out = attention(q, k, v, ...).
+
+    The derivative of the definition above, written out (float64):
+      P = softmax(S + M),  S = scale * Qr Kr^T,  O = P V          (per query head)
+      dV_g  = sum over the heads h of group g of P_h^T dO_h
+      dP    = dO V^T;  dS = P o (dP - D),  D_i = sum_c dO_ic O_ic  (softmax Jacobian)
+      dQr   = scale * dS Kr;  dKr_g = scale * sum_h dS_h^T Qr_h
+      dq    = R^T dQr,  dk = R^T dKr   (RoPE is a rotation: its Jacobian is R)
+    Rounding of the rotated operands to ``operand_dtype`` is part of the forward;
+    the backward treats it as the identity (its derivative is zero almost
+    everywhere, which no training step uses), so the gradients are those of the
+    unrounded function evaluated at the rounded operands.
+    """
+    q = np.asarray(_as_np(q), dtype=np.float64)
+    k = np.asarray(_as_np(k), dtype=np.float64)
+    v = np.asarray(_as_np(v), dtype=np.float64)
+    do = np.asarray(_as_np(dout), dtype=np.float64)
+    B, Hq, T, d = q.shape
+    Hkv, Tk = k.shape[1], k.shape[2]
+    rep = Hq // Hkv
+    sc = _default_scale(d, scale)
+    qpos = int(q_offset) + np.arange(T)
+    kpos = np.arange(Tk)
+    qr = _rotated(q, rope_base, rope_layout, operand_dtype, qpos)
+    kr = _rotated(k, rope_base, rope_layout, operand_dtype, kpos)
+    mask = causal_additive_mask(T, Tk, q_offset) if causal else np.zeros((T, Tk))
+    dqr = np.zeros_like(qr)
+    dkr = np.zeros_like(kr)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // rep
+            p = softmax_rows(attention_scores(qr[b, h], kr[b, g], sc) + mask)
+            o = p @ v[b, g]
+            dv[b, g] += p.T @ do[b, h]
+            dp = do[b, h] @ v[b, g].T
+            dsc = p * (dp - np.sum(do[b, h] * o, axis=-1, keepdims=True))
+            dqr[b, h] = sc * (dsc @ kr[b, g])
+            dkr[b, g] += sc * (dsc.T @ qr[b, h])
+    if rope_base is not None and rope_base > 0:
+        dq = rope_rotate_transpose(dqr, qpos, rope_base, rope_layout)
+        dk = rope_rotate_transpose(dkr, kpos, rope_base, rope_layout)
+    else:
+        dq, dk = dqr, dkr
+    return dq, dk, dv
 
 
 def split_partials(s, v, bounds):

@@ -350,13 +350,100 @@ def pin_decode_step_appends_then_attends(o):
             assert np.array_equal(kc2[b, :, :L], kc[b, :, :L])
 
 
+def _fd_grads(o, q, k, v, do, kw, h=1e-6):
+    """Central finite differences of sum(attention(q, k, v) * do) in float64."""
+    def f(a, b, c):
+        return float(np.sum(o.attention(a, b, c, **kw) * do))
+    grads = []
+    for which in range(3):
+        args = [q, k, v]
+        x = args[which]
+        gx = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            ap, am = list(args), list(args)
+            ap[which], am[which] = xp, xm
+            gx[idx] = (f(*ap) - f(*am)) / (2 * h)
+        grads.append(gx)
+    return grads
+
+
+def pin_backward_finite_differences(o):
+    """The gradients of the backward agree with central differences of the forward."""
+    cases = [dict(Hq=4, Hkv=2, T=7, d=8, kw=dict(causal=True, rope_base=100.0, scale=0.4)),
+             dict(Hq=2, Hkv=1, T=6, d=4, kw=dict(causal=False, rope_base=50.0, scale=0.7,
+                                                 rope_layout="adjacent")),
+             dict(Hq=2, Hkv=2, T=5, d=4, kw=dict(causal=True, rope_base=0.0, scale=0.5))]
+    for i, c in enumerate(cases):
+        q = _rand((1, c["Hq"], c["T"], c["d"]), 210 + i)
+        k = _rand((1, c["Hkv"], c["T"], c["d"]), 220 + i)
+        v = _rand((1, c["Hkv"], c["T"], c["d"]), 230 + i)
+        do = _rand((1, c["Hq"], c["T"], c["d"]), 240 + i)
+        got = o.attention_backward(q, k, v, do, **c["kw"])
+        num = _fd_grads(o, q, k, v, do, c["kw"])
+        for name, a, b in zip("qkv", got, num):
+            assert np.max(np.abs(a - b)) < 1e-7, (i, name, np.max(np.abs(a - b)))
+    # a chunk at an offset: the query rotation and the mask both move
+    q = _rand((1, 2, 4, 8), 250)
+    k = _rand((1, 1, 9, 8), 251)
+    v = _rand((1, 1, 9, 8), 252)
+    do = _rand((1, 2, 4, 8), 253)
+    kw = dict(causal=True, rope_base=100.0, scale=0.45, q_offset=5)
+    got = o.attention_backward(q, k, v, do, **kw)
+    for name, a, b in zip("qkv", got, _fd_grads(o, q, k, v, do, kw)):
+        assert np.max(np.abs(a - b)) < 1e-7, ("offset", name)
+
+
+def pin_backward_autograd(o):
+    """Against torch autograd (float64) of a forward written here with plain torch ops."""
+    B, Hq, Hkv, T, d, base, sc = 2, 6, 2, 33, 16, 10000.0, 0.3
+    q = torch.tensor(_rand((B, Hq, T, d), 260), requires_grad=True)
+    k = torch.tensor(_rand((B, Hkv, T, d), 261), requires_grad=True)
+    v = torch.tensor(_rand((B, Hkv, T, d), 262), requires_grad=True)
+    do = torch.tensor(_rand((B, Hq, T, d), 263))
+    pos = torch.arange(T, dtype=torch.float64)
+    ang = pos[:, None] * base ** (-torch.arange(0, d, 2, dtype=torch.float64) / d)[None, :]
+    cos, sin = torch.cos(ang), torch.sin(ang)
+
+    def rot(x):
+        a, b = x[..., : d // 2], x[..., d // 2:]
+        return torch.cat([a * cos - b * sin, a * sin + b * cos], dim=-1)
+
+    kf = rot(k).repeat_interleave(Hq // Hkv, dim=1)
+    vf = v.repeat_interleave(Hq // Hkv, dim=1)
+    s_ = rot(q) @ kf.transpose(-1, -2) * sc
+    s_ = s_.masked_fill(torch.triu(torch.ones(T, T, dtype=torch.bool), 1), float("-inf"))
+    out = torch.softmax(s_, dim=-1) @ vf
+    (out * do).sum().backward()
+    got = o.attention_backward(q.detach().numpy(), k.detach().numpy(), v.detach().numpy(),
+                               do.numpy(), causal=True, rope_base=base, scale=sc)
+    for a, t in zip(got, (q.grad, k.grad, v.grad)):
+        assert np.max(np.abs(a - t.numpy())) < 1e-12
+
+
+def pin_rope_transpose_inverts(o):
+    x = _rand((3, 11, 16), 270)
+    y = _rand((3, 11, 16), 271)
+    pos = np.arange(11) * 37
+    for layout in ("split_half", "adjacent"):
+        r = o.rope_rotate(x, pos, 10000.0, layout)
+        assert np.max(np.abs(o.rope_rotate_transpose(r, pos, 10000.0, layout) - x)) < 1e-13
+        # <R x, y> = <x, R^T y>
+        lhs = np.sum(r * y)
+        rhs = np.sum(x * o.rope_rotate_transpose(y, pos, 10000.0, layout))
+        assert abs(lhs - rhs) < 1e-10
+
+
 ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exactly_zero,
             pin_mask_variants_differ, pin_gqa_equals_mha_repeated, pin_basis_invariance,
             pin_qq_symmetric, pin_rope_relative, pin_rope_orthogonal, pin_rope_layouts_permute,
             pin_rope_angle_formula, pin_naive_agreement, pin_degenerate_cases,
             pin_decode_equals_prefill_last_row, pin_merge_partials, pin_bf16_rounding,
             pin_chunk_equals_full_rows, pin_chunk_naive, pin_decode_is_chunk_of_one,
-            pin_decode_step_appends_then_attends]
+            pin_decode_step_appends_then_attends, pin_backward_finite_differences,
+            pin_backward_autograd, pin_rope_transpose_inverts]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -577,3 +664,57 @@ def test_planted_decode_step_rotates_key_at_wrong_position():
             vc[b, :, pos] = np.asarray(v_new[b], np.float64)[:, 0]
         return OA.decode(qr, kc, vc, [L + 1 for L in lens], scale=scale), kc, vc
     assert _fails(_Mutant(decode_step=bad), [pin_decode_step_appends_then_attends])
+
+
+def _backward_variant(drop_d=False, last_head_only=False, forward_rotation=False):
+    """The oracle's backward with one planted mistake."""
+    def bwd(q, k, v, dout, *, causal=True, rope_base=0.0, scale=None, rope_layout="split_half",
+            operand_dtype=None, q_offset=0):
+        q, k, v, do = (np.asarray(t, np.float64) for t in (q, k, v, dout))
+        B, Hq, T, d = q.shape
+        Hkv, Tk = k.shape[1], k.shape[2]
+        rep = Hq // Hkv
+        sc = 1 / math.sqrt(d) if (scale is None or scale <= 0) else scale
+        qpos, kpos = q_offset + np.arange(T), np.arange(Tk)
+        qr = OA.rope_rotate(q, qpos, rope_base, rope_layout) if rope_base > 0 else q
+        kr = OA.rope_rotate(k, kpos, rope_base, rope_layout) if rope_base > 0 else k
+        mask = OA.causal_additive_mask(T, Tk, q_offset) if causal else 0.0
+        dqr, dkr, dv = np.zeros_like(qr), np.zeros_like(kr), np.zeros_like(v)
+        for b in range(B):
+            for h in range(Hq):
+                g = h // rep
+                p = OA.softmax_rows(OA.attention_scores(qr[b, h], kr[b, g], sc) + mask)
+                o = p @ v[b, g]
+                keep = (h % rep == rep - 1) or not last_head_only
+                if keep:
+                    dv[b, g] += p.T @ do[b, h]
+                dp = do[b, h] @ v[b, g].T
+                dsc = p * dp if drop_d else p * (dp - np.sum(do[b, h] * o, -1, keepdims=True))
+                dqr[b, h] = sc * dsc @ kr[b, g]
+                if keep:
+                    dkr[b, g] += sc * dsc.T @ qr[b, h]
+        back = OA.rope_rotate if forward_rotation else OA.rope_rotate_transpose
+        if rope_base > 0:
+            return back(dqr, qpos, rope_base, rope_layout), back(dkr, kpos, rope_base, rope_layout), dv
+        return dqr, dkr, dv
+    return bwd
+
+
+def test_backward_variant_helper_is_faithful():
+    assert _fails(_Mutant(attention_backward=_backward_variant()),
+                  [pin_backward_finite_differences, pin_backward_autograd]) == []
+
+
+def test_planted_backward_drops_softmax_correction():
+    assert _fails(_Mutant(attention_backward=_backward_variant(drop_d=True)),
+                  [pin_backward_finite_differences])
+
+
+def test_planted_backward_misses_gqa_sum():
+    assert _fails(_Mutant(attention_backward=_backward_variant(last_head_only=True)),
+                  [pin_backward_finite_differences, pin_backward_autograd])
+
+
+def test_planted_backward_rotates_forward():
+    assert _fails(_Mutant(attention_backward=_backward_variant(forward_rotation=True)),
+                  [pin_backward_finite_differences, pin_backward_autograd])
