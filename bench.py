@@ -492,6 +492,38 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
                      "frac": round(gbs / hbm_peak, 4), "traffic": None,
                      "kernel": "decode_append_kernel + decode_bf16_kernel<128> + "
                                "decode_combine_kernel"}}
+    # backward of the headline prefill (dq, dk, dv), FLOPs = 2.5x the forward's (the
+    # convention for QK^T recomputation + dV + dP + dQ + dK)
+    wp = W.WORKLOADS["llama_gqa_bf16"]
+    q, k, v = (t.to(dev) for t in W.make_prefill_inputs(wp))
+    g.manual_seed(8)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
+    lse = torch.empty(wp.B, wp.Hq, wp.T, dtype=torch.float32, device=dev)
+    o = csattn.attn_fwd(q, k, v, causal=True, rope_base=wp.rope_base, scale=wp.scale, lse=lse,
+                        stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(csattn.bwd_workspace_size(wp.B, wp.Hq, wp.Hkv, wp.T, wp.d, q.dtype,
+                                               wp.rope_base), dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(3 + max(3, reps // 5)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csattn.attn_bwd(q, k, v, o, do, lse, causal=True, rope_base=wp.rope_base, scale=wp.scale,
+                        dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+        e1.record(stream)
+        if i >= 3:
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    csattn.check_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    fl = 2.5 * wp.flops()
+    tf = fl / (ms * 1e-3) / 1e12
+    out["backward"] = {
+        "workload": "llama_gqa_bf16 backward (dq, dk, dv; RoPE 1e4; inputs larger than L2)",
+        "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": fl,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
+                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                     "kernel": "bwd_dkdv_kernel<128> + bwd_dq_kernel<128> (mma.sync)"}}
     return out
 
 

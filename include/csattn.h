@@ -133,6 +133,38 @@ int csattn_attn_fwd_ext(const void* q, const void* k, const void* v, void* out, 
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of device workspace csattn_attn_bwd needs: fp32 rowsum(dout o out)
+ * [B, Hq, T] plus, with RoPE, the rotated q and k (each block 256-byte aligned).
+ */
+size_t csattn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,
+                                 float rope_base);
+
+/*
+ * Backward of csattn_attn_fwd: the gradients of sum(out * dout) with respect to
+ * q, k and v.  Written out from the forward's definition ("The Transformer
+ * architecture", "Scaled dot-product attention", "Now: RoPE"):
+ *   P = exp(S - lse), S = scale * RoPE(q) RoPE(k)^T + M;  D = rowsum(dout o out)
+ *   dv = sum over the group's query heads of P^T dout
+ *   dS = P o (dout v^T - D)
+ *   dq = R^T (scale * dS RoPE(k)),  dk = R^T (scale * sum over heads of dS^T RoPE(q))
+ * with R the rotation at each row's position (R^T = R^-1).  The rounding of the
+ * rotated operands in the forward is taken as the identity.
+ *   q, k, v, causal, rope_base, rope_layout, scale   the forward's arguments
+ *   out   [B, Hq, T, d]  the forward's output;  dout [B, Hq, T, d] its gradient
+ *   lse   fp32 [B, Hq, T] the forward's natural-log log-sum-exp (its lse output)
+ *   dq [B, Hq, T, d], dk, dv [B, Hkv, T, d]  written, same dtype as q
+ *   workspace  >= csattn_bwd_workspace_size() bytes, caller-owned
+ * Requirements: bf16 (CSATTN_ERR_UNSUPPORTED for fp32), d in {64, 128},
+ * Hq % Hkv == 0, T < 2^24 (T <= 49152 with RoPE); all pointers 16-byte aligned
+ * (lse 4-byte).  Asynchronous on `stream`.
+ */
+int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                    int Hq, int Hkv, int T, int d, int dtype, int causal, float rope_base,
+                    int rope_layout, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
  * RoPE of x [B, H, T, d] into x_rot (same shape; must not overlap x), at
  * positions 0..T-1 with theta_p = rope_base^(-2p/d), rounded to the input
  * dtype.  This is the rotation csattn_attn_fwd applies to its keys, exposed to

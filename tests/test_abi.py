@@ -177,6 +177,38 @@ def test_decode_step_rejects_invalid_arguments(lib, kw, status):
     assert b"attn_decode_step" in lib.csattn_last_error()
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(lse=None), -1),
+    (dict(T=0), -1),
+    (dict(Hq=6, Hkv=4), -1),
+    (dict(dtype=0), -2),
+    (dict(d=32), -2),
+    (dict(causal=3), -1),
+    (dict(dq=FAKE + 4), -1),
+    (dict(rope_base=10000.0, T=50000), -2),
+    (dict(ws=None, ws_bytes=0), -5),
+])
+def test_bwd_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, dout=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             B=1, Hq=4, Hkv=2, T=64, d=128, dtype=1, causal=1, rope_base=0.0, rope_layout=0,
+             scale=0.0, ws=FAKE, ws_bytes=1 << 24)
+    a.update(kw)
+    rc = lib.csattn_attn_bwd(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"], a["dq"],
+                             a["dk"], a["dv"], a["B"], a["Hq"], a["Hkv"], a["T"], a["d"],
+                             a["dtype"], a["causal"], a["rope_base"], a["rope_layout"],
+                             a["scale"], a["ws"], a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+
+
+def test_bwd_workspace_size(lib):
+    rows = 4 * 32 * 4096
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert lib.csattn_bwd_workspace_size(4, 32, 8, 4096, 128, 1, 0.0) == al(rows * 4)
+    assert lib.csattn_bwd_workspace_size(4, 32, 8, 4096, 128, 1, 10000.0) == \
+        al(rows * 4) + al(rows * 128 * 2) + al(4 * 8 * 4096 * 128 * 2)
+    assert lib.csattn_bwd_workspace_size(4, 32, 8, 4096, 128, 0, 10000.0) == 0
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.csattn_selftest_bounded_wait(0, None) == -1
     assert lib.csattn_selftest_bounded_wait(2000000, None) == -1

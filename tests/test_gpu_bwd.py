@@ -1,0 +1,107 @@
+"""Backward parity: dq, dk, dv from csattn_attn_bwd against the float64 oracle's
+gradients (oracle.attn.attention_backward) on the same bf16 inputs.
+
+Tolerance.  The kernels round P and dS to bf16 for the tensor-core products
+(relative error <= 2^-9 each, independent across terms) and accumulate in fp32,
+and take out and lse from the bf16 forward; the gradients are sums of many such
+terms, so their relative L2 error is a few 2^-9 ~ 2e-3.  Bound: relative L2
+<= 1e-2 and max-abs <= 2e-2 * max(1, max |ref|) per tensor."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_workloads as W
+import transformer_causal_self_gb300 as csattn
+from oracle import attn as OA
+from tests.gpu_helpers import dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _close(got, ref, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite"
+    err = float(np.max(np.abs(got - ref)))
+    rl2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+    assert rl2 <= 1e-2 and err <= 2e-2 * max(1.0, float(np.max(np.abs(ref)))), \
+        f"{what}: max-abs {err:.3e} (ref max {np.max(np.abs(ref)):.3e}), rel-L2 {rl2:.3e}"
+
+
+def _run(q, k, v, do, causal, base, layout, scale):
+    qd, kd, vd, dod = (t.to(dev()) for t in (q, k, v, do))
+    B, Hq, T, d = q.shape
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev())
+    out = csattn.attn_fwd(qd, kd, vd, causal=causal, rope_base=base, rope_layout=layout,
+                          scale=scale, lse=lse)
+    dq, dk, dv = csattn.attn_bwd(qd, kd, vd, out, dod, lse, causal=causal, rope_base=base,
+                                 rope_layout=layout, scale=scale)
+    csattn.check_status()
+    return dq, dk, dv
+
+
+CASES = [
+    # (B, Hq, Hkv, T, d, causal, rope_base, layout)
+    (2, 4, 2, 200, 128, True, 10000.0, "split_half"),
+    (1, 3, 3, 130, 64, False, 10000.0, "adjacent"),
+    (2, 8, 1, 64, 128, True, 0.0, "split_half"),
+    (1, 2, 1, 1, 128, True, 10000.0, "split_half"),
+    (1, 4, 4, 257, 64, True, 500000.0, "split_half"),
+    (1, 6, 2, 96, 128, False, 0.0, "split_half"),
+]
+
+
+@pytest.mark.parametrize("B,hq,hkv,T,d,causal,base,layout", CASES)
+def test_bwd_parity(B, hq, hkv, T, d, causal, base, layout):
+    w = W.PrefillWorkload("bwd", B=B, Hq=hq, Hkv=hkv, T=T, d=d, dtype="bf16", rope_base=base,
+                          scale=1.0 / math.sqrt(d), causal=causal, seed=T + d + hq)
+    q, k, v = W.make_prefill_inputs(w)
+    g = torch.Generator()
+    g.manual_seed(T)
+    do = torch.randn(B, hq, T, d, generator=g).to(torch.bfloat16)
+    dq, dk, dv = _run(q, k, v, do, causal, base, layout, w.scale)
+    rq, rk, rv = OA.attention_backward(q, k, v, do, causal=causal, rope_base=base, scale=w.scale,
+                                       rope_layout=layout, operand_dtype="bf16")
+    _close(to_np(dq), rq, "dq")
+    _close(to_np(dk), rk, "dk")
+    _close(to_np(dv), rv, "dv")
+
+
+def test_bwd_llama_workload_one_group():
+    """Full-size workload; one KV group (4 query heads) of one batch entry checked."""
+    w = W.WORKLOADS["llama_gqa_bf16"]
+    q, k, v = W.make_prefill_inputs(w)
+    g = torch.Generator()
+    g.manual_seed(99)
+    do = torch.randn(w.B, w.Hq, w.T, w.d, generator=g).to(torch.bfloat16)
+    dq, dk, dv = _run(q, k, v, do, True, w.rope_base, "split_half", w.scale)
+    b, grp = 2, 5
+    rep = w.Hq // w.Hkv
+    hs = slice(grp * rep, (grp + 1) * rep)
+    rq, rk, rv = OA.attention_backward(q[b:b + 1, hs], k[b:b + 1, grp:grp + 1],
+                                       v[b:b + 1, grp:grp + 1], do[b:b + 1, hs], causal=True,
+                                       rope_base=w.rope_base, scale=w.scale, operand_dtype="bf16")
+    _close(to_np(dq[b:b + 1, hs]), rq, "dq group")
+    _close(to_np(dk[b:b + 1, grp:grp + 1]), rk, "dk group")
+    _close(to_np(dv[b:b + 1, grp:grp + 1]), rv, "dv group")
+
+
+def test_bwd_gqa_equals_summed_mha():
+    """dk, dv of a GQA group equal the sums over its heads of the MHA gradients on repeated
+    K/V (the group sum the kernel does in registers)."""
+    B, Hq, Hkv, T, d = 1, 4, 1, 150, 128
+    w = W.PrefillWorkload("g", B=B, Hq=Hq, Hkv=Hkv, T=T, d=d, dtype="bf16", rope_base=10000.0,
+                          scale=1.0 / math.sqrt(d), seed=7)
+    q, k, v = W.make_prefill_inputs(w)
+    g = torch.Generator()
+    g.manual_seed(8)
+    do = torch.randn(B, Hq, T, d, generator=g).to(torch.bfloat16)
+    dq, dk, dv = _run(q, k, v, do, True, w.rope_base, "split_half", w.scale)
+    dq2, dk2, dv2 = _run(q, k.repeat_interleave(Hq, 1).contiguous(),
+                         v.repeat_interleave(Hq, 1).contiguous(), do, True, w.rope_base,
+                         "split_half", w.scale)
+    _close(to_np(dq), to_np(dq2), "dq gqa vs mha")
+    _close(to_np(dk), to_np(dk2).sum(axis=1, keepdims=True), "dk gqa vs summed mha")
+    _close(to_np(dv), to_np(dv2).sum(axis=1, keepdims=True), "dv gqa vs summed mha")

@@ -40,6 +40,9 @@ _SIGNATURES = {
     "csattn_attn_fwd_ext": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 9 + [_c_float, _c_int,
                                                                             _c_float, _vp, _vp,
                                                                             _c_size, _vp]),
+    "csattn_bwd_workspace_size": (_c_size, [_c_int] * 6 + [_c_float]),
+    "csattn_attn_bwd": (_c_int, [_vp] * 9 + [_c_int] * 7 + [_c_float, _c_int, _c_float, _vp,
+                                                             _c_size, _vp]),
     "csattn_rope_rotate": (_c_int, [_vp, _vp] + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "csattn_decode_workspace_size": (_c_size, [_c_int] * 5),
     "csattn_attn_decode": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp,
@@ -123,6 +126,11 @@ def fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, dtype: torch.dtype, rope_base:
     code = CSATTN_BF16 if dtype == torch.bfloat16 else CSATTN_F32
     return int(load_library().csattn_fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, code,
                                                             float(rope_base)))
+
+
+def bwd_workspace_size(B, Hq, Hkv, T, d, dtype: torch.dtype, rope_base: float) -> int:
+    code = CSATTN_BF16 if dtype == torch.bfloat16 else CSATTN_F32
+    return int(load_library().csattn_bwd_workspace_size(B, Hq, Hkv, T, d, code, float(rope_base)))
 
 
 def decode_step_workspace_size(B, Hq, Lmax, d, num_splits: int = 0) -> int:
@@ -213,6 +221,34 @@ def attn_fwd_ext(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                    float(scale), lse.data_ptr() if lse is not None else None,
                                    ws_ptr, ws_bytes, _stream_handle(stream)))
     return out
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+             dout: torch.Tensor, lse: torch.Tensor, *, causal: bool = True,
+             rope_base: float = 0.0, scale: float = 0.0, rope_layout: str = "split_half",
+             dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+             dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+             stream=None):
+    """Gradients (dq, dk, dv) of sum(out * dout) (C: csattn_attn_bwd).
+
+    out and lse are the forward's outputs for the same arguments (lse fp32 [B,Hq,T]).
+    """
+    _need_cuda(q, k, v, out, dout, lse)
+    B, Hq, T, d = q.shape
+    Hkv = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        n = bwd_workspace_size(B, Hq, Hkv, T, d, q.dtype, rope_base)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    lib = load_library()
+    _check(lib.csattn_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), B, Hq, Hkv, T, d, _dtype_code(q), int(bool(causal)),
+                               float(rope_base), _ROPE_LAYOUT[rope_layout], float(scale),
+                               workspace.data_ptr(), workspace.numel(), _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

@@ -267,6 +267,99 @@ int csattn_attn_fwd_ext(const void* q, const void* k, const void* v, void* out, 
                        stream);
 }
 
+size_t csattn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,
+                                 float rope_base) {
+  if (dtype != CSATTN_BF16 || B < 1 || Hq < 1 || Hkv < 1 || T < 1 || d < 1) return 0;
+  auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t rows = static_cast<size_t>(B) * Hq * T;
+  size_t bytes = al(rows * 4);  // rowsum(dout o out), fp32
+  if (rope_base > 0.f)          // rotated q and k
+    bytes += al(rows * d * 2) + al(static_cast<size_t>(B) * Hkv * T * d * 2);
+  return bytes;
+}
+
+int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                    int Hq, int Hkv, int T, int d, int dtype, int causal, float rope_base,
+                    int rope_layout, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  const char* fn = "attn_bwd";
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || dout == nullptr ||
+      lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: null pointer argument", fn);
+  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: B=%d Hq=%d Hkv=%d T=%d must be >= 1", fn, B, Hq,
+                Hkv, T);
+  if (Hq % Hkv != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: Hq=%d is not a multiple of Hkv=%d", fn, Hq, Hkv);
+  if (dtype != CSATTN_BF16)
+    return fail(dtype == CSATTN_F32 ? CSATTN_ERR_UNSUPPORTED : CSATTN_ERR_INVALID_ARG,
+                "%s: only bf16 is implemented (dtype %d)", fn, dtype);
+  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d not in {64,128}", fn, d);
+  if (causal != 0 && causal != 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
+  if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown rope_layout %d", fn, rope_layout);
+  if (!std::isfinite(rope_base) || !std::isfinite(scale))
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: rope_base and scale must be finite", fn);
+  if (T >= (1 << 24)) return fail(CSATTN_ERR_UNSUPPORTED, "%s: T=%d >= 2^24", fn, T);
+  if (rope_base > 0.f && T > kMaxRopePositions)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: RoPE supports T <= %d, got %d", fn,
+                kMaxRopePositions, T);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  const size_t need = csattn_bwd_workspace_size(B, Hq, Hkv, T, d, dtype, rope_base);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return fail(CSATTN_ERR_WORKSPACE,
+                "%s: needs a 16-byte aligned workspace of %zu bytes (got %zu)", fn, need,
+                workspace_bytes);
+  auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t rows = static_cast<size_t>(B) * Hq * T;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  BwdArgs a{};
+  a.v = v;
+  a.out = out;
+  a.dout = dout;
+  a.lse = lse;
+  a.dvec = reinterpret_cast<float*>(ws);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Tq = T;
+  a.Tk = T;
+  a.q_off = 0;
+  a.d = d;
+  a.causal = causal;
+  a.rope = rope_base > 0.f ? (rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2) : 0;
+  a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  if (a.rope) rope_table(&a.theta, d, static_cast<double>(rope_base));
+  uint32_t* status = nullptr;
+  int num_sms = 0;
+  int rc = device_info(&status, &num_sms);
+  if (rc != CSATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  a.qr = q;
+  a.kr = k;
+  if (a.rope) {
+    void* qr = ws + al(rows * 4);
+    void* kr = static_cast<uint8_t*>(qr) + al(rows * d * 2);
+    cudaError_t e = launch_rope_rotate_bf16(q, qr, B, Hq, T, d, a.rope, a.theta, st);
+    if (e == cudaSuccess) e = launch_rope_rotate_bf16(k, kr, B, Hkv, T, d, a.rope, a.theta, st);
+    if (e != cudaSuccess) return fail_cuda(e, "attn_bwd: RoPE kernel launch");
+    a.qr = qr;
+    a.kr = kr;
+  }
+  cudaError_t e = launch_bwd_bf16(a, st);
+  if (e != cudaSuccess) return fail_cuda(e, "attn_bwd: kernel launch");
+  return CSATTN_OK;
+}
+
 int csattn_rope_rotate(const void* x, void* x_rot, int B, int H, int T, int d, int dtype,
                        float rope_base, int rope_layout, void* stream) {
   if (x == nullptr || x_rot == nullptr)

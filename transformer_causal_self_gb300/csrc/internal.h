@@ -41,6 +41,29 @@ cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, in
 cudaError_t launch_fwd_sm103a(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
 cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
 
+// Backward (bf16, d in {64, 128}): dq, dk, dv of sum(out * dout).  qr, kr are the
+// rotated operands of the forward; dvec is fp32 scratch [B, Hq, Tq] for
+// rowsum(dout o out); lse is the forward's natural-log log-sum-exp.
+struct BwdArgs {
+  const void* qr;
+  const void* kr;
+  const void* v;
+  const void* out;
+  const void* dout;
+  const float* lse;
+  float* dvec;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, Hq, Hkv, Tq, Tk, q_off, d;
+  int causal;
+  int rope;  // 0 none, 1 split-half, 2 adjacent: dq, dk are rotated back by R^T
+  float scale;
+  RopeTable theta;
+};
+
+cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream);
+
 struct DecodeArgs {
   const void* q;
   const void* k_cache;
