@@ -523,7 +523,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": fl,
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
-                     "kernel": "bwd_dkdv_kernel<128> + bwd_dq_kernel<128> (mma.sync)"}}
+                     "kernel": "bwd_kv_tc_kernel (tcgen05) + bwd_dq_kernel<128> (mma.sync)"}}
     return out
 
 
@@ -532,6 +532,7 @@ def run_profile_case(args):
 
     fwd:    the llama_gqa_bf16 prefill (RoPE pass + attention kernel), full size.
     decode: the decode_bf16 workload with B=16 sequences (0.5 GB of cache).
+    bwd:    the llama_gqa_bf16 backward (after one forward for out and lse), full size.
     """
     import torch
 
@@ -547,6 +548,15 @@ def run_profile_case(args):
             csattn.rope_rotate(k, k_rot, rope_base=w.rope_base)
             csattn.attn_fwd(q, k_rot, v, out, causal=True, rope_base=w.rope_base, scale=w.scale,
                             k_prerotated=True)
+    elif args.profile == "bwd":
+        w = W.WORKLOADS[PREFILL]
+        q, k, v = (t.to(dev) for t in W.make_prefill_inputs(w))
+        do = torch.randn_like(q)
+        lse = torch.empty(w.B, w.Hq, w.T, dtype=torch.float32, device=dev)
+        out = csattn.attn_fwd(q, k, v, causal=True, rope_base=w.rope_base, scale=w.scale, lse=lse)
+        for _ in range(2):
+            csattn.attn_bwd(q, k, v, out, do, lse, causal=True, rope_base=w.rope_base,
+                            scale=w.scale)
     else:
         w = W.WORKLOADS[DECODE].with_(B=16)
         qd, kc, vc, lens = W.make_decode_inputs(w)
@@ -570,7 +580,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the timing of the chunked-prefill and decode-step rows")
-    ap.add_argument("--profile", choices=["fwd", "decode"], default=None,
+    ap.add_argument("--profile", choices=["fwd", "decode", "bwd"], default=None,
                     help="run a short single-kernel case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:

@@ -500,9 +500,13 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
   if (e != cudaSuccess) return e;
-  dim3 gkv((a.Tk + kTile - 1) / kTile, a.Hkv, a.B);
-  bwd_dkdv_kernel<D><<<gkv, kThreads, smem_kv, stream>>>(p);
-  e = cudaGetLastError();
+  if (D == 128 && a.Tq == a.Tk && a.q_off == 0) {
+    e = launch_bwd_kv_tc(a, stream);
+  } else {
+    dim3 gkv((a.Tk + kTile - 1) / kTile, a.Hkv, a.B);
+    bwd_dkdv_kernel<D><<<gkv, kThreads, smem_kv, stream>>>(p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   dim3 gq((a.Tq + kTile - 1) / kTile, a.Hq, a.B);
   bwd_dq_kernel<D><<<gq, kThreads, smem_q, stream>>>(p);

@@ -1,0 +1,393 @@
+// dK and dV of the attention backward for head size 128 on tcgen05 (the math
+// and the split into a dK/dV kernel and a dQ kernel are described in bwd.cu).
+//
+// One CTA per (128 keys, KV head, batch); it walks the query heads of the KV
+// group and, for each, the 128-row query tiles that see the keys.  Per tile:
+//
+//   S^T  = Kr Qr^T          M=128 keys, N=128 queries, K=128   (SS, TMEM cols [0,128))
+//   dP^T = V dO^T           same shapes                         (SS, cols [128,256))
+//   P^T  = exp(scale*S^T - lse)   dS^T = P^T o (dP^T - D)      (softmax warpgroups)
+//   dV  += P^T dO           M=128 keys, N=128 channels, K=128 queries (TS, cols [256,384))
+//   dK  += dS^T Qr          same                                      (TS, cols [384,512))
+//
+// P^T and dS^T (bf16) are written back into TMEM over the S^T and dP^T columns
+// they were computed from and feed the last two products as the A operand.
+// Warps 0-3 handle queries 0-63 of the tile, warps 4-7 queries 64-127 (thread =
+// key row = TMEM lane); warp 8 loads (TMA for Qr and dO, plain loads for lse and
+// D); warp 9 allocates TMEM and issues the MMAs.  The tensor core runs
+// S^T, dP^T -> (softmax) -> dV, dK in sequence per tile: TMEM holds one tile's
+// S^T and dP^T next to the two 128-column accumulators, so the next tile's
+// products wait for this tile's P^T and dS^T to be consumed.
+//
+// Every wait is bounded (2 s) and sets the status word's timeout bit; no named
+// barriers, so a warp that gives up just leaves its loop.
+#include "internal.h"
+
+namespace csattn {
+namespace {
+
+constexpr int D = 128;
+constexpr int BK = 128;  // keys per CTA
+constexpr int BQ = 128;  // queries per tile
+constexpr int kThreads = 384;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr int NSQ = 2;  // Q / dO stages
+constexpr int TILE = BQ * D * 2;        // 32 KB
+constexpr int BLOCK = BQ * 128;         // one 64-channel column block of a tile
+constexpr int VEC = 2 * BQ * 4;         // lse and D of one tile, fp32
+constexpr int SMEM_DATA = 2 * TILE + NSQ * 2 * TILE + NSQ * VEC;
+constexpr int SMEM_BYTES = SMEM_DATA + 256;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 100000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, 0, 0);  // both K-major
+constexpr uint32_t IDESC_TS = idesc_bf16_f32(128, 128, 0, 1);  // B (dO / Qr) MN-major
+
+struct KvParams {
+  const float* lse;   // [B, Hq, T], natural log
+  const float* dvec;  // [B, Hq, T]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  uint32_t* status;
+  int Hq, Hkv, T, causal, rope;
+  float scale, sl2;
+  RopeTable theta;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status) {
+  const bool ok = mbar_wait(bar, parity, abort, status, kWaitNs);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// packed bf16 column of queries 16kk..16kk+15 inside a P^T or dS^T region
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  return static_cast<uint32_t>(kk < 4 ? 8 * kk : 64 + 8 * (kk - 4));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kv_tc_kernel(const __grid_constant__ KvParams p, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_do) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + TILE;
+  uint8_t* sQ = smem + 2 * TILE;                 // [NSQ] tiles
+  uint8_t* sO = smem + (2 + NSQ) * TILE;         // [NSQ] dO tiles
+  float* sVec = reinterpret_cast<float*>(smem + (2 + 2 * NSQ) * TILE);  // [NSQ][lse 128 | D 128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_DATA);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* q_full = bars + 1;   // [NSQ]: TMA bytes + one arrival for the vectors
+  uint64_t* q_empty = bars + 3;  // [NSQ]
+  uint64_t* s_full = bars + 5;   // S^T and dP^T in TMEM
+  uint64_t* p_full = bars + 6;   // P^T written (8 warps)
+  uint64_t* ds_full = bars + 7;  // dS^T written (8 warps)
+  uint64_t* acc_full = bars + 8; // dK, dV complete
+  uint64_t* teardown = bars + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusDeviceArg);
+    return;
+  }
+  const int k0 = blockIdx.x * BK, g = blockIdx.y, b = blockIdx.z;
+  const int rep = p.Hq / p.Hkv;
+  const int n_qt = (p.T + BQ - 1) / BQ;
+  const int i_begin = p.causal ? blockIdx.x : 0;  // query tiles that see these keys
+  const int per_head = n_qt - i_begin;
+  const int n_it = rep * per_head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NSQ; ++s) {
+      mbar_init(&q_full[s], 2);
+      mbar_init(&q_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 8);
+    mbar_init(ds_full, 8);
+    mbar_init(acc_full, 1);
+    mbar_init(teardown, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ loads (whole warp)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * TILE);
+      const int zk = b * p.Hkv + g;
+      for (int kb = 0; kb < D / 64; ++kb) {
+        tma_load_3d(sK + kb * BLOCK, &tm_k, kv_full, kb * 64, k0, zk);
+        tma_load_3d(sV + kb * BLOCK, &tm_v, kv_full, kb * 64, k0, zk);
+      }
+    }
+    int issued = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NSQ, use = it / NSQ;
+      if (use > 0 && !warp_wait(&q_empty[st], (use - 1) & 1, abort_flag, p.status)) break;
+      const int h = g * rep + it / per_head;
+      const int q0 = (i_begin + it % per_head) * BQ;
+      const int zq = b * p.Hq + h;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&q_full[st], 2 * TILE);
+        for (int kb = 0; kb < D / 64; ++kb) {
+          tma_load_3d(sQ + st * TILE + kb * BLOCK, &tm_q, &q_full[st], kb * 64, q0, zq);
+          tma_load_3d(sO + st * TILE + kb * BLOCK, &tm_do, &q_full[st], kb * 64, q0, zq);
+        }
+      }
+      float* vec = sVec + st * 2 * BQ;
+      const size_t rb = static_cast<size_t>(zq) * p.T;
+      for (int e = lane; e < BQ; e += 32) {
+        const int q = q0 + e;
+        vec[e] = q < p.T ? p.lse[rb + q] * kLog2e : 0.f;
+        vec[BQ + e] = q < p.T ? p.dvec[rb + q] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[st]);
+      ++issued;
+    }
+    if (lane == 0 && *abort_flag) {
+      mbar_wait(kv_full, 0, nullptr, p.status, kDrainNs);
+      const int first = issued > NSQ ? issued - NSQ : 0;
+      for (int t = first; t < issued; ++t)
+        mbar_wait(&q_full[t % NSQ], (t / NSQ) & 1, nullptr, p.status, kDrainNs);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!ok) return false;
+        ok = mbar_wait(bar, parity, abort_flag, p.status, kWaitNs);
+        tc_fence_after();
+        return ok;
+      };
+      const uint32_t k_s = smem_u32(sK), v_s = smem_u32(sV);
+      wait(kv_full, 0);  // also when there is nothing to do: the loads must land first
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int st = it % NSQ;
+        if (!wait(&q_full[st], (it / NSQ) & 1)) break;
+        const uint32_t q_s = smem_u32(sQ + st * TILE), o_s = smem_u32(sO + st * TILE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
+          umma_ss(tmem, smem_desc_sw128(k_s + off, 16, 1024), smem_desc_sw128(q_s + off, 16, 1024),
+                  IDESC_SS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
+          umma_ss(tmem + 128u, smem_desc_sw128(v_s + off, 16, 1024),
+                  smem_desc_sw128(o_s + off, 16, 1024), IDESC_SS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full);
+        if (!wait(p_full, it & 1)) break;
+        // dV += P^T dO: A = P^T (TMEM), B = dO (rows = queries, channels contiguous)
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          umma_ts(tmem + 256u, tmem + packed_col(kk), smem_desc_sw128(o_s + 2048u * kk, BLOCK, 1024),
+                  IDESC_TS, (it > 0 || kk > 0) ? 1u : 0u);
+        if (!wait(ds_full, it & 1)) break;
+        // dK += dS^T Qr
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          umma_ts(tmem + 384u, tmem + 128u + packed_col(kk),
+                  smem_desc_sw128(q_s + 2048u * kk, BLOCK, 1024), IDESC_TS,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&q_empty[st]);
+      }
+      tc_commit(acc_full);
+      tc_commit(teardown);
+      mbar_wait(teardown, 0, nullptr, p.status, kDrainNs);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ P^T, dS^T; epilogue
+    const int x = warp >> 2;                 // query half of the tile
+    const int row = threadIdx.x & 127;       // key row = TMEM lane
+    const int key = k0 + row;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(64 * x);
+    const uint32_t tP = tS;                           // P^T packed: 32 columns
+    const uint32_t tD = tmem + lane_off + 128u + static_cast<uint32_t>(64 * x);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NSQ;
+      const int q0 = (i_begin + it % per_head) * BQ + 64 * x;  // first query of this half
+      if (!warp_wait(s_full, it & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // lse and D of this tile were stored by the load warp before its q_full arrival
+      if (!warp_wait(&q_full[st], (it / NSQ) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      const float* lse2 = sVec + st * 2 * BQ + 64 * x;
+      const float* dv = lse2 + BQ;
+      float pt[64];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld32_sync(tS + 32u * h, r);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int q = q0 + 32 * h + c;
+            const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
+            pt[32 * h + c] =
+                vis ? ex2_approx(fmaf(__uint_as_float(r[c]), p.sl2, -lse2[32 * h + c])) : 0.f;
+          }
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) pk[t] = pack_bf16x2(pt[2 * t], pt[2 * t + 1]);
+        tmem_st32(tP, pk);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+      {
+        uint32_t r[32], pk[16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld32_sync(tD + 32u * h, r);
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const int c = 2 * t;
+            const float d0 = pt[32 * h + c] * (__uint_as_float(r[c]) - dv[32 * h + c]);
+            const float d1 = pt[32 * h + c + 1] * (__uint_as_float(r[c + 1]) - dv[32 * h + c + 1]);
+            pk[t] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tD + 16u * h, pk);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    // epilogue: warps 0-3 write dV, warps 4-7 dK = R^T (scale dK); channels in pairs of
+    // 32-column chunks (c, c + 2) so that split-half RoPE pairs (i, i + 64) meet
+    if (ok && (n_it == 0 || warp_wait(acc_full, 0, abort_flag, p.status))) {
+      tc_fence_after();
+      const uint32_t tacc = tmem + lane_off + (x ? 384u : 256u);
+      __nv_bfloat16* dst =
+          (x ? p.dk : p.dv) + (static_cast<size_t>(b * p.Hkv + g) * p.T + (key < p.T ? key : 0)) * D;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float a0[32], a1[32];
+        {
+          uint32_t r[32];
+          tmem_ld32_sync(tacc + 32u * c, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a0[e] = n_it > 0 ? __uint_as_float(r[e]) : 0.f;
+          tmem_ld32_sync(tacc + 64u + 32u * c, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a1[e] = n_it > 0 ? __uint_as_float(r[e]) : 0.f;
+        }
+        if (x == 1) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            a0[e] *= p.scale;
+            a1[e] *= p.scale;
+          }
+          if (p.rope == 1) {  // pair (i, i + 64), i = 32c + e
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              float cs, sn;
+              rope_cos_sin<true>(key, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
+              const float u = a0[e], w = a1[e];
+              a0[e] = fmaf(u, cs, w * sn);
+              a1[e] = fmaf(-u, sn, w * cs);
+            }
+          } else if (p.rope == 2) {  // pairs (2i, 2i + 1) inside each chunk
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              float cs, sn;
+              rope_cos_sin<true>(key, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
+              float u = a0[2 * t], w = a0[2 * t + 1];
+              a0[2 * t] = fmaf(u, cs, w * sn);
+              a0[2 * t + 1] = fmaf(-u, sn, w * cs);
+              rope_cos_sin<true>(key, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs,
+                                 sn);
+              u = a1[2 * t];
+              w = a1[2 * t + 1];
+              a1[2 * t] = fmaf(u, cs, w * sn);
+              a1[2 * t + 1] = fmaf(-u, sn, w * cs);
+            }
+          }
+        }
+        if (key < p.T) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            reinterpret_cast<uint4*>(dst + 32 * c)[v4] =
+                make_uint4(pack_bf16x2(a0[8 * v4], a0[8 * v4 + 1]),
+                           pack_bf16x2(a0[8 * v4 + 2], a0[8 * v4 + 3]),
+                           pack_bf16x2(a0[8 * v4 + 4], a0[8 * v4 + 5]),
+                           pack_bf16x2(a0[8 * v4 + 6], a0[8 * v4 + 7]));
+            reinterpret_cast<uint4*>(dst + 64 + 32 * c)[v4] =
+                make_uint4(pack_bf16x2(a1[8 * v4], a1[8 * v4 + 1]),
+                           pack_bf16x2(a1[8 * v4 + 2], a1[8 * v4 + 3]),
+                           pack_bf16x2(a1[8 * v4 + 4], a1[8 * v4 + 5]),
+                           pack_bf16x2(a1[8 * v4 + 6], a1[8 * v4 + 7]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream) {
+  KvParams p{};
+  p.lse = a.lse;
+  p.dvec = a.dvec;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.status = a.status;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.T = a.Tq;
+  p.causal = a.causal;
+  p.rope = a.rope;
+  p.scale = a.scale;
+  p.sl2 = a.scale * kLog2e;
+  p.theta = a.theta;
+  alignas(64) CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_bf16_3d(&tq, a.qr, D, a.Tq, a.B * a.Hq, BQ) ||
+      !make_tmap_bf16_3d(&tk, a.kr, D, a.Tk, a.B * a.Hkv, BK) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BK) ||
+      !make_tmap_bf16_3d(&tdo, a.dout, D, a.Tq, a.B * a.Hq, BQ))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Tk + BK - 1) / BK, a.Hkv, a.B);
+  bwd_kv_tc_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
+  return cudaGetLastError();
+}
+
+}  // namespace csattn

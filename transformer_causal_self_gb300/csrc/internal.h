@@ -60,9 +60,12 @@ struct BwdArgs {
   int rope;  // 0 none, 1 split-half, 2 adjacent: dq, dk are rotated back by R^T
   float scale;
   RopeTable theta;
+  uint32_t* status;  // device status word (timeouts of the tcgen05 kernel)
 };
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream);
+// dK, dV for d = 128 on tcgen05 (square T, q_off = 0); called by launch_bwd_bf16
+cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream);
 
 struct DecodeArgs {
   const void* q;
