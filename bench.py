@@ -523,7 +523,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": fl,
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
-                     "kernel": "bwd_kv_tc_kernel (tcgen05) + bwd_dq_kernel<128> (mma.sync)"}}
+                     "kernel": "bwd_kv_tc_kernel + bwd_q_tc_kernel (tcgen05)"}}
     return out
 
 

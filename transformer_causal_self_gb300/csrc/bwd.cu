@@ -508,6 +508,7 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
+  if (D == 128 && a.Tq == a.Tk && a.q_off == 0) return launch_bwd_q_tc(a, stream);
   dim3 gq((a.Tq + kTile - 1) / kTile, a.Hq, a.B);
   bwd_dq_kernel<D><<<gq, kThreads, smem_q, stream>>>(p);
   return cudaGetLastError();

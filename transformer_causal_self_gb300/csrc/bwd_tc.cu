@@ -359,6 +359,259 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// dQ for d = 128: one CTA per (128 queries, query head, batch), walking the key
+// tiles the queries see.  Per key tile j:
+//   S  = Qr Kr_j^T, dP = dO V_j^T   (SS, TMEM columns [0,128) and [128,256))
+//   dS = exp(scale*S - lse) o (dP - D)  (thread = query row; warps 0-3 keys 0-63,
+//                                        warps 4-7 keys 64-127), bf16 into S's columns
+//   dQ += dS Kr_j                   (TS, B = Kr_j with channels contiguous; [256,384))
+// K_j and V_j arrive by TMA through a two-stage ring.
+constexpr int NSKV = 2;
+constexpr int Q_SMEM_DATA = 2 * TILE + NSKV * 2 * TILE;
+constexpr int Q_SMEM_BYTES = Q_SMEM_DATA + 256;
+
+struct QParams {
+  const float* lse;
+  const float* dvec;
+  __nv_bfloat16* dq;
+  uint32_t* status;
+  int Hq, Hkv, T, causal, rope;
+  float scale, sl2;
+  RopeTable theta;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_q_tc_kernel(const __grid_constant__ QParams p, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sQ = smem;
+  uint8_t* sO = smem + TILE;
+  uint8_t* sKV = smem + 2 * TILE;  // [NSKV] x (K tile, V tile)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Q_SMEM_DATA);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;   // [NSKV]
+  uint64_t* kv_empty = bars + 3;  // [NSKV]
+  uint64_t* s_full = bars + 5;
+  uint64_t* ds_full = bars + 6;   // 8 warps
+  uint64_t* acc_full = bars + 7;
+  uint64_t* teardown = bars + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusDeviceArg);
+    return;
+  }
+  const int q0 = blockIdx.x * BQ, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (p.Hq / p.Hkv);
+  const int n_kt = (p.T + BK - 1) / BK;
+  const int n_it = p.causal ? min(n_kt, blockIdx.x + 1) : n_kt;  // key tiles seen
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NSKV; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(ds_full, 8);
+    mbar_init(acc_full, 1);
+    mbar_init(teardown, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpProducer) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const int zq = b * p.Hq + h, zk = b * p.Hkv + g;
+      mbar_arrive_expect_tx(q_full, 2 * TILE);
+      for (int kb = 0; kb < D / 64; ++kb) {
+        tma_load_3d(sQ + kb * BLOCK, &tm_q, q_full, kb * 64, q0, zq);
+        tma_load_3d(sO + kb * BLOCK, &tm_do, q_full, kb * 64, q0, zq);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_it; ++j) {
+        const int st = j % NSKV, use = j / NSKV;
+        if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, abort_flag, p.status, kWaitNs))
+          break;
+        uint8_t* dst = sKV + st * 2 * TILE;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * TILE);
+        for (int kb = 0; kb < D / 64; ++kb) {
+          tma_load_3d(dst + kb * BLOCK, &tm_k, &kv_full[st], kb * 64, j * BK, zk);
+          tma_load_3d(dst + TILE + kb * BLOCK, &tm_v, &kv_full[st], kb * 64, j * BK, zk);
+        }
+        ++issued;
+      }
+      if (*abort_flag) {
+        mbar_wait(q_full, 0, nullptr, p.status, kDrainNs);
+        const int first = issued > NSKV ? issued - NSKV : 0;
+        for (int t = first; t < issued; ++t)
+          mbar_wait(&kv_full[t % NSKV], (t / NSKV) & 1, nullptr, p.status, kDrainNs);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!ok) return false;
+        ok = mbar_wait(bar, parity, abort_flag, p.status, kWaitNs);
+        tc_fence_after();
+        return ok;
+      };
+      const uint32_t q_s = smem_u32(sQ), o_s = smem_u32(sO);
+      wait(q_full, 0);
+      for (int j = 0; j < n_it && ok; ++j) {
+        const int st = j % NSKV;
+        if (!wait(&kv_full[st], (j / NSKV) & 1)) break;
+        const uint32_t k_s = smem_u32(sKV + st * 2 * TILE), v_s = k_s + TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
+          umma_ss(tmem, smem_desc_sw128(q_s + off, 16, 1024), smem_desc_sw128(k_s + off, 16, 1024),
+                  IDESC_SS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
+          umma_ss(tmem + 128u, smem_desc_sw128(o_s + off, 16, 1024),
+                  smem_desc_sw128(v_s + off, 16, 1024), IDESC_SS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full);
+        if (!wait(ds_full, j & 1)) break;
+        // dQ += dS Kr_j: B = Kr_j as (channels x keys), channels contiguous
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_ts(tmem + 256u, tmem + packed_col(kk), smem_desc_sw128(k_s + 2048u * kk, BLOCK, 1024),
+                  IDESC_TS, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&kv_empty[st]);
+      }
+      tc_commit(acc_full);
+      tc_commit(teardown);
+      mbar_wait(teardown, 0, nullptr, p.status, kDrainNs);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    const int x = warp >> 2;              // key half of the tile
+    const int row = threadIdx.x & 127;    // query row = TMEM lane
+    const int q = q0 + row;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(64 * x);
+    const uint32_t tD = tmem + lane_off + 128u + static_cast<uint32_t>(64 * x);
+    const size_t rb = static_cast<size_t>(b * p.Hq + h) * p.T;
+    const float lse2 = q < p.T ? p.lse[rb + q] * kLog2e : 0.f;
+    const float dq_d = q < p.T ? p.dvec[rb + q] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_it; ++j) {
+      if (!warp_wait(s_full, j & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int kb0 = j * BK + 64 * x;  // first key of this half
+      uint32_t pk[32];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t rs[32], rd[32];
+        tmem_ld32_sync(tS + 32u * hh, rs);
+        tmem_ld32_sync(tD + 32u * hh, rd);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          float v[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = 2 * t + u;
+            const int key = kb0 + 32 * hh + c;
+            const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
+            const float pr =
+                vis ? ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2)) : 0.f;
+            v[u] = pr * (__uint_as_float(rd[c]) - dq_d);
+          }
+          pk[16 * hh + t] = pack_bf16x2(v[0], v[1]);
+        }
+      }
+      tmem_st32(tS, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    // epilogue: dQ = R^T (scale dQ); warpgroup x takes columns [32x, 32x+32) and
+    // [64+32x, 64+32x+32) so that split-half pairs (i, i + 64) meet in one thread
+    if (ok && warp_wait(acc_full, 0, abort_flag, p.status)) {
+      tc_fence_after();
+      const int c = x;
+      float a0[32], a1[32];
+      {
+        uint32_t r[32];
+        tmem_ld32_sync(tmem + lane_off + 256u + 32u * c, r);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) a0[e] = __uint_as_float(r[e]) * p.scale;
+        tmem_ld32_sync(tmem + lane_off + 256u + 64u + 32u * c, r);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) a1[e] = __uint_as_float(r[e]) * p.scale;
+      }
+      if (p.rope == 1) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float cs, sn;
+          rope_cos_sin<true>(q, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
+          const float u = a0[e], w = a1[e];
+          a0[e] = fmaf(u, cs, w * sn);
+          a1[e] = fmaf(-u, sn, w * cs);
+        }
+      } else if (p.rope == 2) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          float cs, sn;
+          rope_cos_sin<true>(q, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
+          float u = a0[2 * t], w = a0[2 * t + 1];
+          a0[2 * t] = fmaf(u, cs, w * sn);
+          a0[2 * t + 1] = fmaf(-u, sn, w * cs);
+          rope_cos_sin<true>(q, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs, sn);
+          u = a1[2 * t];
+          w = a1[2 * t + 1];
+          a1[2 * t] = fmaf(u, cs, w * sn);
+          a1[2 * t + 1] = fmaf(-u, sn, w * cs);
+        }
+      }
+      if (q < p.T) {
+        __nv_bfloat16* dst = p.dq + (rb + q) * D;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          reinterpret_cast<uint4*>(dst + 32 * c)[v4] =
+              make_uint4(pack_bf16x2(a0[8 * v4], a0[8 * v4 + 1]),
+                         pack_bf16x2(a0[8 * v4 + 2], a0[8 * v4 + 3]),
+                         pack_bf16x2(a0[8 * v4 + 4], a0[8 * v4 + 5]),
+                         pack_bf16x2(a0[8 * v4 + 6], a0[8 * v4 + 7]));
+          reinterpret_cast<uint4*>(dst + 64 + 32 * c)[v4] =
+              make_uint4(pack_bf16x2(a1[8 * v4], a1[8 * v4 + 1]),
+                         pack_bf16x2(a1[8 * v4 + 2], a1[8 * v4 + 3]),
+                         pack_bf16x2(a1[8 * v4 + 4], a1[8 * v4 + 5]),
+                         pack_bf16x2(a1[8 * v4 + 6], a1[8 * v4 + 7]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream) {
@@ -387,6 +640,38 @@ cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid((a.Tk + BK - 1) / BK, a.Hkv, a.B);
   bwd_kv_tc_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
+  return cudaGetLastError();
+}
+
+}  // namespace csattn
+
+namespace csattn {
+
+cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream) {
+  QParams p{};
+  p.lse = a.lse;
+  p.dvec = a.dvec;
+  p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.status = a.status;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.T = a.Tq;
+  p.causal = a.causal;
+  p.rope = a.rope;
+  p.scale = a.scale;
+  p.sl2 = a.scale * kLog2e;
+  p.theta = a.theta;
+  alignas(64) CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_bf16_3d(&tq, a.qr, D, a.Tq, a.B * a.Hq, BQ) ||
+      !make_tmap_bf16_3d(&tk, a.kr, D, a.Tk, a.B * a.Hkv, BK) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BK) ||
+      !make_tmap_bf16_3d(&tdo, a.dout, D, a.Tq, a.B * a.Hq, BQ))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(bwd_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Q_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Tq + BQ - 1) / BQ, a.Hq, a.B);
+  bwd_q_tc_kernel<<<grid, kThreads, Q_SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
   return cudaGetLastError();
 }
 

@@ -66,6 +66,8 @@ struct BwdArgs {
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream);
 // dK, dV for d = 128 on tcgen05 (square T, q_off = 0); called by launch_bwd_bf16
 cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream);
+// dQ for d = 128 on tcgen05 (square T, q_off = 0); called by launch_bwd_bf16
+cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream);
 
 struct DecodeArgs {
   const void* q;
