@@ -81,12 +81,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;   // [NSQ]: TMA bytes + one arrival for the vectors
   uint64_t* q_empty = bars + 3;  // [NSQ]
-  uint64_t* s_full = bars + 5;   // S^T and dP^T in TMEM
+  uint64_t* s_full = bars + 5;   // S^T in TMEM
   uint64_t* p_full = bars + 6;   // P^T written (8 warps)
   uint64_t* ds_full = bars + 7;  // dS^T written (8 warps)
   uint64_t* acc_full = bars + 8; // dK, dV complete
   uint64_t* teardown = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* dp_full = bars + 10; // dP^T in TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -94,10 +95,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicOr(p.status, kStatusDeviceArg);
     return;
   }
-  const int k0 = blockIdx.x * BK, g = blockIdx.y, b = blockIdx.z;
+  // grid (Hkv, B, key tiles): blocks launch in index order, so z runs slowest and the
+  // key tiles with the most query tiles to visit (the first ones, causally) go first
+  const int kt = blockIdx.z;
+  const int k0 = kt * BK, g = blockIdx.x, b = blockIdx.y;
   const int rep = p.Hq / p.Hkv;
   const int n_qt = (p.T + BQ - 1) / BQ;
-  const int i_begin = p.causal ? blockIdx.x : 0;  // query tiles that see these keys
+  const int i_begin = p.causal ? kt : 0;  // query tiles that see these keys
   const int per_head = n_qt - i_begin;
   const int n_it = rep * per_head;
 
@@ -108,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q_empty[s], 1);
     }
     mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
     mbar_init(p_full, 8);
     mbar_init(ds_full, 8);
     mbar_init(acc_full, 1);
@@ -176,29 +181,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       const uint32_t k_s = smem_u32(sK), v_s = smem_u32(sV);
       wait(kv_full, 0);  // also when there is nothing to do: the loads must land first
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int st = it % NSQ;
-        if (!wait(&q_full[st], (it / NSQ) & 1)) break;
-        const uint32_t q_s = smem_u32(sQ + st * TILE), o_s = smem_u32(sO + st * TILE);
+      auto q_tile = [&](int it) { return smem_u32(sQ + (it % NSQ) * TILE); };
+      auto o_tile = [&](int it) { return smem_u32(sO + (it % NSQ) * TILE); };
+      auto issue_st = [&](int it) {  // S^T = Kr Qr^T
+        const uint32_t q_s = q_tile(it);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
           umma_ss(tmem, smem_desc_sw128(k_s + off, 16, 1024), smem_desc_sw128(q_s + off, 16, 1024),
                   IDESC_SS, kk > 0 ? 1u : 0u);
         }
+        tc_commit(s_full);
+      };
+      auto issue_dpt = [&](int it) {  // dP^T = V dO^T
+        const uint32_t o_s = o_tile(it);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
           umma_ss(tmem + 128u, smem_desc_sw128(v_s + off, 16, 1024),
                   smem_desc_sw128(o_s + off, 16, 1024), IDESC_SS, kk > 0 ? 1u : 0u);
         }
-        tc_commit(s_full);
+        tc_commit(dp_full);
+      };
+      // Order per tile: dV(it) frees the P^T columns, so S^T(it+1) follows it at once and
+      // runs while the softmax warps compute dS^T(it); dK(it) frees the dS^T columns for
+      // dP^T(it+1).
+      if (n_it > 0 && wait(&q_full[0], 0)) {
+        issue_st(0);
+        issue_dpt(0);
+      }
+      for (int it = 0; it < n_it && ok; ++it) {
+        const uint32_t q_s = q_tile(it), o_s = o_tile(it);
         if (!wait(p_full, it & 1)) break;
         // dV += P^T dO: A = P^T (TMEM), B = dO (rows = queries, channels contiguous)
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
           umma_ts(tmem + 256u, tmem + packed_col(kk), smem_desc_sw128(o_s + 2048u * kk, BLOCK, 1024),
                   IDESC_TS, (it > 0 || kk > 0) ? 1u : 0u);
+        const bool next = it + 1 < n_it;
+        if (next) {
+          if (!wait(&q_full[(it + 1) % NSQ], ((it + 1) / NSQ) & 1)) break;
+          issue_st(it + 1);
+        }
         if (!wait(ds_full, it & 1)) break;
         // dK += dS^T Qr
 #pragma unroll
@@ -206,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(tmem + 384u, tmem + 128u + packed_col(kk),
                   smem_desc_sw128(q_s + 2048u * kk, BLOCK, 1024), IDESC_TS,
                   (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&q_empty[st]);
+        tc_commit(&q_empty[it % NSQ]);
+        if (next) issue_dpt(it + 1);
       }
       tc_commit(acc_full);
       tc_commit(teardown);
@@ -261,6 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
+      if (!warp_wait(dp_full, it & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       {
         uint32_t r[32], pk[16];
 #pragma unroll
@@ -364,9 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // tiles the queries see.  Per key tile j:
 //   S  = Qr Kr_j^T, dP = dO V_j^T   (SS, TMEM columns [0,128) and [128,256))
 //   dS = exp(scale*S - lse) o (dP - D)  (thread = query row; warps 0-3 keys 0-63,
-//                                        warps 4-7 keys 64-127), bf16 into S's columns
+//                                        warps 4-7 keys 64-127), bf16 into dP's columns
 //   dQ += dS Kr_j                   (TS, B = Kr_j with channels contiguous; [256,384))
-// K_j and V_j arrive by TMA through a two-stage ring.
+// K_j and V_j arrive by TMA through a two-stage ring.  S(j+1) is issued as soon as the
+// softmax warps have read S(j), so it overlaps their dS work; dP(j+1) follows dQ(j).
 constexpr int NSKV = 2;
 constexpr int Q_SMEM_DATA = 2 * TILE + NSKV * 2 * TILE;
 constexpr int Q_SMEM_BYTES = Q_SMEM_DATA + 256;
@@ -398,7 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ds_full = bars + 6;   // 8 warps
   uint64_t* acc_full = bars + 7;
   uint64_t* teardown = bars + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* dp_full = bars + 9;
+  uint64_t* s_free = bars + 10;   // 8 warps: S(j) read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -406,10 +439,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicOr(p.status, kStatusDeviceArg);
     return;
   }
-  const int q0 = blockIdx.x * BQ, h = blockIdx.y, b = blockIdx.z;
+  // grid (Hq, B, query tiles), z slowest: causally, the last query tiles (most key
+  // tiles to visit) are launched first
+  const int n_qtiles = (p.T + BQ - 1) / BQ;
+  const int qt = p.causal ? n_qtiles - 1 - static_cast<int>(blockIdx.z) : blockIdx.z;
+  const int q0 = qt * BQ, h = blockIdx.x, b = blockIdx.y;
   const int g = h / (p.Hq / p.Hkv);
   const int n_kt = (p.T + BK - 1) / BK;
-  const int n_it = p.causal ? min(n_kt, blockIdx.x + 1) : n_kt;  // key tiles seen
+  const int n_it = p.causal ? min(n_kt, qt + 1) : n_kt;  // key tiles seen
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -418,6 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(s_free, 8);
     mbar_init(ds_full, 8);
     mbar_init(acc_full, 1);
     mbar_init(teardown, 1);
@@ -470,31 +509,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         return ok;
       };
       const uint32_t q_s = smem_u32(sQ), o_s = smem_u32(sO);
-      wait(q_full, 0);
-      for (int j = 0; j < n_it && ok; ++j) {
-        const int st = j % NSKV;
-        if (!wait(&kv_full[st], (j / NSKV) & 1)) break;
-        const uint32_t k_s = smem_u32(sKV + st * 2 * TILE), v_s = k_s + TILE;
+      auto k_tile = [&](int j) { return smem_u32(sKV + (j % NSKV) * 2 * TILE); };
+      auto issue_s = [&](int j) {  // S = Qr Kr_j^T
+        const uint32_t k_s = k_tile(j);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
           umma_ss(tmem, smem_desc_sw128(q_s + off, 16, 1024), smem_desc_sw128(k_s + off, 16, 1024),
                   IDESC_SS, kk > 0 ? 1u : 0u);
         }
+        tc_commit(s_full);
+      };
+      auto issue_dp = [&](int j) {  // dP = dO V_j^T
+        const uint32_t v_s = k_tile(j) + TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
           umma_ss(tmem + 128u, smem_desc_sw128(o_s + off, 16, 1024),
                   smem_desc_sw128(v_s + off, 16, 1024), IDESC_SS, kk > 0 ? 1u : 0u);
         }
-        tc_commit(s_full);
+        tc_commit(dp_full);
+      };
+      if (wait(q_full, 0) && wait(&kv_full[0], 0)) {
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int j = 0; j < n_it && ok; ++j) {
+        const bool next = j + 1 < n_it;
+        if (!wait(s_free, j & 1)) break;
+        if (next) {
+          if (!wait(&kv_full[(j + 1) % NSKV], ((j + 1) / NSKV) & 1)) break;
+          issue_s(j + 1);
+        }
         if (!wait(ds_full, j & 1)) break;
-        // dQ += dS Kr_j: B = Kr_j as (channels x keys), channels contiguous
+        // dQ += dS Kr_j: A = dS (TMEM, over dP), B = Kr_j as (channels x keys)
+        const uint32_t k_s = k_tile(j);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          umma_ts(tmem + 256u, tmem + packed_col(kk), smem_desc_sw128(k_s + 2048u * kk, BLOCK, 1024),
-                  IDESC_TS, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&kv_empty[st]);
+          umma_ts(tmem + 256u, tmem + 128u + packed_col(kk),
+                  smem_desc_sw128(k_s + 2048u * kk, BLOCK, 1024), IDESC_TS,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&kv_empty[j % NSKV]);
+        if (next) issue_dp(j + 1);
       }
       tc_commit(acc_full);
       tc_commit(teardown);
@@ -519,11 +575,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int kb0 = j * BK + 64 * x;  // first key of this half
+      uint32_t rs[64];
+      tmem_ld32_sync(tS, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
+      tmem_ld32_sync(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
+      // S(j) is in registers: the MMA warp may overwrite it with S(j+1)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+      if (!warp_wait(dp_full, j & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       uint32_t pk[32];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        uint32_t rs[32], rd[32];
-        tmem_ld32_sync(tS + 32u * hh, rs);
+        uint32_t rd[32];
         tmem_ld32_sync(tD + 32u * hh, rd);
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
@@ -534,13 +601,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key = kb0 + 32 * hh + c;
             const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
             const float pr =
-                vis ? ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2)) : 0.f;
+                vis ? ex2_approx(fmaf(__uint_as_float(rs[32 * hh + c]), p.sl2, -lse2)) : 0.f;
             v[u] = pr * (__uint_as_float(rd[c]) - dq_d);
           }
           pk[16 * hh + t] = pack_bf16x2(v[0], v[1]);
         }
       }
-      tmem_st32(tS, pk);
+      tmem_st32(tD, pk);  // dS over dP (this half's 64 keys, packed into 32 columns)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -638,7 +705,7 @@ cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.Tk + BK - 1) / BK, a.Hkv, a.B);
+  dim3 grid(a.Hkv, a.B, (a.Tk + BK - 1) / BK);
   bwd_kv_tc_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
   return cudaGetLastError();
 }
@@ -670,7 +737,7 @@ cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(bwd_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Q_SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.Tq + BQ - 1) / BQ, a.Hq, a.B);
+  dim3 grid(a.Hq, a.B, (a.Tq + BQ - 1) / BQ);
   bwd_q_tc_kernel<<<grid, kThreads, Q_SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
   return cudaGetLastError();
 }
