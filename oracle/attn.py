@@ -30,7 +30,7 @@ Sources (page title, then section):
   * "Transformer Math and Implementation Deep Dive", "Attention Equation"
     (cross-attention): with no causal mask, Tq and Tk need not be equal.
 
-Readings where the pages leave a step open (each one also listed in the design doc):
+Readings where the pages leave a step open:
   * RoPE frequencies theta_i = base^(-2i/d), i = 0..d/2-1, positions from 0.
   * The rotated q and k are rounded to the input dtype (round-to-nearest-even)
     before the dot product, as the pages' ``apply_rope`` returns a tensor of the

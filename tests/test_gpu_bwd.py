@@ -50,6 +50,8 @@ CASES = [
     (1, 2, 1, 1, 128, True, 10000.0, "split_half"),
     (1, 4, 4, 257, 64, True, 500000.0, "split_half"),
     (1, 6, 2, 96, 128, False, 0.0, "split_half"),
+    (1, 4, 2, 150, 128, True, 10000.0, "adjacent"),
+    (2, 2, 2, 385, 64, True, 10000.0, "split_half"),
 ]
 
 

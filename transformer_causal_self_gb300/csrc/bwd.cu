@@ -13,7 +13,8 @@
 // Transformer architecture" (cooking-agi), "Now: RoPE": a rotation, so its
 // Jacobian transpose is the inverse rotation) and lse the forward's log-sum-exp.
 //
-// Two kernels, no atomics:
+// d = 128 runs the tcgen05 kernels of bwd_tc.cu; this file holds the row-dot
+// kernel for D and the mma.sync kernels used for d = 64.  Two kernels, no atomics:
 //   bwd_dkdv_kernel  one CTA per (64 keys, KV head, batch): loops over the
 //                    group's query heads and the query tiles that see the keys;
 //                    dK and dV stay in registers (warp w owns keys 16w..16w+15).
@@ -500,15 +501,10 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
   if (e != cudaSuccess) return e;
-  if (D == 128 && a.Tq == a.Tk && a.q_off == 0) {
-    e = launch_bwd_kv_tc(a, stream);
-  } else {
-    dim3 gkv((a.Tk + kTile - 1) / kTile, a.Hkv, a.B);
-    bwd_dkdv_kernel<D><<<gkv, kThreads, smem_kv, stream>>>(p);
-    e = cudaGetLastError();
-  }
+  dim3 gkv((a.Tk + kTile - 1) / kTile, a.Hkv, a.B);
+  bwd_dkdv_kernel<D><<<gkv, kThreads, smem_kv, stream>>>(p);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (D == 128 && a.Tq == a.Tk && a.q_off == 0) return launch_bwd_q_tc(a, stream);
   dim3 gq((a.Tq + kTile - 1) / kTile, a.Hq, a.B);
   bwd_dq_kernel<D><<<gq, kThreads, smem_q, stream>>>(p);
   return cudaGetLastError();
@@ -517,11 +513,18 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream) {
-  switch (a.d) {
-    case 64: return launch_d<64>(a, stream);
-    case 128: return launch_d<128>(a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.d == 64) return launch_d<64>(a, stream);
+  if (a.d != 128 || a.Tq != a.Tk || a.q_off != 0) return cudaErrorInvalidValue;
+  // d = 128: D = rowsum(dout o out), then the two tcgen05 kernels (bwd_tc.cu)
+  const long long rows = static_cast<long long>(a.B) * a.Hq * a.Tq;
+  bwd_rowdot_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.dout), static_cast<const __nv_bfloat16*>(a.out), a.dvec,
+      rows, 128);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_bwd_kv_tc(a, stream);
+  if (e != cudaSuccess) return e;
+  return launch_bwd_q_tc(a, stream);
 }
 
 }  // namespace csattn
