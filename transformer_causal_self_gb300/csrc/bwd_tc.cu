@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sVec = reinterpret_cast<float*>(smem + (2 + 2 * NSQ) * TILE);  // [NSQ][lse 128 | D 128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_DATA);
   uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;   // [NSQ]: TMA bytes + one arrival for the vectors
+  uint64_t* q_full = bars + 1;   // [NSQ]: Qr and dO tiles (TMA bytes)
   uint64_t* q_empty = bars + 3;  // [NSQ]
   uint64_t* s_full = bars + 5;   // S^T in TMEM
   uint64_t* p_full = bars + 6;   // P^T written (8 warps)
@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = bars + 8; // dK, dV complete
   uint64_t* teardown = bars + 9;
   uint64_t* dp_full = bars + 10; // dP^T in TMEM
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* vec_full = bars + 11; // [NSQ]: lse and D of the tile stored by the load warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,8 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int s = 0; s < NSQ; ++s) {
-      mbar_init(&q_full[s], 2);
+      mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
+      mbar_init(&vec_full[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         vec[BQ + e] = q < p.T ? p.dvec[rb + q] : 0.f;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&q_full[st]);
+      if (lane == 0) mbar_arrive(&vec_full[st]);
       ++issued;
     }
     if (lane == 0 && *abort_flag) {
@@ -256,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // lse and D of this tile were stored by the load warp before its q_full arrival
-      if (!warp_wait(&q_full[st], (it / NSQ) & 1, abort_flag, p.status)) {
+      // lse and D of this tile were stored by the load warp before its vec_full arrival
+      if (!warp_wait(&vec_full[st], (it / NSQ) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
