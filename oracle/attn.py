@@ -49,7 +49,7 @@ __all__ = [
     "softmax_rows", "rope_inv_freq", "rope_cos_sin", "rope_rotate", "round_to",
     "round_to_bf16", "expand_kv_heads", "causal_additive_mask", "attention_scores",
     "attention", "attention_rows", "attention_lse", "attention_backward", "decode",
-    "decode_step", "merge_partials", "split_partials", "rope_rotate_transpose",
+    "decode_paged", "decode_step", "merge_partials", "split_partials", "rope_rotate_transpose",
 ]
 
 _BF16_MAX = float.fromhex("0x1.fep127")
@@ -266,6 +266,28 @@ def decode(q, k_cache, v_cache, seq_lens, scale=None):
         s = np.einsum("hd,hld->hl", qb, kb) * sc
         out[b, :, 0] = np.einsum("hl,hld->hd", softmax_rows(s), vb)
     return out
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, page_size: int, scale=None):
+    """Decode over a paged cache: k_pages, v_pages [num_pages, Hkv, page_size, d];
+    row t of sequence b lives in page block_table[b][t // page_size] at offset
+    t % page_size.  The pages of each sequence are gathered into a contiguous
+    cache and ``decode`` applies."""
+    kp = np.asarray(_as_np(k_pages), dtype=np.float64)
+    vp = np.asarray(_as_np(v_pages), dtype=np.float64)
+    bt = np.asarray(_as_np(block_table)).astype(np.int64)
+    lens = [int(x) for x in np.asarray(_as_np(seq_lens)).reshape(-1)]
+    B = len(lens)
+    Hkv, d = kp.shape[1], kp.shape[3]
+    Lmax = max(1, max(lens))
+    kc = np.zeros((B, Hkv, Lmax, d))
+    vc = np.zeros((B, Hkv, Lmax, d))
+    for b, L in enumerate(lens):
+        for t in range(L):
+            page, off = bt[b, t // page_size], t % page_size
+            kc[b, :, t] = kp[page, :, off]
+            vc[b, :, t] = vp[page, :, off]
+    return decode(q, kc, vc, lens, scale=scale)
 
 
 def decode_step(q_new, k_new, v_new, k_cache, v_cache, cache_lens, *, rope_base=0.0,

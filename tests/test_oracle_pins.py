@@ -436,6 +436,28 @@ def pin_rope_transpose_inverts(o):
         assert abs(lhs - rhs) < 1e-10
 
 
+def pin_decode_paged_equals_contiguous(o):
+    """A contiguous cache scattered into shuffled pages decodes to the same result."""
+    B, Hkv, rep, d, page = 3, 2, 2, 8, 4
+    lens = [1, 9, 12]
+    n_lp = 3  # logical pages per sequence
+    kc = _rand((B, Hkv, n_lp * page, d), 280)
+    vc = _rand((B, Hkv, n_lp * page, d), 281)
+    q = _rand((B, Hkv * rep, 1, d), 282)
+    perm = np.random.default_rng(283).permutation(B * n_lp + 2)  # two spare pages
+    kp = np.full((B * n_lp + 2, Hkv, page, d), np.nan)
+    vp = np.full((B * n_lp + 2, Hkv, page, d), np.nan)
+    table = np.zeros((B, n_lp), dtype=np.int32)
+    for b in range(B):
+        for lp in range(n_lp):
+            pp = perm[b * n_lp + lp]
+            table[b, lp] = pp
+            kp[pp] = kc[b, :, lp * page:(lp + 1) * page]
+            vp[pp] = vc[b, :, lp * page:(lp + 1) * page]
+    got = o.decode_paged(q, kp, vp, table, lens, page)
+    assert np.max(np.abs(got - o.decode(q, kc, vc, lens))) < 1e-12
+
+
 ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exactly_zero,
             pin_mask_variants_differ, pin_gqa_equals_mha_repeated, pin_basis_invariance,
             pin_qq_symmetric, pin_rope_relative, pin_rope_orthogonal, pin_rope_layouts_permute,
@@ -443,7 +465,8 @@ ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exa
             pin_decode_equals_prefill_last_row, pin_merge_partials, pin_bf16_rounding,
             pin_chunk_equals_full_rows, pin_chunk_naive, pin_decode_is_chunk_of_one,
             pin_decode_step_appends_then_attends, pin_backward_finite_differences,
-            pin_backward_autograd, pin_rope_transpose_inverts]
+            pin_backward_autograd, pin_rope_transpose_inverts,
+            pin_decode_paged_equals_contiguous]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -718,3 +741,23 @@ def test_planted_backward_misses_gqa_sum():
 def test_planted_backward_rotates_forward():
     assert _fails(_Mutant(attention_backward=_backward_variant(forward_rotation=True)),
                   [pin_backward_finite_differences, pin_backward_autograd])
+
+
+def test_planted_paged_offset_swapped():
+    def bad(q, k_pages, v_pages, block_table, seq_lens, page_size, scale=None):
+        kp, vp = np.asarray(k_pages, np.float64), np.asarray(v_pages, np.float64)
+        bt = np.asarray(block_table).astype(np.int64)
+        lens = [int(x) for x in seq_lens]
+        B, Hkv, d = len(lens), kp.shape[1], kp.shape[3]
+        kc = np.zeros((B, Hkv, max(lens), d))
+        vc = np.zeros((B, Hkv, max(lens), d))
+        n_lp = bt.shape[1]
+        for b, L in enumerate(lens):
+            for t in range(L):
+                page, off = bt[b, t % n_lp], t // n_lp  # page and offset taken the wrong way
+                if off >= page_size:
+                    off = page_size - 1
+                kc[b, :, t] = kp[page, :, off]
+                vc[b, :, t] = vp[page, :, off]
+        return OA.decode(q, kc, vc, lens, scale=scale)
+    assert _fails(_Mutant(decode_paged=bad), [pin_decode_paged_equals_contiguous])
