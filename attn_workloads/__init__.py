@@ -193,6 +193,41 @@ def make_decode_inputs(w: DecodeWorkload, seed: Optional[int] = None,
     return q.contiguous(), k_cache, v_cache, seq_lens.to(torch.int32)
 
 
+def page_cache(k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens, page_size: int,
+               seed: int = 0, spare: int = 0):
+    """Scatter contiguous caches [B, Hkv, Lmax, d] into a shuffled pool of pages.
+
+    Returns (k_pages, v_pages [num_pages, Hkv, page_size, d], block_table int32
+    [B, ceil(Lmax / page_size)]) on the caches' device: the pages that hold rows
+    < seq_lens[b] go to seeded random slots of the pool, `spare` unused pages are
+    added, and table entries past a sequence's last page are -1.  Pure data
+    placement: row t of sequence b ends up in page table[b, t // page_size] at
+    offset t % page_size.
+    """
+    B, Hkv, Lmax, d = k_cache.shape
+    dev = k_cache.device
+    max_pages = -(-Lmax // page_size)
+    pad = max_pages * page_size - Lmax
+    lens = torch.as_tensor(seq_lens, dtype=torch.int64).cpu()
+    used = torch.arange(max_pages).unsqueeze(0) < (-(-lens // page_size)).unsqueeze(1)
+    n_used = int(used.sum())
+    num_pages = n_used + spare
+    perm = torch.randperm(num_pages, generator=_gen(seed))[:n_used]
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    table[used] = perm.to(torch.int32)
+    sel = used.reshape(-1).nonzero().squeeze(1).to(dev)
+    out = []
+    for c in (k_cache, v_cache):
+        if pad:
+            c = torch.nn.functional.pad(c, (0, 0, 0, pad))
+        blocks = c.reshape(B, Hkv, max_pages, page_size, d).permute(0, 2, 1, 3, 4)
+        blocks = blocks.reshape(B * max_pages, Hkv, page_size, d)
+        pool = torch.zeros(num_pages, Hkv, page_size, d, dtype=c.dtype, device=dev)
+        pool[perm.to(dev)] = blocks.index_select(0, sel)
+        out.append(pool)
+    return out[0], out[1], table.to(dev)
+
+
 def sample_query_rows(T: int, n: int, seed: int) -> list:
     """Seeded subset of query rows for sampled parity; always holds the tile edges."""
     fixed = {0, 1, 127, 128, T - 1, T // 2, min(T - 1, 255), min(T - 1, 256)}

@@ -428,6 +428,8 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
     decode_step: the decode_bf16 batch with the new token appended at row L_b - 1 and
     rotated inside the call (csattn_attn_decode_step), attending over the same L_b rows
     as the headline decode; its cache is > 2 GB, so no flush.
+    decode_paged: the headline decode over the same rows stored in 128-row pages of a
+    shuffled pool (csattn_attn_decode_paged); > 1 GB of pages, no flush.
     Each: 3 warm-up launches, then `reps` launches, each bracketed by CUDA events on the
     launching stream; the mean is reported."""
     out = {}
@@ -492,6 +494,32 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
                      "frac": round(gbs / hbm_peak, 4), "traffic": None,
                      "kernel": "decode_append_kernel + decode_bf16_kernel<128> + "
                                "decode_combine_kernel"}}
+    # the same decode over a paged copy of the cache: 128-row pages in a shuffled pool
+    kp, vp, table = W.page_cache(kc, vc, lens_h, 128, seed=9)
+    od = torch.empty_like(qn)
+    ws = torch.empty(csattn.decode_workspace_size(wd.B, wd.Hq, table.shape[1] * 128, wd.d, 0),
+                     dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(3 + reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csattn.attn_decode_paged(qn, kp, vp, table, lens, od, scale=wd.scale,
+                                 max_seq_len=max_len, workspace=ws, stream=stream)
+        e1.record(stream)
+        if i >= 3:
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    csattn.check_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    gbs = dbytes / (ms * 1e-3) / 1e9
+    out["decode_paged"] = {
+        "workload": "decode_bf16 (B=64, Hq=32, Hkv=8, d=128, L~U[512,8192]) with the cache in "
+                    "128-row pages, scattered over a shuffled pool (block table per sequence)",
+        "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": dbytes,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "kernel": "decode_bf16_kernel<128> (paged reads) + decode_combine_kernel"}}
+    del kp, vp, table
     # backward of the headline prefill (dq, dk, dv), FLOPs = 2.5x the forward's (the
     # convention for QK^T recomputation + dV + dP + dQ + dK)
     wp = W.WORKLOADS["llama_gqa_bf16"]

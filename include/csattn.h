@@ -205,6 +205,27 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * KV-cache decode over a paged cache (the appended cache of "The Transformer
+ * architecture", section "Hands-on", stored in fixed-size pages):
+ *   k_pages, v_pages [num_pages, Hkv, page_size, d] bf16 (keys already rotated)
+ *   block_table device int32 [B, max_pages]: row t of sequence b lives in page
+ *              block_table[b * max_pages + t / page_size] at offset t % page_size
+ *   q, seq_lens, out, scale, num_splits as csattn_attn_decode; max_seq_len
+ *              <= max_pages * page_size
+ *   workspace  >= csattn_decode_workspace_size(B, Hq, max_pages * page_size, d,
+ *              num_splits) bytes
+ * page_size is a multiple of 64 (one decode tile never crosses a page).  Pages
+ * are read only for rows < seq_lens[b]; a page index outside [0, num_pages)
+ * raises CSATTN_ERR_DEVICE_ARG in the status word and those rows read as zeros.
+ * Other errors and requirements as csattn_attn_decode.
+ */
+int csattn_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                             const int32_t* block_table, const int32_t* seq_lens, void* out, int B,
+                             int Hq, int Hkv, int page_size, int num_pages, int max_pages, int d,
+                             int dtype, float scale, int max_seq_len, int num_splits,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace csattn_attn_decode_step needs: the decode
  * partials of csattn_decode_workspace_size (rounded up to 256 bytes) followed
  * by the rotated queries, B*Hq*d*2 bytes.

@@ -154,6 +154,32 @@ def test_decode_rejects_invalid_arguments(lib, kw, status):
 
 
 @pytest.mark.parametrize("kw,status", [
+    (dict(table=None), -1),
+    (dict(table=FAKE + 2), -1),
+    (dict(page_size=0), -1),
+    (dict(page_size=96), -1),
+    (dict(num_pages=0), -1),
+    (dict(max_pages=0), -1),
+    (dict(max_len=4 * 128 + 1), -1),
+    (dict(d=96), -2),
+    (dict(dtype=0), -2),
+    (dict(seq=None), -1),
+    (dict(splits=2, ws=FAKE, ws_bytes=64), -5),
+])
+def test_decode_paged_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, table=FAKE, seq=FAKE, out=FAKE, B=2, Hq=8, Hkv=2,
+             page_size=128, num_pages=16, max_pages=4, d=128, dtype=1, scale=0.0, max_len=512,
+             splits=0, ws=FAKE, ws_bytes=1 << 24)
+    a.update(kw)
+    rc = lib.csattn_attn_decode_paged(a["q"], a["k"], a["v"], a["table"], a["seq"], a["out"],
+                                      a["B"], a["Hq"], a["Hkv"], a["page_size"], a["num_pages"],
+                                      a["max_pages"], a["d"], a["dtype"], a["scale"], a["max_len"],
+                                      a["splits"], a["ws"], a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"attn_decode_paged" in lib.csattn_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
     (dict(q_new=None), -1),
     (dict(k_new=FAKE + 8), -1),
     (dict(rope_layout=7), -1),

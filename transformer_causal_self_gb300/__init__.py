@@ -53,6 +53,8 @@ _SIGNATURES = {
     "csattn_attn_decode_step": (_c_int, [_vp] * 7 + [_c_int] * 6 + [_c_float, _c_int, _c_float,
                                                                     _c_int, _c_int, _vp, _c_size,
                                                                     _vp]),
+    "csattn_attn_decode_paged": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _c_int, _c_int, _vp,
+                                                                    _c_size, _vp]),
     "csattn_check_status": (_c_int, [_vp]),
     "csattn_selftest_bounded_wait": (_c_int, [_c_int, _vp]),
     "csattn_last_error": (ctypes.c_char_p, []),
@@ -314,6 +316,40 @@ def attn_decode_step(q_new: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tens
                                        _ROPE_LAYOUT[rope_layout], float(scale), int(max_seq_len),
                                        int(num_splits), workspace.data_ptr(), workspace.numel(),
                                        _stream_handle(stream)))
+    return out
+
+
+def attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                      block_table: torch.Tensor, seq_lens: torch.Tensor,
+                      out: Optional[torch.Tensor] = None, *, scale: float = 0.0,
+                      max_seq_len: Optional[int] = None, num_splits: int = 0,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode over a paged cache (C: csattn_attn_decode_paged).
+
+    k_pages/v_pages [num_pages, Hkv, page_size, d]; block_table int32 [B, max_pages] and
+    seq_lens int32 [B] on the device.  max_seq_len defaults to max_pages * page_size.
+    """
+    _need_cuda(q, k_pages, v_pages, block_table, seq_lens)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    B, Hq, _, d = q.shape
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * page_size
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda(out)
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_size(B, Hq, max_pages * page_size, d, num_splits),
+                                dtype=torch.uint8, device=q.device)
+    lib = load_library()
+    _check(lib.csattn_attn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                        block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
+                                        B, Hq, Hkv, page_size, num_pages, max_pages, d,
+                                        _dtype_code(q), float(scale), int(max_seq_len),
+                                        int(num_splits), workspace.data_ptr(), workspace.numel(),
+                                        _stream_handle(stream)))
     return out
 
 

@@ -442,7 +442,8 @@ int decode_check(const char* fn, const void* q, const void* k_cache, const void*
 int decode_impl(const char* fn, const void* q, const void* k_cache, const void* v_cache,
                 const int32_t* seq_lens, int len_add, void* out, int B, int Hq, int Hkv, int Lmax,
                 int d, int dtype, float scale, int max_seq_len, int num_splits, void* workspace,
-                size_t workspace_bytes, void* stream) {
+                size_t workspace_bytes, void* stream, const int32_t* block_table = nullptr,
+                int page_size = 0, int num_pages = 0, int max_pages = 0) {
   int rc = decode_check(fn, q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, Lmax, d, dtype, scale,
                         max_seq_len, num_splits);
   if (rc != CSATTN_OK) return rc;
@@ -452,6 +453,10 @@ int decode_impl(const char* fn, const void* q, const void* k_cache, const void* 
   a.v_cache = v_cache;
   a.seq_lens = seq_lens;
   a.len_add = len_add;
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages;
   a.out = out;
   a.B = B;
   a.Hq = Hq;
@@ -504,6 +509,33 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                        void* workspace, size_t workspace_bytes, void* stream) {
   return decode_impl("attn_decode", q, k_cache, v_cache, seq_lens, 0, out, B, Hq, Hkv, Lmax, d,
                      dtype, scale, max_seq_len, num_splits, workspace, workspace_bytes, stream);
+}
+
+int csattn_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                             const int32_t* block_table, const int32_t* seq_lens, void* out, int B,
+                             int Hq, int Hkv, int page_size, int num_pages, int max_pages, int d,
+                             int dtype, float scale, int max_seq_len, int num_splits,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  const char* fn = "attn_decode_paged";
+  if (block_table == nullptr)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: block_table must be non-null", fn);
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: block_table must be 4-byte aligned", fn);
+  if (page_size < 64 || page_size % 64 != 0 || page_size > 65536)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: page_size=%d must be a multiple of 64 in [64, 65536]",
+                fn, page_size);
+  if (num_pages < 1 || max_pages < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: num_pages=%d and max_pages=%d must be >= 1", fn,
+                num_pages, max_pages);
+  if (Hkv >= 1 && static_cast<long long>(num_pages) * Hkv > (1LL << 31) - 1)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: num_pages * Hkv too large", fn);
+  const long long lmax = static_cast<long long>(max_pages) * page_size;
+  if (lmax > (1 << 30))
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: max_pages * page_size too large", fn);
+  // the logical cache of a sequence is max_pages * page_size rows long
+  return decode_impl(fn, q, k_pages, v_pages, seq_lens, 0, out, B, Hq, Hkv, static_cast<int>(lmax),
+                     d, dtype, scale, max_seq_len, num_splits, workspace, workspace_bytes, stream,
+                     block_table, page_size, num_pages, max_pages);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }

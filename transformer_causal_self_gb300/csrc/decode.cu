@@ -45,6 +45,8 @@ struct DParams {
   const __nv_bfloat16* q;
   const int32_t* seq_lens;
   int len_add;
+  const int32_t* block_table;  // paged cache, or nullptr
+  int page_size, num_pages, max_pages;
   float* part_o;
   float* part_ml;
   uint32_t* status;
@@ -135,10 +137,22 @@ __global__ void __launch_bounds__(kThreads)
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         uint8_t* kdst = smem + s * C::STAGE_BYTES;
         uint8_t* vdst = kdst + C::TILE_BYTES;
-        const int row = k_begin + t * KT;
+        int row = k_begin + t * KT, zz = z;
+        if (p.block_table != nullptr) {
+          // a 64-row tile never crosses a page (page_size and the tile start are
+          // multiples of 64); a page index outside the pool reads zeros (the plane
+          // coordinate is past the tensor map) and is reported
+          int page = p.block_table[static_cast<size_t>(b) * p.max_pages + row / p.page_size];
+          if (page < 0 || page >= p.num_pages) {
+            atomicOr(p.status, kStatusDeviceArg);
+            page = p.num_pages;
+          }
+          zz = page * p.Hkv + kvh;
+          row = row % p.page_size;
+        }
         for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &full[s], kb * 64, row, z);
-          tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &full[s], kb * 64, row, z);
+          tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &full[s], kb * 64, row, zz);
+          tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &full[s], kb * 64, row, zz);
         }
         ++issued;
       }
@@ -369,6 +383,10 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.seq_lens = a.seq_lens;
   p.len_add = a.len_add;
+  p.block_table = a.block_table;
+  p.page_size = a.page_size;
+  p.num_pages = a.num_pages;
+  p.max_pages = a.max_pages;
   p.part_o = a.part_o;
   p.part_ml = a.part_ml;
   p.status = a.status;
@@ -383,8 +401,10 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
 
   alignas(64) CUtensorMap tk, tv;
-  if (!make_tmap_bf16_3d(&tk, a.k_cache, D, a.Lmax, a.B * a.Hkv, KT) ||
-      !make_tmap_bf16_3d(&tv, a.v_cache, D, a.Lmax, a.B * a.Hkv, KT))
+  const int rows = a.block_table != nullptr ? a.page_size : a.Lmax;
+  const int planes = a.block_table != nullptr ? a.num_pages * a.Hkv : a.B * a.Hkv;
+  if (!make_tmap_bf16_3d(&tk, a.k_cache, D, rows, planes, KT) ||
+      !make_tmap_bf16_3d(&tv, a.v_cache, D, rows, planes, KT))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);

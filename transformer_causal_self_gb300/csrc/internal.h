@@ -75,6 +75,11 @@ struct DecodeArgs {
   const void* v_cache;
   const int32_t* seq_lens;
   int len_add;     // sequence b has seq_lens[b] + len_add cached rows
+  // paged cache (block_table != nullptr): k_cache, v_cache are [num_pages, Hkv,
+  // page_size, d]; row t of sequence b is in page block_table[b * max_pages +
+  // t / page_size] at offset t % page_size.  page_size is a multiple of 64.
+  const int32_t* block_table;
+  int page_size, num_pages, max_pages;
   void* out;
   int B, Hq, Hkv, Lmax, d;
   float scale;
