@@ -5,7 +5,11 @@ Tolerance.  The kernels round P and dS to bf16 for the tensor-core products
 (relative error <= 2^-9 each, independent across terms) and accumulate in fp32,
 and take out and lse from the bf16 forward; the gradients are sums of many such
 terms, so their relative L2 error is a few 2^-9 ~ 2e-3.  Bound: relative L2
-<= 1e-2 and max-abs <= 2e-2 * max(1, max |ref|) per tensor."""
+<= 1e-2 and max-abs <= 2e-2 * max(1, max |ref|) per tensor.  The relative L2 is
+taken against max(||ref||, 1e-3 sqrt(n)): where the exact gradient is zero (T = 1,
+a single key, dP and D = rowsum(dO o O) are the same dot product summed in
+different orders, so dS = P (dP - D) is fp32 rounding noise) it bounds the RMS
+error by 1e-5 instead of dividing by zero."""
 import math
 
 import numpy as np
@@ -25,7 +29,7 @@ def _close(got, ref, what):
     ref = np.asarray(ref, np.float64)
     assert np.all(np.isfinite(got)), f"{what}: non-finite"
     err = float(np.max(np.abs(got - ref)))
-    rl2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+    rl2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-3 * math.sqrt(ref.size)))
     assert rl2 <= 1e-2 and err <= 2e-2 * max(1.0, float(np.max(np.abs(ref)))), \
         f"{what}: max-abs {err:.3e} (ref max {np.max(np.abs(ref)):.3e}), rel-L2 {rl2:.3e}"
 

@@ -442,26 +442,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   }
 }
 
-// D[row] = sum_c dO[row, c] O[row, c] (fp32), one warp per row
+// D[row] = sum_c dO[row, c] O[row, c] (fp32).  A row is d/8 lanes, each with one
+// 16-byte load of dO and of O (d in {64, 128, 256}: 4, 2 or 1 rows per warp), the
+// partial sums reduced over the row's lanes with shuffles.
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ dout,
                                                          const __nv_bfloat16* __restrict__ out,
                                                          float* __restrict__ dvec, long long rows,
                                                          int d) {
-  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const __nv_bfloat16* a = dout + row * d;
-  const __nv_bfloat16* o = out + row * d;
+  const int lpr = d / 8;  // lanes per row
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = t / lpr;
+  const int c = static_cast<int>(t % lpr) * 8;
   float sum = 0.f;
-  for (int c = 2 * lane; c < d; c += 64) {
-    const uint32_t wa = *reinterpret_cast<const uint32_t*>(a + c);
-    const uint32_t wo = *reinterpret_cast<const uint32_t*>(o + c);
-    sum = fmaf(bf16lo_to_f32(wa), bf16lo_to_f32(wo), sum);
-    sum = fmaf(bf16hi_to_f32(wa), bf16hi_to_f32(wo), sum);
-  }
+  if (row < rows) {
+    const uint4 wa = __ldg(reinterpret_cast<const uint4*>(dout + row * d + c));
+    const uint4 wo = __ldg(reinterpret_cast<const uint4*>(out + row * d + c));
+    const uint32_t a4[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t o4[4] = {wo.x, wo.y, wo.z, wo.w};
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  if (lane == 0) dvec[row] = sum;
+    for (int e = 0; e < 4; ++e) {
+      sum = fmaf(bf16lo_to_f32(a4[e]), bf16lo_to_f32(o4[e]), sum);
+      sum = fmaf(bf16hi_to_f32(a4[e]), bf16hi_to_f32(o4[e]), sum);
+    }
+  }
+  for (int off = lpr / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (row < rows && (threadIdx.x & (lpr - 1)) == 0) dvec[row] = sum;
 }
 
 template <int D>
@@ -488,7 +493,7 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t stream) {
   p.theta = a.theta;
 
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.Tq;
-  bwd_rowdot_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+  bwd_rowdot_kernel<<<static_cast<unsigned>((rows * (D / 8) + 255) / 256), 256, 0, stream>>>(
       p.dout, static_cast<const __nv_bfloat16*>(a.out), a.dvec, rows, D);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -517,7 +522,7 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream) {
   if (a.d != 128 || a.Tq != a.Tk || a.q_off != 0) return cudaErrorInvalidValue;
   // d = 128: D = rowsum(dout o out), then the two tcgen05 kernels (bwd_tc.cu)
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.Tq;
-  bwd_rowdot_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+  bwd_rowdot_kernel<<<static_cast<unsigned>((rows * (128 / 8) + 255) / 256), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.dout), static_cast<const __nv_bfloat16*>(a.out), a.dvec,
       rows, 128);
   cudaError_t e = cudaGetLastError();

@@ -7,17 +7,17 @@
 //   S^T  = Kr Qr^T          M=128 keys, N=128 queries, K=128   (SS, TMEM cols [0,128))
 //   dP^T = V dO^T           same shapes                         (SS, cols [128,256))
 //   P^T  = exp(scale*S^T - lse)   dS^T = P^T o (dP^T - D)      (softmax warpgroups)
-//   dV  += P^T dO           M=128 keys, N=128 channels, K=128 queries (TS, cols [256,384))
+//   dV  += P^T dO           M=128 keys, N=128 channels, K=128 queries (SS, cols [256,384))
 //   dK  += dS^T Qr          same                                      (TS, cols [384,512))
 //
-// P^T and dS^T (bf16) are written back into TMEM over the S^T and dP^T columns
-// they were computed from and feed the last two products as the A operand.
+// P^T (bf16) goes to shared memory (K-major, 128-byte swizzle) and feeds dV as
+// the A operand, so the S^T columns are free as soon as the softmax warps have
+// read them and S^T of the next tile overlaps this tile's softmax; dS^T (bf16)
+// is written back into TMEM over the dP^T columns and feeds dK from there.
 // Warps 0-3 handle queries 0-63 of the tile, warps 4-7 queries 64-127 (thread =
 // key row = TMEM lane); warp 8 loads (TMA for Qr and dO, plain loads for lse and
-// D); warp 9 allocates TMEM and issues the MMAs.  The tensor core runs
-// S^T, dP^T -> (softmax) -> dV, dK in sequence per tile: TMEM holds one tile's
-// S^T and dP^T next to the two 128-column accumulators, so the next tile's
-// products wait for this tile's P^T and dS^T to be consumed.
+// D); warp 9 allocates TMEM and issues the MMAs in the order S^T(it+1), dV(it),
+// dK(it), dP^T(it+1): dK(it) frees the dS^T columns for dP^T(it+1).
 //
 // Every wait is bounded (2 s) and sets the status word's timeout bit; no named
 // barriers, so a warp that gives up just leaves its loop.
@@ -36,13 +36,14 @@ constexpr int NSQ = 2;  // Q / dO stages
 constexpr int TILE = BQ * D * 2;        // 32 KB
 constexpr int BLOCK = BQ * 128;         // one 64-channel column block of a tile
 constexpr int VEC = 2 * BQ * 4;         // lse and D of one tile, fp32
-constexpr int SMEM_DATA = 2 * TILE + NSQ * 2 * TILE + NSQ * VEC;
+constexpr int SMEM_DATA = 2 * TILE + NSQ * 2 * TILE + TILE + NSQ * VEC;  // + P^T tile
 constexpr int SMEM_BYTES = SMEM_DATA + 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, 0, 0);  // both K-major
 constexpr uint32_t IDESC_TS = idesc_bf16_f32(128, 128, 0, 1);  // B (dO / Qr) MN-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, 0, 1);  // A = P^T K-major, B = dO MN-major
 
 struct KvParams {
   const float* lse;   // [B, Hq, T], natural log
@@ -76,7 +77,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = smem + TILE;
   uint8_t* sQ = smem + 2 * TILE;                 // [NSQ] tiles
   uint8_t* sO = smem + (2 + NSQ) * TILE;         // [NSQ] dO tiles
-  float* sVec = reinterpret_cast<float*>(smem + (2 + 2 * NSQ) * TILE);  // [NSQ][lse 128 | D 128]
+  uint8_t* sP = smem + (2 + 2 * NSQ) * TILE;     // P^T: rows = keys, queries contiguous
+  float* sVec = reinterpret_cast<float*>(smem + (3 + 2 * NSQ) * TILE);  // [NSQ][lse 128 | D 128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_DATA);
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;   // [NSQ]: Qr and dO tiles (TMA bytes)
@@ -88,7 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* teardown = bars + 9;
   uint64_t* dp_full = bars + 10; // dP^T in TMEM
   uint64_t* vec_full = bars + 11; // [NSQ]: lse and D of the tile stored by the load warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* s_free = bars + 13;   // S^T read by the softmax warps (8 warps)
+  uint64_t* dv_done = bars + 14;  // dV(it) complete: the P^T tile may be rewritten
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -117,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(p_full, 8);
     mbar_init(ds_full, 8);
+    mbar_init(s_free, 8);
+    mbar_init(dv_done, 1);
     mbar_init(acc_full, 1);
     mbar_init(teardown, 1);
     *abort_flag = 0;
@@ -205,26 +211,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(dp_full);
       };
-      // Order per tile: dV(it) frees the P^T columns, so S^T(it+1) follows it at once and
-      // runs while the softmax warps compute dS^T(it); dK(it) frees the dS^T columns for
-      // dP^T(it+1).
+      // Order per tile: S^T(it+1) as soon as the softmax warps have read S^T(it), so it
+      // overlaps their work on tile it; dK(it) frees the dS^T columns for dP^T(it+1).
       if (n_it > 0 && wait(&q_full[0], 0)) {
         issue_st(0);
         issue_dpt(0);
       }
+      const uint32_t p_s = smem_u32(sP);
       for (int it = 0; it < n_it && ok; ++it) {
         const uint32_t q_s = q_tile(it), o_s = o_tile(it);
-        if (!wait(p_full, it & 1)) break;
-        // dV += P^T dO: A = P^T (TMEM), B = dO (rows = queries, channels contiguous)
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          umma_ts(tmem + 256u, tmem + packed_col(kk), smem_desc_sw128(o_s + 2048u * kk, BLOCK, 1024),
-                  IDESC_TS, (it > 0 || kk > 0) ? 1u : 0u);
         const bool next = it + 1 < n_it;
         if (next) {
+          if (!wait(s_free, it & 1)) break;
           if (!wait(&q_full[(it + 1) % NSQ], ((it + 1) / NSQ) & 1)) break;
           issue_st(it + 1);
         }
+        if (!wait(p_full, it & 1)) break;
+        // dV += P^T dO: A = P^T (shared memory, K-major), B = dO (rows = queries,
+        // channels contiguous)
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
+          umma_ss(tmem + 256u, smem_desc_sw128(p_s + off, 16, 1024),
+                  smem_desc_sw128(o_s + 2048u * kk, BLOCK, 1024), IDESC_PV,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(dv_done);
         if (!wait(ds_full, it & 1)) break;
         // dK += dS^T Qr
 #pragma unroll
@@ -247,8 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = k0 + row;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(64 * x);
-    const uint32_t tP = tS;                           // P^T packed: 32 columns
     const uint32_t tD = tmem + lane_off + 128u + static_cast<uint32_t>(64 * x);
+    // this thread's row of P^T: 64 queries = one 128-byte row of column block x
+    uint8_t* const prow = sP + x * BLOCK + row * 128;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSQ;
@@ -267,25 +280,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* dv = lse2 + BQ;
       float pt[64];
       {
-        uint32_t r[32];
+        uint32_t r[64];
+        tmem_ld64_sync(tS, r);
+        // S^T(it) is in registers: the MMA warp may write S^T(it+1)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tmem_ld32_sync(tS + 32u * h, r);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int q = q0 + 32 * h + c;
-            const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
-            pt[32 * h + c] =
-                vis ? ex2_approx(fmaf(__uint_as_float(r[c]), p.sl2, -lse2[32 * h + c])) : 0.f;
-          }
+        for (int c = 0; c < 64; ++c) {
+          const int q = q0 + c;
+          const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
+          pt[c] = vis ? ex2_approx(fmaf(__uint_as_float(r[c]), p.sl2, -lse2[c])) : 0.f;
         }
-        uint32_t pk[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) pk[t] = pack_bf16x2(pt[2 * t], pt[2 * t + 1]);
-        tmem_st32(tP, pk);
-        tmem_st_wait();
       }
-      tc_fence_before();
+      // the P^T tile is free once dV(it-1) has completed
+      if (it > 0 && !warp_wait(dv_done, (it - 1) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
+            make_uint4(pack_bf16x2(pt[8 * c], pt[8 * c + 1]), pack_bf16x2(pt[8 * c + 2], pt[8 * c + 3]),
+                       pack_bf16x2(pt[8 * c + 4], pt[8 * c + 5]),
+                       pack_bf16x2(pt[8 * c + 6], pt[8 * c + 7]));
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
       if (!warp_wait(dp_full, it & 1, abort_flag, p.status)) {
@@ -584,6 +603,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
+      // P = exp(S - lse) while dP(j) is still being computed
+      float pr[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int key = kb0 + c;
+        const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
+        pr[c] = vis ? ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2)) : 0.f;
+      }
       if (!warp_wait(dp_full, j & 1, abort_flag, p.status)) {
         ok = false;
         break;
@@ -596,17 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32_sync(tD + 32u * hh, rd);
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-          float v[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = 2 * t + u;
-            const int key = kb0 + 32 * hh + c;
-            const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
-            const float pr =
-                vis ? ex2_approx(fmaf(__uint_as_float(rs[32 * hh + c]), p.sl2, -lse2)) : 0.f;
-            v[u] = pr * (__uint_as_float(rd[c]) - dq_d);
-          }
-          pk[16 * hh + t] = pack_bf16x2(v[0], v[1]);
+          const int c = 2 * t;
+          pk[16 * hh + t] = pack_bf16x2(pr[32 * hh + c] * (__uint_as_float(rd[c]) - dq_d),
+                                        pr[32 * hh + c + 1] * (__uint_as_float(rd[c + 1]) - dq_d));
         }
       }
       tmem_st32(tD, pk);  // dS over dP (this half's 64 keys, packed into 32 columns)
