@@ -286,11 +286,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free);
+        // every (key, query) of this warpgroup's half tile is visible: no per-element test
+        const bool all_vis =
+            q0 + 63 < p.T && k0 + BK <= p.T && (!p.causal || q0 >= k0 + BK - 1);
+        if (all_vis) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int q = q0 + c;
-          const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
-          pt[c] = vis ? ex2_approx(fmaf(__uint_as_float(r[c]), p.sl2, -lse2[c])) : 0.f;
+          for (int c = 0; c < 64; ++c)
+            pt[c] = ex2_approx(fmaf(__uint_as_float(r[c]), p.sl2, -lse2[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int q = q0 + c;
+            const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
+            pt[c] = vis ? ex2_approx(fmaf(__uint_as_float(r[c]), p.sl2, -lse2[c])) : 0.f;
+          }
         }
       }
       // the P^T tile is free once dV(it-1) has completed
@@ -605,11 +614,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(s_free);
       // P = exp(S - lse) while dP(j) is still being computed
       float pr[64];
+      // every (query, key) of this warpgroup's half tile is visible: no per-element test
+      const bool all_vis =
+          kb0 + 63 < p.T && q0 + BQ <= p.T && (!p.causal || kb0 + 63 <= q0);
+      if (all_vis) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int key = kb0 + c;
-        const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
-        pr[c] = vis ? ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2)) : 0.f;
+        for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const int key = kb0 + c;
+          const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
+          pr[c] = vis ? ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2)) : 0.f;
+        }
       }
       if (!warp_wait(dp_full, j & 1, abort_flag, p.status)) {
         ok = false;
