@@ -118,7 +118,7 @@ __device__ __forceinline__ void rope_transpose_rows(float (&acc)[D / 8][4], int 
       for (int e = 0; e < 4; ++e) {
         const int p = 8 * nt + cq + (e & 1);
         float c, s;
-        rope_cos_sin<true>((e < 2) ? pos0 : pos1, th.hi[p], th.lo[p], c, s);
+        rope_cos_sin<false>((e < 2) ? pos0 : pos1, th.hi[p], th.lo[p], c, s);
         const float a = acc[nt][e], b = acc[nt + D / 16][e];
         acc[nt][e] = fmaf(a, c, b * s);
         acc[nt + D / 16][e] = fmaf(-a, s, b * c);
@@ -130,7 +130,7 @@ __device__ __forceinline__ void rope_transpose_rows(float (&acc)[D / 8][4], int 
       for (int h = 0; h < 2; ++h) {
         const int p = (8 * nt + cq) >> 1;
         float c, s;
-        rope_cos_sin<true>(h ? pos1 : pos0, th.hi[p], th.lo[p], c, s);
+        rope_cos_sin<false>(h ? pos1 : pos0, th.hi[p], th.lo[p], c, s);
         const float a = acc[nt][2 * h], b = acc[nt][2 * h + 1];
         acc[nt][2 * h] = fmaf(a, c, b * s);
         acc[nt][2 * h + 1] = fmaf(-a, s, b * c);

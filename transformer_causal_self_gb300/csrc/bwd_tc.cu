@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               float cs, sn;
-              rope_cos_sin<true>(key, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
+              rope_cos_sin<false>(key, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
               const float u = a0[e], w = a1[e];
               a0[e] = fmaf(u, cs, w * sn);
               a1[e] = fmaf(-u, sn, w * cs);
@@ -379,11 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
               float cs, sn;
-              rope_cos_sin<true>(key, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
+              rope_cos_sin<false>(key, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
               float u = a0[2 * t], w = a0[2 * t + 1];
               a0[2 * t] = fmaf(u, cs, w * sn);
               a0[2 * t + 1] = fmaf(-u, sn, w * cs);
-              rope_cos_sin<true>(key, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs,
+              rope_cos_sin<false>(key, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs,
                                  sn);
               u = a1[2 * t];
               w = a1[2 * t + 1];
@@ -670,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           float cs, sn;
-          rope_cos_sin<true>(q, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
+          rope_cos_sin<false>(q, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
           const float u = a0[e], w = a1[e];
           a0[e] = fmaf(u, cs, w * sn);
           a1[e] = fmaf(-u, sn, w * cs);
@@ -679,11 +679,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
           float cs, sn;
-          rope_cos_sin<true>(q, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
+          rope_cos_sin<false>(q, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
           float u = a0[2 * t], w = a0[2 * t + 1];
           a0[2 * t] = fmaf(u, cs, w * sn);
           a0[2 * t + 1] = fmaf(-u, sn, w * cs);
-          rope_cos_sin<true>(q, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs, sn);
+          rope_cos_sin<false>(q, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs, sn);
           u = a1[2 * t];
           w = a1[2 * t + 1];
           a1[2 * t] = fmaf(u, cs, w * sn);
