@@ -420,29 +420,70 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dQ for d = 128: one CTA per (128 queries, query head, batch), walking the key
-// tiles the queries see.  Per key tile j:
+// dQ for d = 128, persistent: one CTA per SM walks work items (128 queries of one
+// query head), longest first (causally the last query tiles), in rounds of
+// gridDim.x items with alternating direction.  Per item, per key tile j:
 //   S  = Qr Kr_j^T, dP = dO V_j^T   (SS, TMEM columns [0,128) and [128,256))
 //   dS = exp(scale*S - lse) o (dP - D)  (thread = query row; warps 0-3 keys 0-63,
 //                                        warps 4-7 keys 64-127), bf16 into dP's columns
-//   dQ += dS Kr_j                   (TS, B = Kr_j with channels contiguous; [256,384))
-// K_j and V_j arrive by TMA through a two-stage ring.  S(j+1) is issued as soon as the
-// softmax warps have read S(j), so it overlaps their dS work; dP(j+1) follows dQ(j).
+//   dQ += dS Kr_j                   (TS, B = Kr_j with channels contiguous)
+// into one of two accumulators ([256,384) for even items, [384,512) for odd ones),
+// so the next item's products start while warps 12-15 drain the finished dQ
+// (R^T, scale, store).  K_j and V_j arrive by TMA through a two-stage ring that
+// runs across items; S(g+1) is issued as soon as the softmax warps have read S(g)
+// (g counts key tiles over all items of the CTA), dP(g+1) follows dQ(g).
 constexpr int NSKV = 2;
 constexpr int Q_SMEM_DATA = 2 * TILE + NSKV * 2 * TILE;
 constexpr int Q_SMEM_BYTES = Q_SMEM_DATA + 256;
+constexpr int kThreadsQ = 512;
+constexpr int kWarpEpiQ = 12;       // warps 12-15: dQ epilogue (TMEM lane quadrants 0-3)
+constexpr int kRegsSoftmaxQ = 152;  // 2*128*152 + 128*96 + 128*112 = 65536 = 512 * 128
+constexpr int kRegsCtlQ = 96;
+constexpr int kRegsEpiQ = 112;
 
 struct QParams {
   const float* lse;
   const float* dvec;
   __nv_bfloat16* dq;
   uint32_t* status;
-  int Hq, Hkv, T, causal, rope;
+  int B, Hq, Hkv, T, causal, rope, n_items;
   float scale, sl2;
   RopeTable theta;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+struct QItem {
+  int qt, b, h, n_it;
+};
+
+// i-th item of this CTA: rounds of gridDim.x items, alternating direction
+__device__ __forceinline__ int q_item_index(int i) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return i * G + ((i & 1) ? (G - 1 - c) : c);
+}
+
+__device__ __forceinline__ QItem q_item(const QParams& p, int u) {
+  const int n_qtiles = (p.T + BQ - 1) / BQ;
+  const int n_kt = (p.T + BK - 1) / BK;
+  const int per = p.B * p.Hq;
+  const int r = u / per, rem = u - r * per;
+  QItem it;
+  it.qt = p.causal ? n_qtiles - 1 - r : r;
+  it.b = rem / p.Hq;
+  it.h = rem - it.b * p.Hq;
+  it.n_it = p.causal ? min(n_kt, it.qt + 1) : n_kt;
+  return it;
+}
+
+template <int N>
+__device__ __forceinline__ void q_regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void q_regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+__global__ void __launch_bounds__(kThreadsQ, 1)
     bwd_q_tc_kernel(const __grid_constant__ QParams p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -453,15 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sKV = smem + 2 * TILE;  // [NSKV] x (K tile, V tile)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Q_SMEM_DATA);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [NSKV]
-  uint64_t* kv_empty = bars + 3;  // [NSKV]
-  uint64_t* s_full = bars + 5;
-  uint64_t* ds_full = bars + 6;   // 8 warps
-  uint64_t* acc_full = bars + 7;
-  uint64_t* teardown = bars + 8;
-  uint64_t* dp_full = bars + 9;
-  uint64_t* s_free = bars + 10;   // 8 warps: S(j) read
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* q_empty = bars + 1;   // the item's last S and dP completed
+  uint64_t* kv_full = bars + 2;   // [NSKV]
+  uint64_t* kv_empty = bars + 4;  // [NSKV]
+  uint64_t* s_full = bars + 6;
+  uint64_t* s_free = bars + 7;    // 8 warps: S(g) read
+  uint64_t* dp_full = bars + 8;
+  uint64_t* ds_full = bars + 9;   // 8 warps
+  uint64_t* acc_full = bars + 10;   // [2] dQ accumulator complete
+  uint64_t* acc_empty = bars + 12;  // [2] 4 epilogue warps have read it
+  uint64_t* teardown = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -469,26 +512,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicOr(p.status, kStatusDeviceArg);
     return;
   }
-  // grid (Hq, B, query tiles), z slowest: causally, the last query tiles (most key
-  // tiles to visit) are launched first
-  const int n_qtiles = (p.T + BQ - 1) / BQ;
-  const int qt = p.causal ? n_qtiles - 1 - static_cast<int>(blockIdx.z) : blockIdx.z;
-  const int q0 = qt * BQ, h = blockIdx.x, b = blockIdx.y;
-  const int g = h / (p.Hq / p.Hkv);
-  const int n_kt = (p.T + BK - 1) / BK;
-  const int n_it = p.causal ? min(n_kt, qt + 1) : n_kt;  // key tiles seen
-
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < NSKV; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(dp_full, 1);
     mbar_init(s_free, 8);
+    mbar_init(dp_full, 1);
     mbar_init(ds_full, 8);
-    mbar_init(acc_full, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
     mbar_init(teardown, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -499,37 +537,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kWarpProducer) {
+  if (warp >= 8 && warp < kWarpEpiQ) {
+   q_regs_dec<kRegsCtlQ>();
+   if (warp == kWarpProducer) {
     if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int zq = b * p.Hq + h, zk = b * p.Hkv + g;
-      mbar_arrive_expect_tx(q_full, 2 * TILE);
-      for (int kb = 0; kb < D / 64; ++kb) {
-        tma_load_3d(sQ + kb * BLOCK, &tm_q, q_full, kb * 64, q0, zq);
-        tma_load_3d(sO + kb * BLOCK, &tm_do, q_full, kb * 64, q0, zq);
-      }
-      int issued = 0;
-      for (int j = 0; j < n_it; ++j) {
-        const int st = j % NSKV, use = j / NSKV;
-        if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, abort_flag, p.status, kWaitNs))
-          break;
-        uint8_t* dst = sKV + st * 2 * TILE;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * TILE);
+      bool ok = true;
+      int g = 0, issued = 0, items = 0;
+      for (int i = 0; ok; ++i) {
+        const int u = q_item_index(i);
+        if (u >= p.n_items) break;
+        const QItem it = q_item(p, u);
+        const int zq = it.b * p.Hq + it.h, zk = it.b * p.Hkv + it.h / (p.Hq / p.Hkv);
+        if (i > 0 && !mbar_wait(q_empty, (i - 1) & 1, abort_flag, p.status, kWaitNs)) break;
+        mbar_arrive_expect_tx(q_full, 2 * TILE);
         for (int kb = 0; kb < D / 64; ++kb) {
-          tma_load_3d(dst + kb * BLOCK, &tm_k, &kv_full[st], kb * 64, j * BK, zk);
-          tma_load_3d(dst + TILE + kb * BLOCK, &tm_v, &kv_full[st], kb * 64, j * BK, zk);
+          tma_load_3d(sQ + kb * BLOCK, &tm_q, q_full, kb * 64, it.qt * BQ, zq);
+          tma_load_3d(sO + kb * BLOCK, &tm_do, q_full, kb * 64, it.qt * BQ, zq);
         }
-        ++issued;
+        ++items;
+        for (int j = 0; j < it.n_it; ++j, ++g) {
+          const int st = g % NSKV, use = g / NSKV;
+          if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, abort_flag, p.status, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = sKV + st * 2 * TILE;
+          mbar_arrive_expect_tx(&kv_full[st], 2 * TILE);
+          for (int kb = 0; kb < D / 64; ++kb) {
+            tma_load_3d(dst + kb * BLOCK, &tm_k, &kv_full[st], kb * 64, j * BK, zk);
+            tma_load_3d(dst + TILE + kb * BLOCK, &tm_v, &kv_full[st], kb * 64, j * BK, zk);
+          }
+          ++issued;
+        }
       }
       if (*abort_flag) {
-        mbar_wait(q_full, 0, nullptr, p.status, kDrainNs);
+        if (items > 0) mbar_wait(q_full, (items - 1) & 1, nullptr, p.status, kDrainNs);
         const int first = issued > NSKV ? issued - NSKV : 0;
         for (int t = first; t < issued; ++t)
           mbar_wait(&kv_full[t % NSKV], (t / NSKV) & 1, nullptr, p.status, kDrainNs);
       }
     }
-  } else if (warp == kWarpMma) {
+   } else if (warp == kWarpMma) {
     if (lane == 0) {
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -539,9 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return ok;
       };
       const uint32_t q_s = smem_u32(sQ), o_s = smem_u32(sO);
-      auto k_tile = [&](int j) { return smem_u32(sKV + (j % NSKV) * 2 * TILE); };
-      auto issue_s = [&](int j) {  // S = Qr Kr_j^T
-        const uint32_t k_s = k_tile(j);
+      auto k_tile = [&](int g) { return smem_u32(sKV + (g % NSKV) * 2 * TILE); };
+      auto issue_s = [&](int g) {  // S = Qr Kr^T
+        const uint32_t k_s = k_tile(g);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
@@ -550,8 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(s_full);
       };
-      auto issue_dp = [&](int j) {  // dP = dO V_j^T
-        const uint32_t v_s = k_tile(j) + TILE;
+      auto issue_dp = [&](int g) {  // dP = dO V^T
+        const uint32_t v_s = k_tile(g) + TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
@@ -560,152 +612,195 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(dp_full);
       };
-      if (wait(q_full, 0) && wait(&kv_full[0], 0)) {
-        issue_s(0);
-        issue_dp(0);
-      }
-      for (int j = 0; j < n_it && ok; ++j) {
-        const bool next = j + 1 < n_it;
-        if (!wait(s_free, j & 1)) break;
-        if (next) {
-          if (!wait(&kv_full[(j + 1) % NSKV], ((j + 1) / NSKV) & 1)) break;
-          issue_s(j + 1);
-        }
-        if (!wait(ds_full, j & 1)) break;
-        // dQ += dS Kr_j: A = dS (TMEM, over dP), B = Kr_j as (channels x keys)
-        const uint32_t k_s = k_tile(j);
+      int g = 0;
+      for (int i = 0; ok; ++i) {
+        const int u = q_item_index(i);
+        if (u >= p.n_items) break;
+        const QItem it = q_item(p, u);
+        const int ab = i & 1;
+        const uint32_t t_acc = tmem + 256u + 128u * static_cast<uint32_t>(ab);
+        // S(g), dP(g) of the item's first key tile: its Q and dO, the S columns read
+        // (s_free of the previous tile), the dP columns consumed (dQ issued before)
+        if (!wait(q_full, i & 1)) break;
+        if (g > 0 && !wait(s_free, (g - 1) & 1)) break;
+        if (!wait(&kv_full[g % NSKV], (g / NSKV) & 1)) break;
+        issue_s(g);
+        issue_dp(g);
+        if (it.n_it == 1) tc_commit(q_empty);
+        for (int j = 0; j < it.n_it && ok; ++j, ++g) {
+          const bool next = j + 1 < it.n_it;
+          if (next) {
+            if (!wait(s_free, g & 1)) break;
+            if (!wait(&kv_full[(g + 1) % NSKV], ((g + 1) / NSKV) & 1)) break;
+            issue_s(g + 1);
+          }
+          if (!wait(ds_full, g & 1)) break;
+          // the accumulator's previous item (i - 2) has been read by the epilogue warps
+          if (j == 0 && i >= 2 && !wait(&acc_empty[ab], ((i >> 1) - 1) & 1)) break;
+          // dQ += dS Kr: A = dS (TMEM, over dP), B = Kr as (channels x keys)
+          const uint32_t k_s = k_tile(g);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma_ts(tmem + 256u, tmem + 128u + packed_col(kk),
-                  smem_desc_sw128(k_s + 2048u * kk, BLOCK, 1024), IDESC_TS,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&kv_empty[j % NSKV]);
-        if (next) issue_dp(j + 1);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_ts(t_acc, tmem + 128u + packed_col(kk), smem_desc_sw128(k_s + 2048u * kk, BLOCK, 1024),
+                    IDESC_TS, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&kv_empty[g % NSKV]);
+          if (next) {
+            issue_dp(g + 1);
+            if (j + 2 == it.n_it) tc_commit(q_empty);  // S and dP of the last key tile issued
+          } else {
+            tc_commit(&acc_full[ab]);
+          }
+        }
       }
-      tc_commit(acc_full);
       tc_commit(teardown);
       mbar_wait(teardown, 0, nullptr, p.status, kDrainNs);
     }
     __syncwarp();
+   }
   } else if (warp < 8) {
+    q_regs_inc<kRegsSoftmaxQ>();
     const int x = warp >> 2;              // key half of the tile
     const int row = threadIdx.x & 127;    // query row = TMEM lane
-    const int q = q0 + row;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(64 * x);
     const uint32_t tD = tmem + lane_off + 128u + static_cast<uint32_t>(64 * x);
-    const size_t rb = static_cast<size_t>(b * p.Hq + h) * p.T;
-    const float lse2 = q < p.T ? p.lse[rb + q] * kLog2e : 0.f;
-    const float dq_d = q < p.T ? p.dvec[rb + q] : 0.f;
     bool ok = true;
-    for (int j = 0; j < n_it; ++j) {
-      if (!warp_wait(s_full, j & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int kb0 = j * BK + 64 * x;  // first key of this half
-      uint32_t rs[64];
-      tmem_ld32_sync(tS, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
-      tmem_ld32_sync(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
-      // S(j) is in registers: the MMA warp may overwrite it with S(j+1)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-      // P = exp(S - lse) while dP(j) is still being computed
-      float pr[64];
-      // every (query, key) of this warpgroup's half tile is visible: no per-element test
-      const bool all_vis =
-          kb0 + 63 < p.T && q0 + BQ <= p.T && (!p.causal || kb0 + 63 <= q0);
-      if (all_vis) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int key = kb0 + c;
-          const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
-          pr[c] = vis ? ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2)) : 0.f;
+    int g = 0;
+    for (int i = 0; ok; ++i) {
+      const int u = q_item_index(i);
+      if (u >= p.n_items) break;
+      const QItem it = q_item(p, u);
+      const int q0 = it.qt * BQ, q = q0 + row;
+      const size_t rb = static_cast<size_t>(it.b * p.Hq + it.h) * p.T;
+      const float lse2 = q < p.T ? p.lse[rb + q] * kLog2e : 0.f;
+      const float dq_d = q < p.T ? p.dvec[rb + q] : 0.f;
+      for (int j = 0; j < it.n_it; ++j, ++g) {
+        if (!warp_wait(s_full, g & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
         }
-      }
-      if (!warp_wait(dp_full, j & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t pk[32];
+        tc_fence_after();
+        const int kb0 = j * BK + 64 * x;  // first key of this half
+        uint32_t rs[64];
+        tmem_ld64_sync(tS, rs);
+        // S(g) is in registers: the MMA warp may overwrite it with S(g+1)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        // P = exp(S - lse) while dP(g) is still being computed
+        float pr[64];
+        // every (query, key) of this warpgroup's half tile is visible: no per-element test
+        const bool all_vis =
+            kb0 + 63 < p.T && q0 + BQ <= p.T && (!p.causal || kb0 + 63 <= q0);
+        if (all_vis) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t rd[32];
-        tmem_ld32_sync(tD + 32u * hh, rd);
+          for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2));
+        } else {
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const int c = 2 * t;
-          pk[16 * hh + t] = pack_bf16x2(pr[32 * hh + c] * (__uint_as_float(rd[c]) - dq_d),
-                                        pr[32 * hh + c + 1] * (__uint_as_float(rd[c + 1]) - dq_d));
+          for (int c = 0; c < 64; ++c) {
+            const int key = kb0 + c;
+            const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
+            pr[c] = vis ? ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2)) : 0.f;
+          }
         }
+        if (!warp_wait(dp_full, g & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t pk[32];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t rd[32];
+          tmem_ld32_sync(tD + 32u * hh, rd);
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const int c = 2 * t;
+            pk[16 * hh + t] = pack_bf16x2(pr[32 * hh + c] * (__uint_as_float(rd[c]) - dq_d),
+                                          pr[32 * hh + c + 1] * (__uint_as_float(rd[c + 1]) - dq_d));
+          }
+        }
+        tmem_st32(tD, pk);  // dS over dP (this half's 64 keys, packed into 32 columns)
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_full);
       }
-      tmem_st32(tD, pk);  // dS over dP (this half's 64 keys, packed into 32 columns)
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
     }
-    // epilogue: dQ = R^T (scale dQ); warpgroup x takes columns [32x, 32x+32) and
-    // [64+32x, 64+32x+32) so that split-half pairs (i, i + 64) meet in one thread
-    if (ok && warp_wait(acc_full, 0, abort_flag, p.status)) {
+  } else {
+    // ------------------------------------------------------------ dQ epilogue (warps 12-15)
+    // thread = query row; dQ = R^T (scale dQ) with split-half pairs (i, i + 64) taken
+    // as column chunks (32c + e, 64 + 32c + e)
+    q_regs_dec<kRegsEpiQ>();
+    const int row = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int i = 0;; ++i) {
+      const int u = q_item_index(i);
+      if (u >= p.n_items) break;
+      const QItem it = q_item(p, u);
+      const int ab = i & 1;
+      const int q = it.qt * BQ + row;
+      if (!warp_wait(&acc_full[ab], (i >> 1) & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      const int c = x;
-      float a0[32], a1[32];
-      {
-        uint32_t r[32];
-        tmem_ld32_sync(tmem + lane_off + 256u + 32u * c, r);
+      const uint32_t t_acc = tmem + lane_off + 256u + 128u * static_cast<uint32_t>(ab);
+      __nv_bfloat16* dst = p.dq + (static_cast<size_t>(it.b * p.Hq + it.h) * p.T + q) * D;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float a0[32], a1[32];
+        {
+          uint32_t r[32];
+          tmem_ld32_sync(t_acc + 32u * c, r);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) a0[e] = __uint_as_float(r[e]) * p.scale;
-        tmem_ld32_sync(tmem + lane_off + 256u + 64u + 32u * c, r);
+          for (int e = 0; e < 32; ++e) a0[e] = __uint_as_float(r[e]) * p.scale;
+          tmem_ld32_sync(t_acc + 64u + 32u * c, r);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) a1[e] = __uint_as_float(r[e]) * p.scale;
-      }
-      if (p.rope == 1) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float cs, sn;
-          rope_cos_sin<false>(q, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
-          const float u = a0[e], w = a1[e];
-          a0[e] = fmaf(u, cs, w * sn);
-          a1[e] = fmaf(-u, sn, w * cs);
+          for (int e = 0; e < 32; ++e) a1[e] = __uint_as_float(r[e]) * p.scale;
         }
-      } else if (p.rope == 2) {
+        if (p.rope == 1) {
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          float cs, sn;
-          rope_cos_sin<false>(q, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
-          float u = a0[2 * t], w = a0[2 * t + 1];
-          a0[2 * t] = fmaf(u, cs, w * sn);
-          a0[2 * t + 1] = fmaf(-u, sn, w * cs);
-          rope_cos_sin<false>(q, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs, sn);
-          u = a1[2 * t];
-          w = a1[2 * t + 1];
-          a1[2 * t] = fmaf(u, cs, w * sn);
-          a1[2 * t + 1] = fmaf(-u, sn, w * cs);
+          for (int e = 0; e < 32; ++e) {
+            float cs, sn;
+            rope_cos_sin<false>(q, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
+            const float u0 = a0[e], w = a1[e];
+            a0[e] = fmaf(u0, cs, w * sn);
+            a1[e] = fmaf(-u0, sn, w * cs);
+          }
+        } else if (p.rope == 2) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            float cs, sn;
+            rope_cos_sin<false>(q, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
+            float u0 = a0[2 * t], w = a0[2 * t + 1];
+            a0[2 * t] = fmaf(u0, cs, w * sn);
+            a0[2 * t + 1] = fmaf(-u0, sn, w * cs);
+            rope_cos_sin<false>(q, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs,
+                                sn);
+            u0 = a1[2 * t];
+            w = a1[2 * t + 1];
+            a1[2 * t] = fmaf(u0, cs, w * sn);
+            a1[2 * t + 1] = fmaf(-u0, sn, w * cs);
+          }
+        }
+        if (q < p.T) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            reinterpret_cast<uint4*>(dst + 32 * c)[v4] =
+                make_uint4(pack_bf16x2(a0[8 * v4], a0[8 * v4 + 1]),
+                           pack_bf16x2(a0[8 * v4 + 2], a0[8 * v4 + 3]),
+                           pack_bf16x2(a0[8 * v4 + 4], a0[8 * v4 + 5]),
+                           pack_bf16x2(a0[8 * v4 + 6], a0[8 * v4 + 7]));
+            reinterpret_cast<uint4*>(dst + 64 + 32 * c)[v4] =
+                make_uint4(pack_bf16x2(a1[8 * v4], a1[8 * v4 + 1]),
+                           pack_bf16x2(a1[8 * v4 + 2], a1[8 * v4 + 3]),
+                           pack_bf16x2(a1[8 * v4 + 4], a1[8 * v4 + 5]),
+                           pack_bf16x2(a1[8 * v4 + 6], a1[8 * v4 + 7]));
+          }
         }
       }
-      if (q < p.T) {
-        __nv_bfloat16* dst = p.dq + (rb + q) * D;
-#pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          reinterpret_cast<uint4*>(dst + 32 * c)[v4] =
-              make_uint4(pack_bf16x2(a0[8 * v4], a0[8 * v4 + 1]),
-                         pack_bf16x2(a0[8 * v4 + 2], a0[8 * v4 + 3]),
-                         pack_bf16x2(a0[8 * v4 + 4], a0[8 * v4 + 5]),
-                         pack_bf16x2(a0[8 * v4 + 6], a0[8 * v4 + 7]));
-          reinterpret_cast<uint4*>(dst + 64 + 32 * c)[v4] =
-              make_uint4(pack_bf16x2(a1[8 * v4], a1[8 * v4 + 1]),
-                         pack_bf16x2(a1[8 * v4 + 2], a1[8 * v4 + 3]),
-                         pack_bf16x2(a1[8 * v4 + 4], a1[8 * v4 + 5]),
-                         pack_bf16x2(a1[8 * v4 + 6], a1[8 * v4 + 7]));
-        }
-      }
+      // the accumulator may take the item after next
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   }
 
@@ -758,11 +853,13 @@ cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream) {
   p.dvec = a.dvec;
   p.dq = static_cast<__nv_bfloat16*>(a.dq);
   p.status = a.status;
+  p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.T = a.Tq;
   p.causal = a.causal;
   p.rope = a.rope;
+  p.n_items = a.B * a.Hq * ((a.Tq + BQ - 1) / BQ);
   p.scale = a.scale;
   p.sl2 = a.scale * kLog2e;
   p.theta = a.theta;
@@ -775,8 +872,9 @@ cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(bwd_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Q_SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.Hq, a.B, (a.Tq + BQ - 1) / BQ);
-  bwd_q_tc_kernel<<<grid, kThreads, Q_SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
+  const int sms = a.num_sms > 0 ? a.num_sms : 1;
+  const int grid = p.n_items < sms ? p.n_items : sms;
+  bwd_q_tc_kernel<<<grid, kThreadsQ, Q_SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
   return cudaGetLastError();
 }
 

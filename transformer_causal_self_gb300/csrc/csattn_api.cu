@@ -344,6 +344,7 @@ int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out
   int rc = device_info(&status, &num_sms);
   if (rc != CSATTN_OK) return rc;
   a.status = status;
+  a.num_sms = num_sms;
   if (d == 128 && tensor_map_encoder() == nullptr)
     return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -56,6 +56,7 @@ struct BwdArgs {
   void* dk;
   void* dv;
   int B, Hq, Hkv, Tq, Tk, q_off, d;
+  int num_sms;  // persistent dQ kernel grid
   int causal;
   int rope;  // 0 none, 1 split-half, 2 adjacent: dq, dk are rotated back by R^T
   float scale;
