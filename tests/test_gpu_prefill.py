@@ -91,6 +91,28 @@ def test_bf16_parity(B, Hq, Hkv, T, d, causal, base, layout):
     assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-2
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,T,d", [
+    (4, 64, 64, 300, 128),   # MHA, 3 query tiles: the longest units have no tile A
+    (4, 48, 16, 300, 128),   # group of 3: head pairs, then consecutive-tile units
+    (4, 64, 64, 300, 64),
+])
+def test_bf16_many_units_per_cta(B, Hq, Hkv, T, d):
+    """Enough units that every CTA runs several, among them the single-tile units of
+    an odd tile count ahead of two-tile ones; a sample of heads against the oracle."""
+    w = W.PrefillWorkload("many_units", B=B, Hq=Hq, Hkv=Hkv, T=T, d=d, dtype="bf16",
+                          rope_base=10000.0, scale=1.0 / math.sqrt(d), causal=True,
+                          seed=B + Hq + d)
+    q, k, v = W.make_prefill_inputs(w)
+    out = _run(q, k, v, causal=True, rope_base=w.rope_base, scale=w.scale).cpu()
+    rep = Hq // Hkv
+    for b, h in [(0, 0), (1, Hq - 1), (2, Hq // 2 + 1), (3, 7), (3, Hq - 2)]:
+        g = h // rep
+        ref = OA.attention(q[b:b + 1, h:h + 1], k[b:b + 1, g:g + 1], v[b:b + 1, g:g + 1],
+                           causal=True, rope_base=w.rope_base, scale=w.scale,
+                           operand_dtype="bf16")
+        assert_bf16_close(to_np(out[b:b + 1, h:h + 1]), ref, f"head ({b},{h})")
+
+
 def test_bf16_rotated_keys_match_oracle_rounding():
     """The rotated keys (left in the workspace) equal the oracle's rounded rotation."""
     w = W.WORKLOADS["llama_gqa_bf16"].with_(B=1, Hq=4, Hkv=2, T=1000)

@@ -446,7 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           return;
         }
-        if ((x ? un2.n[1] : un2.n[0]) == 0) continue;
+        // an absent tile (tile A of the last, single-tile pair) has nothing to rotate;
+        // this warpgroup still runs that unit (masked) and prepares the next one after it
+        if ((x ? un2.n[1] : un2.n[0]) == 0) return;
         uint32_t& cq = x ? cqb : cqa;
         if (fail || !warp_wait(&q_full[x], cq & 1, abort_flag, p.status, kWaitNs)) {
           fail = true;
