@@ -77,6 +77,25 @@ def test_bf16_chunks(d, hq, hkv, Tq, Tk, off, causal, base):
     assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-3
 
 
+@pytest.mark.parametrize("d,hq,hkv,Tq,Tk,off,causal", [
+    (128, 64, 64, 300, 1000, 700, True),    # MHA, odd query-tile count at an offset
+    (128, 48, 16, 300, 500, 0, False),      # group of 3, rectangular
+    (64, 64, 64, 300, 800, 500, True),
+])
+def test_bf16_chunks_many_units_per_cta(d, hq, hkv, Tq, Tk, off, causal):
+    """More units than SMs (several per CTA, single-tile units among them); a sample of
+    heads against the oracle."""
+    B = 4
+    q, k, v = _inputs(B, hq, hkv, Tq, Tk, d, "bf16", seed=d + hq + Tq)
+    out = _run(q, k, v, q_offset=off, causal=causal, rope_base=10000.0, scale=0.0).cpu()
+    rep = hq // hkv
+    for b, h in [(0, 0), (1, hq - 1), (2, hq // 2 + 1), (3, 5)]:
+        g = h // rep
+        ref = OA.attention(q[b:b + 1, h:h + 1], k[b:b + 1, g:g + 1], v[b:b + 1, g:g + 1],
+                           causal=causal, rope_base=10000.0, operand_dtype="bf16", q_offset=off)
+        assert_bf16_close(to_np(out[b:b + 1, h:h + 1]), ref, f"head ({b},{h})")
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_aligned_chunks_reproduce_full_prefill_bitwise(d):
     """Chunks at offsets that are multiples of the 128-row tile run the same tiles in

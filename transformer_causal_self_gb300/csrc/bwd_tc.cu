@@ -26,24 +26,30 @@
 namespace csattn {
 namespace {
 
-constexpr int D = 128;
 constexpr int BK = 128;  // keys per CTA
 constexpr int BQ = 128;  // queries per tile
 constexpr int kThreads = 384;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int NSQ = 2;  // Q / dO stages
-constexpr int TILE = BQ * D * 2;        // 32 KB
-constexpr int BLOCK = BQ * 128;         // one 64-channel column block of a tile
+constexpr int BLOCK = BQ * 128;         // one 64-channel column block of a 128-row tile
+constexpr int PTILE = BK * BQ * 2;      // the P^T tile, 32 KB
 constexpr int VEC = 2 * BQ * 4;         // lse and D of one tile, fp32
-constexpr int SMEM_DATA = 2 * TILE + NSQ * 2 * TILE + TILE + NSQ * VEC;  // + P^T tile
-constexpr int SMEM_BYTES = SMEM_DATA + 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, 0, 0);  // both K-major
-constexpr uint32_t IDESC_TS = idesc_bf16_f32(128, 128, 0, 1);  // B (dO / Qr) MN-major
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, 0, 1);  // A = P^T K-major, B = dO MN-major
+constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, 0, 0);  // both K-major (S^T, dP^T, S, dP)
+
+// Head-size dependent sizes (d = 64 or 128): a Q / dO / K / V tile is d/64 column
+// blocks of 128 rows; dV, dK and dQ are N = d products with B read MN-major.
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head size 64 or 128");
+  static constexpr int TILE = BQ * D * 2;
+  static constexpr int SMEM_DATA = 2 * TILE + NSQ * 2 * TILE + PTILE + NSQ * VEC;
+  static constexpr int SMEM_BYTES = SMEM_DATA + 256;
+  static constexpr uint32_t IDESC_N = idesc_bf16_f32(128, D, 0, 1);  // A K-major, B MN-major
+};
 
 struct KvParams {
   const float* lse;   // [B, Hq, T], natural log
@@ -67,19 +73,22 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
   return static_cast<uint32_t>(kk < 4 ? 8 * kk : 64 + 8 * (kk - 4));
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_tc_kernel(const __grid_constant__ KvParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_do) {
+  using C = BwdCfg<D>;
+  constexpr int TILE = C::TILE;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sK = smem;
   uint8_t* sV = smem + TILE;
   uint8_t* sQ = smem + 2 * TILE;                 // [NSQ] tiles
   uint8_t* sO = smem + (2 + NSQ) * TILE;         // [NSQ] dO tiles
   uint8_t* sP = smem + (2 + 2 * NSQ) * TILE;     // P^T: rows = keys, queries contiguous
-  float* sVec = reinterpret_cast<float*>(smem + (3 + 2 * NSQ) * TILE);  // [NSQ][lse 128 | D 128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_DATA);
+  float* sVec = reinterpret_cast<float*>(smem + (2 + 2 * NSQ) * TILE + PTILE);  // [NSQ][lse | D]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_DATA);
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;   // [NSQ]: Qr and dO tiles (TMA bytes)
   uint64_t* q_empty = bars + 3;  // [NSQ]
@@ -233,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
           umma_ss(tmem + 256u, smem_desc_sw128(p_s + off, 16, 1024),
-                  smem_desc_sw128(o_s + 2048u * kk, BLOCK, 1024), IDESC_PV,
+                  smem_desc_sw128(o_s + 2048u * kk, BLOCK, 1024), C::IDESC_N,
                   (it > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(dv_done);
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
           umma_ts(tmem + 384u, tmem + 128u + packed_col(kk),
-                  smem_desc_sw128(q_s + 2048u * kk, BLOCK, 1024), IDESC_TS,
+                  smem_desc_sw128(q_s + 2048u * kk, BLOCK, 1024), C::IDESC_N,
                   (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&q_empty[it % NSQ]);
         if (next) issue_dpt(it + 1);
@@ -341,22 +350,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     }
-    // epilogue: warps 0-3 write dV, warps 4-7 dK = R^T (scale dK); channels in pairs of
-    // 32-column chunks (c, c + 2) so that split-half RoPE pairs (i, i + 64) meet
+    // epilogue: warps 0-3 write dV, warps 4-7 dK = R^T (scale dK); channels in 32-column
+    // chunks 32c and d/2 + 32c so that split-half RoPE pairs (i, i + d/2) meet
     if (ok && (n_it == 0 || warp_wait(acc_full, 0, abort_flag, p.status))) {
       tc_fence_after();
       const uint32_t tacc = tmem + lane_off + (x ? 384u : 256u);
       __nv_bfloat16* dst =
           (x ? p.dk : p.dv) + (static_cast<size_t>(b * p.Hkv + g) * p.T + (key < p.T ? key : 0)) * D;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         float a0[32], a1[32];
         {
           uint32_t r[32];
           tmem_ld32_sync(tacc + 32u * c, r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) a0[e] = n_it > 0 ? __uint_as_float(r[e]) : 0.f;
-          tmem_ld32_sync(tacc + 64u + 32u * c, r);
+          tmem_ld32_sync(tacc + static_cast<uint32_t>(D / 2) + 32u * c, r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) a1[e] = n_it > 0 ? __uint_as_float(r[e]) : 0.f;
         }
@@ -366,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             a0[e] *= p.scale;
             a1[e] *= p.scale;
           }
-          if (p.rope == 1) {  // pair (i, i + 64), i = 32c + e
+          if (p.rope == 1) {  // pair (i, i + d/2), i = 32c + e
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               float cs, sn;
@@ -383,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float u = a0[2 * t], w = a0[2 * t + 1];
               a0[2 * t] = fmaf(u, cs, w * sn);
               a0[2 * t + 1] = fmaf(-u, sn, w * cs);
-              rope_cos_sin<false>(key, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs,
-                                 sn);
+              rope_cos_sin<false>(key, p.theta.hi[D / 4 + 16 * c + t],
+                                  p.theta.lo[D / 4 + 16 * c + t], cs, sn);
               u = a1[2 * t];
               w = a1[2 * t + 1];
               a1[2 * t] = fmaf(u, cs, w * sn);
@@ -400,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            pack_bf16x2(a0[8 * v4 + 2], a0[8 * v4 + 3]),
                            pack_bf16x2(a0[8 * v4 + 4], a0[8 * v4 + 5]),
                            pack_bf16x2(a0[8 * v4 + 6], a0[8 * v4 + 7]));
-            reinterpret_cast<uint4*>(dst + 64 + 32 * c)[v4] =
+            reinterpret_cast<uint4*>(dst + D / 2 + 32 * c)[v4] =
                 make_uint4(pack_bf16x2(a1[8 * v4], a1[8 * v4 + 1]),
                            pack_bf16x2(a1[8 * v4 + 2], a1[8 * v4 + 3]),
                            pack_bf16x2(a1[8 * v4 + 4], a1[8 * v4 + 5]),
@@ -433,8 +442,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // runs across items; S(g+1) is issued as soon as the softmax warps have read S(g)
 // (g counts key tiles over all items of the CTA), dP(g+1) follows dQ(g).
 constexpr int NSKV = 2;
-constexpr int Q_SMEM_DATA = 2 * TILE + NSKV * 2 * TILE;
-constexpr int Q_SMEM_BYTES = Q_SMEM_DATA + 256;
 constexpr int kThreadsQ = 512;
 constexpr int kWarpEpiQ = 12;       // warps 12-15: dQ epilogue (TMEM lane quadrants 0-3)
 constexpr int kRegsSoftmaxQ = 152;  // 2*128*152 + 128*96 + 128*112 = 65536 = 512 * 128
@@ -483,11 +490,14 @@ __device__ __forceinline__ void q_regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreadsQ, 1)
     bwd_q_tc_kernel(const __grid_constant__ QParams p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do) {
+  constexpr int TILE = BwdCfg<D>::TILE;
+  constexpr int Q_SMEM_DATA = 2 * TILE + NSKV * 2 * TILE;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sQ = smem;
   uint8_t* sO = smem + TILE;
@@ -642,7 +652,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             umma_ts(t_acc, tmem + 128u + packed_col(kk), smem_desc_sw128(k_s + 2048u * kk, BLOCK, 1024),
-                    IDESC_TS, (j > 0 || kk > 0) ? 1u : 0u);
+                    BwdCfg<D>::IDESC_N, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&kv_empty[g % NSKV]);
           if (next) {
             issue_dp(g + 1);
@@ -729,8 +739,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ epilogue (warps 12-15)
-    // thread = query row; dQ = R^T (scale dQ) with split-half pairs (i, i + 64) taken
-    // as column chunks (32c + e, 64 + 32c + e)
+    // thread = query row; dQ = R^T (scale dQ) with split-half pairs (i, i + d/2) taken
+    // as column chunks (32c + e, d/2 + 32c + e)
     q_regs_dec<kRegsEpiQ>();
     const int row = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -745,14 +755,14 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       const uint32_t t_acc = tmem + lane_off + 256u + 128u * static_cast<uint32_t>(ab);
       __nv_bfloat16* dst = p.dq + (static_cast<size_t>(it.b * p.Hq + it.h) * p.T + q) * D;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         float a0[32], a1[32];
         {
           uint32_t r[32];
           tmem_ld32_sync(t_acc + 32u * c, r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) a0[e] = __uint_as_float(r[e]) * p.scale;
-          tmem_ld32_sync(t_acc + 64u + 32u * c, r);
+          tmem_ld32_sync(t_acc + static_cast<uint32_t>(D / 2) + 32u * c, r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) a1[e] = __uint_as_float(r[e]) * p.scale;
         }
@@ -773,8 +783,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             float u0 = a0[2 * t], w = a0[2 * t + 1];
             a0[2 * t] = fmaf(u0, cs, w * sn);
             a0[2 * t + 1] = fmaf(-u0, sn, w * cs);
-            rope_cos_sin<false>(q, p.theta.hi[32 + 16 * c + t], p.theta.lo[32 + 16 * c + t], cs,
-                                sn);
+            rope_cos_sin<false>(q, p.theta.hi[D / 4 + 16 * c + t], p.theta.lo[D / 4 + 16 * c + t],
+                                cs, sn);
             u0 = a1[2 * t];
             w = a1[2 * t + 1];
             a1[2 * t] = fmaf(u0, cs, w * sn);
@@ -789,7 +799,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                            pack_bf16x2(a0[8 * v4 + 2], a0[8 * v4 + 3]),
                            pack_bf16x2(a0[8 * v4 + 4], a0[8 * v4 + 5]),
                            pack_bf16x2(a0[8 * v4 + 6], a0[8 * v4 + 7]));
-            reinterpret_cast<uint4*>(dst + 64 + 32 * c)[v4] =
+            reinterpret_cast<uint4*>(dst + D / 2 + 32 * c)[v4] =
                 make_uint4(pack_bf16x2(a1[8 * v4], a1[8 * v4 + 1]),
                            pack_bf16x2(a1[8 * v4 + 2], a1[8 * v4 + 3]),
                            pack_bf16x2(a1[8 * v4 + 4], a1[8 * v4 + 5]),
@@ -814,7 +824,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream) {
+template <int D>
+cudaError_t launch_kv_d(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
   KvParams p{};
   p.lse = a.lse;
   p.dvec = a.dvec;
@@ -835,19 +847,27 @@ cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream) {
       !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BK) ||
       !make_tmap_bf16_3d(&tdo, a.dout, D, a.Tq, a.B * a.Hq, BQ))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(a.Hkv, a.B, (a.Tk + BK - 1) / BK);
-  bwd_kv_tc_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
+  bwd_kv_tc_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
   return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return launch_kv_d<64>(a, stream);
+  if (a.d == 128) return launch_kv_d<128>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace csattn
 
 namespace csattn {
 
-cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream) {
+template <int D>
+cudaError_t launch_q_d(const BwdArgs& a, cudaStream_t stream) {
+  constexpr int smem_bytes = (2 + 2 * NSKV) * BwdCfg<D>::TILE + 256;
   QParams p{};
   p.lse = a.lse;
   p.dvec = a.dvec;
@@ -869,13 +889,19 @@ cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream) {
       !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BK) ||
       !make_tmap_bf16_3d(&tdo, a.dout, D, a.Tq, a.B * a.Hq, BQ))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Q_SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(bwd_q_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
   const int grid = p.n_items < sms ? p.n_items : sms;
-  bwd_q_tc_kernel<<<grid, kThreadsQ, Q_SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
+  bwd_q_tc_kernel<D><<<grid, kThreadsQ, smem_bytes, stream>>>(p, tq, tk, tv, tdo);
   return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return launch_q_d<64>(a, stream);
+  if (a.d == 128) return launch_q_d<128>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace csattn
