@@ -94,6 +94,33 @@ def test_bwd_llama_workload_one_group():
     _close(to_np(dv[b:b + 1, grp:grp + 1]), rv, "dv group")
 
 
+@pytest.mark.parametrize("B,hq,hkv,T,d,causal", [
+    (4, 48, 16, 512, 64, False),    # 768 dQ work items: several per persistent CTA
+    (4, 64, 64, 300, 128, True),    # MHA, odd query-tile count
+])
+def test_bwd_many_items_per_cta(B, hq, hkv, T, d, causal):
+    """More work items than SMs, so the persistent dQ kernel reuses both TMEM
+    accumulators; two KV groups checked against the oracle."""
+    w = W.PrefillWorkload("bwd_many", B=B, Hq=hq, Hkv=hkv, T=T, d=d, dtype="bf16",
+                          rope_base=10000.0, scale=1.0 / math.sqrt(d), causal=causal,
+                          seed=B + hq + T)
+    q, k, v = W.make_prefill_inputs(w)
+    g = torch.Generator()
+    g.manual_seed(T + 1)
+    do = torch.randn(B, hq, T, d, generator=g).to(torch.bfloat16)
+    dq, dk, dv = _run(q, k, v, do, causal, w.rope_base, "split_half", w.scale)
+    rep = hq // hkv
+    for b, grp in [(0, hkv - 1), (3, hkv // 2)]:
+        hs = slice(grp * rep, (grp + 1) * rep)
+        rq, rk, rv = OA.attention_backward(q[b:b + 1, hs], k[b:b + 1, grp:grp + 1],
+                                           v[b:b + 1, grp:grp + 1], do[b:b + 1, hs],
+                                           causal=causal, rope_base=w.rope_base, scale=w.scale,
+                                           operand_dtype="bf16")
+        _close(to_np(dq[b:b + 1, hs]), rq, f"dq ({b},{grp})")
+        _close(to_np(dk[b:b + 1, grp:grp + 1]), rk, f"dk ({b},{grp})")
+        _close(to_np(dv[b:b + 1, grp:grp + 1]), rv, f"dv ({b},{grp})")
+
+
 def test_bwd_gqa_equals_summed_mha():
     """dk, dv of a GQA group equal the sums over its heads of the MHA gradients on repeated
     K/V (the group sum the kernel does in registers)."""

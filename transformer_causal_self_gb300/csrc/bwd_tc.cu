@@ -847,8 +847,8 @@ cudaError_t launch_kv_d(const BwdArgs& a, cudaStream_t stream) {
       !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BK) ||
       !make_tmap_bf16_3d(&tdo, a.dout, D, a.Tq, a.B * a.Hq, BQ))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static SmemLimitOnce smem_limit;
+  cudaError_t e = smem_limit.set(bwd_kv_tc_kernel<D>, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(a.Hkv, a.B, (a.Tk + BK - 1) / BK);
   bwd_kv_tc_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
@@ -889,8 +889,8 @@ cudaError_t launch_q_d(const BwdArgs& a, cudaStream_t stream) {
       !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BK) ||
       !make_tmap_bf16_3d(&tdo, a.dout, D, a.Tq, a.B * a.Hq, BQ))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_q_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  static SmemLimitOnce smem_limit;
+  cudaError_t e = smem_limit.set(bwd_q_tc_kernel<D>, smem_bytes);
   if (e != cudaSuccess) return e;
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
   const int grid = p.n_items < sms ? p.n_items : sms;

@@ -406,8 +406,8 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   if (!make_tmap_bf16_3d(&tk, a.k_cache, D, rows, planes, KT) ||
       !make_tmap_bf16_3d(&tv, a.v_cache, D, rows, planes, KT))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static SmemLimitOnce smem_limit;
+  cudaError_t e = smem_limit.set(decode_bf16_kernel<D>, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_splits, a.Hkv, a.B);
   decode_bf16_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tk, tv);

@@ -420,8 +420,8 @@ cudaError_t launch_d64(const FwdArgs& a, const void* k_eff, cudaStream_t stream)
       !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BN))
     return cudaErrorInvalidValue;
 
-  cudaError_t e = cudaFuncSetAttribute(fwd_sm103a_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static SmemLimitOnce smem_limit;
+  cudaError_t e = smem_limit.set(fwd_sm103a_kernel<D>, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = p.nUnits < a.num_sms ? p.nUnits : a.num_sms;
   fwd_sm103a_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv);

@@ -671,8 +671,8 @@ cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStre
       !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BN) ||
       !make_tmap_bf16_3d(&to, a.out, D, a.Tq, a.B * a.Hq, BM))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
+  static SmemLimitOnce smem_limit;
+  cudaError_t e = smem_limit.set(fwd_d128_kernel, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = p.nUnits < a.num_sms ? p.nUnits : a.num_sms;
   fwd_d128_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tq, tk, tv, to);

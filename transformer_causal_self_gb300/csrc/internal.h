@@ -3,6 +3,7 @@
 // checked every argument.  They return a cudaError_t from the launch.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -115,6 +116,23 @@ void* tensor_map_encoder();
 
 // 3-D bf16 tensor map over rows of `d` elements: dims {d, rows, planes},
 // box {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
+// Raises a kernel's dynamic shared-memory limit once per device (the attribute
+// lasts for the process), so repeated launches skip the driver call.
+struct SmemLimitOnce {
+  std::atomic<uint64_t> done{0};
+  template <typename Kernel>
+  cudaError_t set(Kernel* kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
+
 bool make_tmap_bf16_3d(void* tmap_out, const void* base, int d, int rows, int planes,
                        int box_rows);
 
