@@ -133,6 +133,10 @@ WORKLOADS = {
     "llama_chunk_bf16": ChunkWorkload("llama_chunk_bf16", B=4, Hq=32, Hkv=8, Tq=1024, Tk=4096,
                                       q_offset=3072, d=128, dtype="bf16", rope_base=10000.0,
                                       scale=1.0 / math.sqrt(128)),
+    # cross / rectangular attention: 1024 queries against 4096 keys, no mask, no RoPE
+    "llama_cross_bf16": ChunkWorkload("llama_cross_bf16", B=4, Hq=32, Hkv=8, Tq=1024, Tk=4096,
+                                      q_offset=0, d=128, dtype="bf16", rope_base=0.0,
+                                      scale=1.0 / math.sqrt(128), causal=False),
     "decode_bf16": DecodeWorkload("decode_bf16", B=64, Hq=32, Hkv=8, d=128, Lmax=8192,
                                   Lmin=512, dtype="bf16", scale=1.0 / math.sqrt(128)),
 }

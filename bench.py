@@ -425,6 +425,8 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
 
     chunked_prefill: llama_chunk_bf16 (1024 queries after a 3072-token cache) through
     csattn_attn_fwd_ext, L2 flushed before each launch (its inputs are ~L2-sized).
+    rectangular: llama_cross_bf16 (1024 queries against 4096 keys, no mask), the same
+    entry point, L2 flushed before each launch.
     decode_step: the decode_bf16 batch with the new token appended at row L_b - 1 and
     rotated inside the call (csattn_attn_decode_step), attending over the same L_b rows
     as the headline decode; its cache is > 2 GB, so no flush.
@@ -461,7 +463,35 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
                      "kernel": "fwd_d128_kernel"}}
-    del q, k, v, k_rot, o, flush
+    del q, k, v, k_rot, o
+
+    # rectangular, unmasked (cross-attention shaped): 1024 queries x 4096 keys per head
+    wx = W.WORKLOADS["llama_cross_bf16"]
+    q, k, v = (t.to(dev) for t in W.make_chunk_inputs(wx))
+    o = torch.empty_like(q)
+    ts = []
+    for i in range(3 + reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csattn.attn_fwd_ext(q, k, v, o, q_offset=0, causal=False, rope_base=0.0, scale=wx.scale,
+                            stream=stream)
+        e1.record(stream)
+        if i >= 3:
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    csattn.check_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    tf = wx.flops() / (ms * 1e-3) / 1e12
+    out["rectangular"] = {
+        "workload": "llama_cross_bf16 (B=4, Hq=32, Hkv=8, Tq=1024, Tk=4096, d=128, no mask, "
+                    "no RoPE)",
+        "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+        "flops": wx.flops(), "l2": "flushed before each launch",
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
+                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                     "kernel": "fwd_d128_kernel"}}
+    del q, k, v, o, flush
 
     g = torch.Generator()
     g.manual_seed(7)

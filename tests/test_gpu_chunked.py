@@ -149,3 +149,18 @@ def test_chunk_workload_sampled_rows():
         ref = OA.attention_rows(q, k, v, b, h, rows, causal=True, rope_base=w.rope_base,
                                 scale=w.scale, operand_dtype="bf16", q_offset=w.q_offset)
         assert_bf16_close(oc[b, h, rows].double().numpy(), ref, f"chunk workload b={b} h={h}")
+
+
+def test_cross_workload_sampled_rows():
+    """The rectangular (unmasked, cross-attention shaped) bench workload, sampled rows."""
+    w = W.WORKLOADS["llama_cross_bf16"]
+    q, k, v = W.make_chunk_inputs(w)
+    out = csattn.attn_fwd_ext(q.to(dev()), k.to(dev()), v.to(dev()), q_offset=0, causal=False,
+                              rope_base=0.0, scale=w.scale)
+    csattn.check_status()
+    oc = out.cpu()
+    for b, h in ((0, 3), (2, 17), (3, 30)):
+        rows = W.sample_query_rows(w.Tq, 96, seed=b * 100 + h + 1)
+        ref = OA.attention_rows(q, k, v, b, h, rows, causal=False, rope_base=0.0, scale=w.scale,
+                                operand_dtype="bf16")
+        assert_bf16_close(oc[b, h, rows].double().numpy(), ref, f"cross workload b={b} h={h}")
