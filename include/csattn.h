@@ -112,7 +112,11 @@ size_t csattn_fwd_ext_workspace_size(int B, int Hq, int Hkv, int Tq, int Tk, int
  * (cross-)attention ("The Transformer architecture", "Hands-on": the query at
  * position p sees cached keys 0..p; "Transformer Math and Implementation Deep
  * Dive", "Attention Equation": Tq and Tk need not match without a mask).
- *   q    [B, Hq,  Tq, d];  k, v [B, Hkv, Tk, d];  out [B, Hq, Tq, d]
+ *   q    [B, Hq,  Tq, d];  k [B, Hkv, Tk, d];  v [B, Hkv, Tk, dv];  out [B, Hq, Tq, dv]
+ *   dv           head size of v and out ("Scaled dot-product attention": the
+ *                values need not have the keys' width); <= 0 means dv = d.
+ *                bf16: d, dv in {64, 128}; fp32: d, dv in {16, 32, 64, 128}.
+ *                The default scale stays 1/sqrt(d) and RoPE acts on q and k.
  *   q_offset     position of query row 0: row i sits at q_offset + i; keys sit
  *                at 0..Tk-1.  With causal = 1, row i sees keys j <= q_offset + i
  *                (a chunked prefill passes Tk = q_offset + Tq: the cached prefix
@@ -128,8 +132,8 @@ size_t csattn_fwd_ext_workspace_size(int B, int Hq, int Hkv, int Tq, int Tk, int
  * (CSATTN_ERR_UNSUPPORTED otherwise).
  */
 int csattn_attn_fwd_ext(const void* q, const void* k, const void* v, void* out, int B, int Hq,
-                        int Hkv, int Tq, int Tk, int q_offset, int d, int dtype, int causal,
-                        float rope_base, int rope_layout, float scale, float* lse,
+                        int Hkv, int Tq, int Tk, int q_offset, int d, int dv, int dtype,
+                        int causal, float rope_base, int rope_layout, float scale, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*

@@ -114,14 +114,18 @@ def test_fwd_rejects_invalid_arguments(lib, kw, status):
     (dict(dtype=1, rope_base=10000.0, Tk=50000), -2),
     (dict(dtype=1, rope_base=10000.0, ws=None, ws_bytes=0), -5),
     (dict(dtype=1, rope_base=10000.0, Tk=512, ws=FAKE, ws_bytes=1 * 2 * 256 * 64 * 2), -5),
+    (dict(dv=96), -2),
+    (dict(dtype=1, dv=32), -2),
+    (dict(dtype=1, d=32, dv=64), -2),
 ])
 def test_fwd_ext_rejects_invalid_arguments(lib, kw, status):
     a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, Hq=4, Hkv=2, Tq=64, Tk=256, q_offset=192,
-             d=64, dtype=0, causal=1, rope_base=0.0, rope_layout=0, scale=0.0, lse=None, ws=None,
-             ws_bytes=0)
+             d=64, dv=0, dtype=0, causal=1, rope_base=0.0, rope_layout=0, scale=0.0, lse=None,
+             ws=None, ws_bytes=0)
     a.update(kw)
     rc = lib.csattn_attn_fwd_ext(a["q"], a["k"], a["v"], a["out"], a["B"], a["Hq"], a["Hkv"],
-                                 a["Tq"], a["Tk"], a["q_offset"], a["d"], a["dtype"], a["causal"],
+                                 a["Tq"], a["Tk"], a["q_offset"], a["d"], a["dv"], a["dtype"],
+                                 a["causal"],
                                  a["rope_base"], a["rope_layout"], a["scale"], a["lse"], a["ws"],
                                  a["ws_bytes"], None)
     assert rc == status, lib.csattn_last_error()

@@ -164,3 +164,36 @@ def test_cross_workload_sampled_rows():
         ref = OA.attention_rows(q, k, v, b, h, rows, causal=False, rope_base=0.0, scale=w.scale,
                                 operand_dtype="bf16")
         assert_bf16_close(oc[b, h, rows].double().numpy(), ref, f"cross workload b={b} h={h}")
+
+
+@pytest.mark.parametrize("dtype,d,dv,hq,hkv,Tq,Tk,off,causal,base", [
+    ("bf16", 64, 128, 8, 2, 200, 700, 500, True, 10000.0),   # narrow q, k; wide v
+    ("bf16", 128, 64, 8, 2, 200, 700, 500, True, 10000.0),   # wide q, k; narrow v
+    ("bf16", 64, 128, 6, 6, 300, 129, 0, False, 0.0),        # rectangular
+    ("bf16", 128, 64, 4, 1, 129, 1000, 10, False, 10000.0),
+    ("bf16", 64, 128, 64, 64, 300, 300, 0, True, 10000.0),    # many units per CTA
+    ("f32", 16, 32, 4, 1, 16, 64, 48, True, 10000.0),
+    ("f32", 128, 16, 2, 2, 33, 70, 37, True, 10000.0),
+    ("f32", 32, 128, 6, 2, 20, 45, 0, False, 0.0),
+])
+def test_value_width_differs_from_key_width(dtype, d, dv, hq, hkv, Tq, Tk, off, causal, base):
+    """v and out with dv channels, q and k with d ("Scaled dot-product attention": the
+    weights come from q and k; v sets the output width)."""
+    B = 2
+    g = torch.Generator()
+    g.manual_seed(d + 3 * dv + Tq)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    q = torch.randn(B, hq, Tq, d, generator=g).to(dt)
+    k = torch.randn(B, hkv, Tk, d, generator=g).to(dt)
+    v = torch.randn(B, hkv, Tk, dv, generator=g).to(dt)
+    lse = torch.empty(B, hq, Tq, dtype=torch.float32, device=dev())
+    out = _run(q, k, v, q_offset=off, causal=causal, rope_base=base, scale=0.0, lse=lse)
+    assert out.shape == (B, hq, Tq, dv)
+    od = "bf16" if dtype == "bf16" else "f32"
+    ref = OA.attention(q, k, v, causal=causal, rope_base=base, operand_dtype=od, q_offset=off)
+    if dtype == "bf16":
+        assert_bf16_close(to_np(out), ref, f"d={d} dv={dv}")
+    else:
+        assert_f32_close(to_np(out), ref, f"d={d} dv={dv}")
+    ref_lse = OA.attention_lse(q, k, causal=causal, rope_base=base, operand_dtype=od, q_offset=off)
+    assert np.max(np.abs(to_np(lse) - ref_lse)) < (2e-3 if dtype == "bf16" else 1e-4)

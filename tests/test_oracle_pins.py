@@ -187,6 +187,26 @@ def pin_naive_agreement(o):
             assert np.max(np.abs(a - b)) < 1e-12, (i, rnd, np.max(np.abs(a - b)))
 
 
+def pin_value_width(o):
+    """Values of another width than the keys ("Scaled dot-product attention": the weights
+    come from q and k alone): agreement with the scalar loops for d_v != d_k, default
+    scale 1/sqrt(d_k), and a single visible key returns its value row exactly."""
+    for i, (dk, dv, causal, base) in enumerate([(4, 16, True, 10000.0), (16, 4, False, 0.0),
+                                               (8, 2, True, 500000.0)]):
+        q = _rand((1, 4, 7, dk), 300 + i, 2.0)
+        k = _rand((1, 2, 9, dk), 310 + i, 2.0)
+        v = _rand((1, 2, 9, dv), 320 + i)
+        a = o.attention(q, k, v, causal=causal, rope_base=base, q_offset=2)
+        b = np.array(ON.naive_attention(_to_list(q), _to_list(k), _to_list(v), causal, base, None,
+                                        "split_half", q_offset=2))
+        assert a.shape == (1, 4, 7, dv)
+        assert np.max(np.abs(a - b)) < 1e-12, (i, np.max(np.abs(a - b)))
+    q = _rand((1, 2, 1, 8), 330)
+    k = _rand((1, 2, 1, 8), 331)
+    v = _rand((1, 2, 1, 24), 332)
+    assert np.array_equal(o.attention(q, k, v, causal=False), v)
+
+
 def pin_degenerate_cases(o):
     q = _rand((1, 2, 1, 8), 90)
     k = _rand((1, 2, 1, 8), 91)
@@ -466,7 +486,7 @@ ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exa
             pin_chunk_equals_full_rows, pin_chunk_naive, pin_decode_is_chunk_of_one,
             pin_decode_step_appends_then_attends, pin_backward_finite_differences,
             pin_backward_autograd, pin_rope_transpose_inverts,
-            pin_decode_paged_equals_contiguous]
+            pin_decode_paged_equals_contiguous, pin_value_width]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -512,7 +532,8 @@ class _Mutant:
             v = np.asarray(v, np.float64)
             B, Hq, T, d = q.shape
             Tk = k.shape[2]
-            sc = 1 / math.sqrt(d) if (scale is None or scale <= 0) else scale
+            dsc = v.shape[-1] if "scale_from_v" in repl else d
+            sc = 1 / math.sqrt(dsc) if (scale is None or scale <= 0) else scale
             if rope_base > 0:
                 q = me.round_to(me.rope_rotate(q, q_offset + np.arange(T), rope_base, rope_layout),
                                 operand_dtype)
@@ -761,3 +782,8 @@ def test_planted_paged_offset_swapped():
                 vc[b, :, t] = vp[page, :, off]
         return OA.decode(q, kc, vc, lens, scale=scale)
     assert _fails(_Mutant(decode_paged=bad), [pin_decode_paged_equals_contiguous])
+
+
+def test_planted_scale_from_value_width():
+    """The default scale taken from v's width instead of the keys' fails a pin."""
+    assert _fails(_Mutant(scale_from_v=True), [pin_value_width])

@@ -37,7 +37,7 @@ _SIGNATURES = {
     "csattn_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _c_float,
                                                                         _vp, _vp, _c_size, _vp]),
     "csattn_fwd_ext_workspace_size": (_c_size, [_c_int] * 7 + [_c_float]),
-    "csattn_attn_fwd_ext": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 9 + [_c_float, _c_int,
+    "csattn_attn_fwd_ext": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 10 + [_c_float, _c_int,
                                                                             _c_float, _vp, _vp,
                                                                             _c_size, _vp]),
     "csattn_bwd_workspace_size": (_c_size, [_c_int] * 6 + [_c_float]),
@@ -198,15 +198,17 @@ def attn_fwd_ext(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                  k_prerotated: bool = False, stream=None) -> torch.Tensor:
     """Chunked / rectangular prefill (C: csattn_attn_fwd_ext).
 
-    q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d].  Query row i sits at position q_offset + i;
-    with causal it sees keys j <= q_offset + i.  RoPE rotates q at q_offset + i
-    and k at 0..Tk-1 (unless k_prerotated).  lse, if given, is fp32 [B,Hq,Tq].
+    q [B,Hq,Tq,d], k [B,Hkv,Tk,d], v [B,Hkv,Tk,dv]; out [B,Hq,Tq,dv].  Query row i
+    sits at position q_offset + i; with causal it sees keys j <= q_offset + i.  RoPE
+    rotates q at q_offset + i and k at 0..Tk-1 (unless k_prerotated).  lse, if given,
+    is fp32 [B,Hq,Tq].
     """
     _need_cuda(q, k, v)
     B, Hq, Tq, d = q.shape
     Hkv, Tk = k.shape[1], k.shape[2]
+    dv = v.shape[3]
     if out is None:
-        out = torch.empty_like(q)
+        out = q.new_empty((B, Hq, Tq, dv))
     _need_cuda(out)
     if lse is not None:
         _need_cuda(lse)
@@ -217,7 +219,7 @@ def attn_fwd_ext(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     lib = load_library()
     _check(lib.csattn_attn_fwd_ext(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq,
-                                   Hkv, Tq, Tk, int(q_offset), d, _dtype_code(q),
+                                   Hkv, Tq, Tk, int(q_offset), d, dv, _dtype_code(q),
                                    int(bool(causal)), float(rope_base),
                                    _ROPE_LAYOUT[rope_layout] | (K_PREROTATED if k_prerotated else 0),
                                    float(scale), lse.data_ptr() if lse is not None else None,

@@ -160,9 +160,9 @@ namespace {
 
 // Shared by csattn_attn_fwd (Tq = Tk = T, q_offset = 0) and csattn_attn_fwd_ext.
 int attn_fwd_impl(const char* fn, const void* q, const void* k, const void* v, void* out, int B,
-                  int Hq, int Hkv, int Tq, int Tk, int q_offset, int d, int dtype, int causal,
-                  float rope_base, int rope_layout, float scale, float* lse, void* workspace,
-                  size_t workspace_bytes, void* stream) {
+                  int Hq, int Hkv, int Tq, int Tk, int q_offset, int d, int dv, int dtype,
+                  int causal, float rope_base, int rope_layout, float scale, float* lse,
+                  void* workspace, size_t workspace_bytes, void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: q, k, v and out must be non-null", fn);
   if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1)
@@ -183,8 +183,11 @@ int attn_fwd_impl(const char* fn, const void* q, const void* k, const void* v, v
     return fail(CSATTN_ERR_INVALID_ARG, "%s: rope_base and scale must be finite", fn);
   if (d != 16 && d != 32 && d != 64 && d != 128)
     return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d not in {16,32,64,128}", fn, d);
-  if (dtype == CSATTN_BF16 && d != 64 && d != 128)
-    return fail(CSATTN_ERR_UNSUPPORTED, "%s: bf16 supports d in {64,128}, got %d", fn, d);
+  if (dv != 16 && dv != 32 && dv != 64 && dv != 128)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: dv=%d not in {16,32,64,128}", fn, dv);
+  if (dtype == CSATTN_BF16 && ((d != 64 && d != 128) || (dv != 64 && dv != 128)))
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: bf16 supports d, dv in {64,128}, got %d, %d", fn, d,
+                dv);
   if (Tq >= (1 << 24) || Tk >= (1 << 24) || q_offset >= (1 << 24))
     return fail(CSATTN_ERR_UNSUPPORTED, "%s: Tq=%d, Tk=%d and q_offset=%d must be < 2^24", fn, Tq,
                 Tk, q_offset);
@@ -218,6 +221,7 @@ int attn_fwd_impl(const char* fn, const void* q, const void* k, const void* v, v
   a.Tk = Tk;
   a.q_off = q_offset;
   a.d = d;
+  a.dv = dv;
   a.causal = causal;
   a.rope = rope_base > 0.f ? (rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2) : 0;
   a.rope_k = (a.rope != 0 && !k_prerotated) ? 1 : 0;
@@ -254,17 +258,17 @@ int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int 
                     int Hkv, int T, int d, int dtype, int causal, float rope_base,
                     int rope_layout, float scale, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  return attn_fwd_impl("attn_fwd", q, k, v, out, B, Hq, Hkv, T, T, 0, d, dtype, causal, rope_base,
-                       rope_layout, scale, lse, workspace, workspace_bytes, stream);
+  return attn_fwd_impl("attn_fwd", q, k, v, out, B, Hq, Hkv, T, T, 0, d, d, dtype, causal,
+                       rope_base, rope_layout, scale, lse, workspace, workspace_bytes, stream);
 }
 
 int csattn_attn_fwd_ext(const void* q, const void* k, const void* v, void* out, int B, int Hq,
-                        int Hkv, int Tq, int Tk, int q_offset, int d, int dtype, int causal,
-                        float rope_base, int rope_layout, float scale, float* lse,
+                        int Hkv, int Tq, int Tk, int q_offset, int d, int dv, int dtype,
+                        int causal, float rope_base, int rope_layout, float scale, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream) {
-  return attn_fwd_impl("attn_fwd_ext", q, k, v, out, B, Hq, Hkv, Tq, Tk, q_offset, d, dtype,
-                       causal, rope_base, rope_layout, scale, lse, workspace, workspace_bytes,
-                       stream);
+  return attn_fwd_impl("attn_fwd_ext", q, k, v, out, B, Hq, Hkv, Tq, Tk, q_offset, d,
+                       dv > 0 ? dv : d, dtype, causal, rope_base, rope_layout, scale, lse,
+                       workspace, workspace_bytes, stream);
 }
 
 size_t csattn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,

@@ -17,7 +17,8 @@
 // At the end of a unit a softmax warpgroup rotates the next unit's Q (which
 // has landed by then) before its epilogue, so the MMA warp can start the next
 // unit's S = Q K^T while the epilogue stores O.
-// TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [256+D,256+2D).
+// TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [256+D,256+2D), with D
+// the head size of v and out (64); q and k have DK = 64 or 128 channels.
 // P (bf16) overwrites the first 64 columns of its S region and feeds the
 // second MMA straight from TMEM.
 //
@@ -39,40 +40,41 @@ namespace {
 
 using namespace fwd;
 
-template <int D>
+template <int DK, int D>
 struct Cfg {
-  static constexpr int KB = D / 64;              // 128-byte column blocks per row
   static constexpr int BLOCK_BYTES = BM * 128;   // one column block of a 128-row tile
-  static constexpr int TILE_BYTES = BM * D * 2;  // one Q / K / V tile
-  static constexpr int NS = 8;                   // K/V ring stages
-  static constexpr int SMEM_TILE_BYTES = (2 + NS) * TILE_BYTES;
+  static constexpr int Q_BYTES = BM * DK * 2;    // one Q or K tile
+  static constexpr int V_BYTES = BM * D * 2;     // one V tile
+  static constexpr int TILE_BYTES = Q_BYTES > V_BYTES ? Q_BYTES : V_BYTES;  // a ring stage
+  static constexpr int NS = DK == 64 ? 8 : 4;    // K/V ring stages
+  static constexpr int SMEM_TILE_BYTES = 2 * Q_BYTES + NS * TILE_BYTES;
   static constexpr int SMEM_BYTES = SMEM_TILE_BYTES + 1024 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);
 };
 
 // O (+)= P V: M=128, N=D, K=128 keys; P from TMEM, V MN-major (rows = keys).
-template <int D>
+template <int DK, int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                          bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
     umma_ts(d_tmem, p_tmem + 8u * kk, smem_desc_sw128(v_smem + 2048u * kk, BM * 128, 1024),
-            Cfg<D>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+            Cfg<DK, D>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
-template <int D>
+template <int DK, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103a_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
-  using C = Cfg<D>;
+  using C = Cfg<DK, D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ[2] = {smem, smem + C::TILE_BYTES};
-  uint8_t* sKV = smem + 2 * C::TILE_BYTES;
+  uint8_t* sQ[2] = {smem, smem + C::Q_BYTES};
+  uint8_t* sKV = smem + 2 * C::Q_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_TILE_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* q_ready = bars + 2;
@@ -136,9 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 !mbar_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, p.status, kWaitNs)) {
               ok = false;
             } else {
-              mbar_arrive_expect_tx(&q_full[x], C::TILE_BYTES);
+              mbar_arrive_expect_tx(&q_full[x], C::Q_BYTES);
 #pragma unroll
-              for (int kb = 0; kb < C::KB; ++kb)
+              for (int kb = 0; kb < DK / 64; ++kb)
                 tma_load_3d(sQ[x] + kb * C::BLOCK_BYTES, &tm_q, &q_full[x], kb * 64, un.q0[x],
                             un.b * p.Hq + un.h[x]);
               ++nq[x];
@@ -152,9 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
+            mbar_arrive_expect_tx(&kv_full[s], t == 0 ? C::Q_BYTES : C::V_BYTES);
             uint8_t* dst = sKV + s * C::TILE_BYTES;
-            for (int kb = 0; kb < C::KB; ++kb)
+            for (int kb = 0; kb < (t == 0 ? DK : D) / 64; ++kb)
               tma_load_3d(dst + kb * C::BLOCK_BYTES, t == 0 ? &tm_k : &tm_v, &kv_full[s], kb * 64,
                           j * BN, un.b * p.Hkv + un.kvh);
             ++fill;
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++cq[x];
             if (!k0_ready) k0_ready = wait(&kv_full[s0], (fill / C::NS) & 1);
             if (k0_ready) {
-              issue_qk<D>(tS[x], sQa[x], sKV0 + s0 * C::TILE_BYTES);
+              issue_qk<DK>(tS[x], sQa[x], sKV0 + s0 * C::TILE_BYTES);
               tc_commit(&s_full[x]);
               if (un.n[x] == 1) tc_commit(&q_empty[x]);
             }
@@ -217,13 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++cp[x];
               if (!v_ready) v_ready = wait(&kv_full[sV], (fV / C::NS) & 1);
               if (v_ready && (j > 0 || cu[x] == 0 || wait(&o_empty[x], (cu[x] - 1) & 1))) {
-                issue_pv<D>(tO[x], tS[x], sKV0 + sV * C::TILE_BYTES, j > 0);
+                issue_pv<DK, D>(tO[x], tS[x], sKV0 + sV * C::TILE_BYTES, j > 0);
                 if (x == 1) tc_commit(&kv_empty[sV]);
                 if (j == un.n[x] - 1) tc_commit(&o_full[x]);
                 if (j + 1 < un.n[x]) {
                   if (!k_ready) k_ready = wait(&kv_full[sK], (fK / C::NS) & 1);
                   if (k_ready) {
-                    issue_qk<D>(tS[x], sQa[x], sKV0 + sK * C::TILE_BYTES);
+                    issue_qk<DK>(tS[x], sQa[x], sKV0 + sK * C::TILE_BYTES);
                     tc_commit(&s_full[x]);
                     if (j + 1 == un.n[x] - 1) tc_commit(&q_empty[x]);
                     if (x == 1) tc_commit(&kv_empty[sK]);
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++cq;
         if (p.rope) {
-          rotate_q_row<D>(x ? sQ[1] : sQ[0], row, p.q_off + (x ? un2.q0[1] : un2.q0[0]) + row, p.rope,
+          rotate_q_row<DK>(x ? sQ[1] : sQ[0], row, p.q_off + (x ? un2.q0[1] : un2.q0[0]) + row, p.rope,
                           p.theta);
           fence_proxy_async_smem();
         }
@@ -410,32 +412,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-cudaError_t launch_d64(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
+template <int DK>
+cudaError_t launch_v64(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
   constexpr int D = 64;
-  using C = Cfg<D>;
+  using C = Cfg<DK, D>;
   const Params p = make_params(a);
   alignas(64) CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, a.B * a.Hq, BM) ||
-      !make_tmap_bf16_3d(&tk, k_eff, D, a.Tk, a.B * a.Hkv, BN) ||
+  if (!make_tmap_bf16_3d(&tq, a.q, DK, a.Tq, a.B * a.Hq, BM) ||
+      !make_tmap_bf16_3d(&tk, k_eff, DK, a.Tk, a.B * a.Hkv, BN) ||
       !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BN))
     return cudaErrorInvalidValue;
-
   static SmemLimitOnce smem_limit;
-  cudaError_t e = smem_limit.set(fwd_sm103a_kernel<D>, C::SMEM_BYTES);
+  cudaError_t e = smem_limit.set(fwd_sm103a_kernel<DK, D>, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = p.nUnits < a.num_sms ? p.nUnits : a.num_sms;
-  fwd_sm103a_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv);
+  fwd_sm103a_kernel<DK, D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// q, k with a.d channels and v, out with a.dv channels, each 64 or 128: v of 128
+// channels runs the O^T kernel (fwd_sm103a_d128.cu), v of 64 this file's kernel
 cudaError_t launch_fwd_sm103a(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
-  switch (a.d) {
-    case 64: return launch_d64(a, k_eff, stream);
-    case 128: return launch_fwd_sm103a_d128(a, k_eff, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.dv == 128) return launch_fwd_sm103a_d128(a, k_eff, stream);
+  if (a.dv != 64) return cudaErrorInvalidValue;
+  if (a.d == 64) return launch_v64<64>(a, k_eff, stream);
+  if (a.d == 128) return launch_v64<128>(a, k_eff, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace csattn

@@ -52,9 +52,9 @@ namespace {
 using namespace fwd;
 
 
-constexpr int D = 128;
+constexpr int D = 128;                               // head size of v and out
 constexpr int NS = 3;                                // K/V ring stages
-constexpr int TILE_BYTES = BM * D * 2;              // 32 KB
+constexpr int TILE_BYTES = BM * D * 2;              // 32 KB (a Q or K tile of d_k = 64 uses half)
 constexpr int BLOCK_BYTES = BM * 128;               // 16 KB
 constexpr int P_BYTES = 2 * BM * BN * 2;            // 64 KB: 256 rows x 128 keys
 constexpr int SMEM_DATA = (2 + NS) * TILE_BYTES + P_BYTES;  // 229376
@@ -102,8 +102,9 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int x, 
                : "memory");
 }
 
-// RoPE of 16-channel chunks [c_begin, c_end) of row r in one or two Q tiles at the same
-// position: the angles are computed once and applied to both tiles.
+// RoPE of 16-channel chunks [c_begin, c_end) of row r in one or two Q tiles (head size
+// DK) at the same position: the angles are computed once and applied to both tiles.
+template <int DK>
 __device__ __forceinline__ void rotate_chunks(uint8_t* tile0, uint8_t* tile1, int r, int pos,
                                               int layout, const RopeTable& th, int c_begin,
                                               int c_end) {
@@ -112,7 +113,7 @@ __device__ __forceinline__ void rotate_chunks(uint8_t* tile0, uint8_t* tile1, in
     int e0, e1;
     if (layout == 1) {
       e0 = 8 * c;
-      e1 = D / 2 + 8 * c;
+      e1 = DK / 2 + 8 * c;
     } else {
       e0 = 16 * c;
       e1 = 16 * c + 8;
@@ -192,6 +193,8 @@ __device__ __forceinline__ void issue_pvt(uint32_t d_tmem, uint32_t v_smem, uint
   }
 }
 
+// DK: head size of q and k (64 or 128); v and out have D = 128 channels.
+template <int DK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_d128_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -264,15 +267,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t fill = 0;
       uint32_t nq[2] = {0, 0};
       bool ok = true;
-      auto load = [&](const CUtensorMap* m, int j, int z) {
+      // one K (DK channels) or V (D channels) tile into the next ring stage
+      auto load = [&](const CUtensorMap* m, int width, int j, int z) {
         const uint32_t s = fill % NS, use = fill / NS;
         if (use > 0 && !mbar_wait(&kv_empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) {
           ok = false;
           return;
         }
-        mbar_arrive_expect_tx(&kv_full[s], TILE_BYTES);
+        mbar_arrive_expect_tx(&kv_full[s], static_cast<uint32_t>(BN * width * 2));
         uint8_t* dst = sKV + s * TILE_BYTES;
-        for (int kb = 0; kb < D / 64; ++kb)
+        for (int kb = 0; kb < width / 64; ++kb)
           tma_load_3d(dst + kb * BLOCK_BYTES, m, &kv_full[s], kb * 64, j * BN, z);
         ++fill;
       };
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Unit un2 = decode_unit(p, u2);
             for (int x = 0; x < 2; ++x)
               if (un2.n[x] > 0)
-                for (int kb = 0; kb < D / 64; ++kb)
+                for (int kb = 0; kb < DK / 64; ++kb)
                   tma_prefetch_l2_3d(&tm_q, kb * 64, un2.q0[x], un2.b * p.Hq + un2.h[x]);
           }
         }
@@ -298,9 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 !mbar_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, p.status, kWaitNs)) {
               ok = false;
             } else {
-              mbar_arrive_expect_tx(&q_full[x], TILE_BYTES);
+              mbar_arrive_expect_tx(&q_full[x], static_cast<uint32_t>(BM * DK * 2));
 #pragma unroll
-              for (int kb = 0; kb < D / 64; ++kb)
+              for (int kb = 0; kb < DK / 64; ++kb)
                 tma_load_3d(sQ[x] + kb * BLOCK_BYTES, &tm_q, &q_full[x], kb * 64, un.q0[x],
                             un.b * p.Hq + un.h[x]);
               ++nq[x];
@@ -310,10 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K leads V by one tile: K_0, then (K_{j+1}, V_j) for each j
         const int n = un.n[1];
         const int z = un.b * p.Hkv + un.kvh;
-        if (ok) load(&tm_k, 0, z);
+        if (ok) load(&tm_k, DK, 0, z);
         for (int j = 0; j < n && ok; ++j) {
-          if (j + 1 < n) load(&tm_k, j + 1, z);
-          if (ok) load(&tm_v, j, z);
+          if (j + 1 < n) load(&tm_k, DK, j + 1, z);
+          if (ok) load(&tm_v, D, j, z);
         }
       }
       if (*abort_flag) {
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait(&q_ready[x], cq[x] & 1)) break;
             ++cq[x];
           }
-          issue_qk<D>(tS[x], sQa[x], stage(fK0));
+          issue_qk<DK>(tS[x], sQa[x], stage(fK0));
           tc_commit(&s_full[x]);
           if (n == 1 && un.n[x] > 0) tc_commit(&q_empty[x]);
         }
@@ -369,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = 0; x < 2; ++x) {
               if (!wait(&s_free[x], cfree[x] & 1)) break;
               ++cfree[x];
-              issue_qk<D>(tS[x], sQa[x], stage(fK));
+              issue_qk<DK>(tS[x], sQa[x], stage(fK));
               tc_commit(&s_full[x]);
               if (j + 1 == n - 1 && un.n[x] > 0) tc_commit(&q_empty[x]);
             }
@@ -435,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++cqa;
           ++cqb;
           if (p.rope) {
-            rotate_chunks(sQ[0], sQ[1], row, p.q_off + un2.q0[0] + row, p.rope, p.theta, x * (D / 32),
-                          (x + 1) * (D / 32));
+            rotate_chunks<DK>(sQ[0], sQ[1], row, p.q_off + un2.q0[0] + row, p.rope, p.theta,
+                              x * (DK / 32), (x + 1) * (DK / 32));
             fence_proxy_async_smem();
           }
           __syncwarp();
@@ -456,9 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++cq;
         if (p.rope) {
-          rotate_chunks(x ? sQ[1] : sQ[0], nullptr, row, p.q_off + (x ? un2.q0[1] : un2.q0[0]) + row,
+          rotate_chunks<DK>(x ? sQ[1] : sQ[0], nullptr, row, p.q_off + (x ? un2.q0[1] : un2.q0[0]) + row,
                         p.rope, p.theta,
-                        0, D / 16);
+                        0, DK / 16);
           fence_proxy_async_smem();
         }
         __syncwarp();
@@ -660,23 +664,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-
-}  // namespace
-
-cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
+template <int DK>
+cudaError_t launch_dk(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
   const Params p = make_params(a);
   alignas(64) CUtensorMap tq, tk, tv, to;
-  if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, a.B * a.Hq, BM) ||
-      !make_tmap_bf16_3d(&tk, k_eff, D, a.Tk, a.B * a.Hkv, BN) ||
+  if (!make_tmap_bf16_3d(&tq, a.q, DK, a.Tq, a.B * a.Hq, BM) ||
+      !make_tmap_bf16_3d(&tk, k_eff, DK, a.Tk, a.B * a.Hkv, BN) ||
       !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BN) ||
       !make_tmap_bf16_3d(&to, a.out, D, a.Tq, a.B * a.Hq, BM))
     return cudaErrorInvalidValue;
   static SmemLimitOnce smem_limit;
-  cudaError_t e = smem_limit.set(fwd_d128_kernel, SMEM_BYTES);
+  cudaError_t e = smem_limit.set(fwd_d128_kernel<DK>, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = p.nUnits < a.num_sms ? p.nUnits : a.num_sms;
-  fwd_d128_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tq, tk, tv, to);
+  fwd_d128_kernel<DK><<<grid, kThreads, SMEM_BYTES, stream>>>(p, tq, tk, tv, to);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// v and out with 128 channels; q and k with a.d = 64 or 128
+cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
+  if (a.d == 128) return launch_dk<128>(a, k_eff, stream);
+  if (a.d == 64) return launch_dk<64>(a, k_eff, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace csattn

@@ -19,6 +19,7 @@ struct FwdArgs {
   void* out;
   float* lse;
   int B, Hq, Hkv, d;
+  int dv;            // head size of v and out (d: head size of q and k)
   int Tq, Tk;        // query rows, key rows
   int q_off;         // position of query row 0 (keys sit at 0..Tk-1)
   int causal;        // 1: key j visible to query i iff j <= q_off + i
@@ -30,15 +31,16 @@ struct FwdArgs {
   int num_sms;
 };
 
-// fp32 SIMT path (any d in {16,32,64,128}).
+// fp32 SIMT path (d and dv each in {16,32,64,128}).
 cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t stream);
 
 // bf16 path: x_rot = RoPE(x) for x [B, H, T, d] bf16 (rope 1 split-half, 2 adjacent).
 cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, int T, int d,
                                     int rope, const RopeTable& theta, cudaStream_t stream);
 
-// bf16 tcgen05 prefill; `k_eff` is k itself or its rotated copy.  d = 64 runs
-// the kernel in fwd_sm103a.cu, d = 128 the one in fwd_sm103a_d128.cu.
+// bf16 tcgen05 prefill; `k_eff` is k itself or its rotated copy.  q, k have d
+// and v, out dv channels (each 64 or 128): dv = 64 runs the kernel in
+// fwd_sm103a.cu, dv = 128 the one in fwd_sm103a_d128.cu.
 cudaError_t launch_fwd_sm103a(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
 cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
 
