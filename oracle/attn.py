@@ -50,7 +50,7 @@ __all__ = [
     "round_to_bf16", "expand_kv_heads", "causal_additive_mask", "attention_scores",
     "attention", "attention_rows", "attention_lse", "attention_backward", "decode",
     "decode_paged", "decode_step", "merge_partials", "split_partials", "rope_rotate_transpose",
-]
+    "cache_append", "cache_append_paged"]
 
 _BF16_MAX = float.fromhex("0x1.fep127")
 
@@ -318,6 +318,51 @@ def decode_step(q_new, k_new, v_new, k_cache, v_cache, cache_lens, *, rope_base=
         vc[b, :, pos] = v_new[b, :, 0]
     out = decode(qr, kc, vc, [L + 1 for L in lens], scale=scale)
     return out, kc, vc
+
+
+def cache_append(k_new, v_new, k_cache, v_cache, cache_lens, *, rope_base=0.0,
+                 rope_layout="split_half", operand_dtype=None):
+    """Append Tn tokens per sequence to contiguous caches [B, Hkv, Lmax, d].
+
+    Token t of sequence b sits at position p = cache_lens[b] + t ("The
+    Transformer architecture", "Hands-on": the cache grows by one row per
+    token, at cache.pos); its key is rotated at p (RoPE on keys, never on
+    values: same page, "Now: RoPE") and rounded to ``operand_dtype``, and key
+    and value are written to row p.  Returns the new caches as float64 arrays.
+    """
+    k_new = np.asarray(_as_np(k_new), dtype=np.float64)
+    v_new = np.asarray(_as_np(v_new), dtype=np.float64)
+    kc = np.array(_as_np(k_cache), dtype=np.float64)
+    vc = np.array(_as_np(v_cache), dtype=np.float64)
+    Tn = k_new.shape[2]
+    lens = [int(x) for x in np.asarray(_as_np(cache_lens)).reshape(-1)]
+    for b, L in enumerate(lens):
+        pos = L + np.arange(Tn)
+        kc[b, :, L:L + Tn] = _rotated(k_new[b], rope_base, rope_layout, operand_dtype, pos)
+        vc[b, :, L:L + Tn] = v_new[b]
+    return kc, vc
+
+
+def cache_append_paged(k_new, v_new, k_pages, v_pages, block_table, cache_lens, page_size: int,
+                       *, rope_base=0.0, rope_layout="split_half", operand_dtype=None):
+    """``cache_append`` into paged caches [num_pages, Hkv, page_size, d]: row r of
+    sequence b lives in page block_table[b][r // page_size] at offset r % page_size.
+    Returns the new page pools as float64 arrays."""
+    k_new = np.asarray(_as_np(k_new), dtype=np.float64)
+    v_new = np.asarray(_as_np(v_new), dtype=np.float64)
+    kp = np.array(_as_np(k_pages), dtype=np.float64)
+    vp = np.array(_as_np(v_pages), dtype=np.float64)
+    bt = np.asarray(_as_np(block_table)).astype(np.int64)
+    Tn = k_new.shape[2]
+    lens = [int(x) for x in np.asarray(_as_np(cache_lens)).reshape(-1)]
+    for b, L in enumerate(lens):
+        kr = _rotated(k_new[b], rope_base, rope_layout, operand_dtype, L + np.arange(Tn))
+        for t in range(Tn):
+            r = L + t
+            page, off = bt[b, r // page_size], r % page_size
+            kp[page, :, off] = kr[:, t]
+            vp[page, :, off] = v_new[b, :, t]
+    return kp, vp
 
 
 def rope_rotate_transpose(x, positions, base: float, layout: str = "split_half"):

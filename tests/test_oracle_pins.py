@@ -207,6 +207,62 @@ def pin_value_width(o):
     assert np.array_equal(o.attention(q, k, v, causal=False), v)
 
 
+def pin_cache_append_positions(o):
+    """Appending a sequence to an empty cache in chunks puts at row t the key rotated at
+    position t (the whole sequence rotated at once) and the value itself."""
+    B, Hkv, d, Lmax = 2, 2, 8, 20
+    k = _rand((B, Hkv, 16, d), 340)
+    v = _rand((B, Hkv, 16, d), 341)
+    kc = np.full((B, Hkv, Lmax, d), np.nan)
+    vc = np.full((B, Hkv, Lmax, d), np.nan)
+    L = 0
+    for a, b in ((0, 5), (5, 12), (12, 16)):
+        kc, vc = o.cache_append(k[:, :, a:b], v[:, :, a:b], kc, vc, [L, L], rope_base=10000.0,
+                                operand_dtype="bf16")
+        L = b
+    want = o.round_to_bf16(o.rope_rotate(k, np.arange(16), 10000.0))
+    assert np.array_equal(kc[:, :, :16], want)
+    assert np.array_equal(vc[:, :, :16], v)
+    assert np.all(np.isnan(kc[:, :, 16:])) and np.all(np.isnan(vc[:, :, 16:]))
+
+
+def pin_cache_append_matches_decode_step(o):
+    """One appended token writes the same cache rows as the decode step's append."""
+    B, Hq, Hkv, d, Lmax = 3, 4, 2, 8, 12
+    kc = _rand((B, Hkv, Lmax, d), 350)
+    vc = _rand((B, Hkv, Lmax, d), 351)
+    q1 = _rand((B, Hq, 1, d), 352)
+    k1 = _rand((B, Hkv, 1, d), 353)
+    v1 = _rand((B, Hkv, 1, d), 354)
+    lens = [0, 5, 11]
+    _, kd, vd = o.decode_step(q1, k1, v1, kc, vc, lens, rope_base=10000.0,
+                              rope_layout="adjacent", operand_dtype="bf16")
+    ka, va = o.cache_append(k1, v1, kc, vc, lens, rope_base=10000.0, rope_layout="adjacent",
+                            operand_dtype="bf16")
+    assert np.array_equal(ka, kd) and np.array_equal(va, vd)
+
+
+def pin_cache_append_paged_equals_contiguous(o):
+    """Appending into shuffled pages and gathering them back through the block table
+    gives the contiguous append."""
+    B, Hkv, d, page, n_lp = 2, 2, 8, 4, 4
+    kc = np.zeros((B, Hkv, n_lp * page, d))
+    vc = np.zeros((B, Hkv, n_lp * page, d))
+    kn = _rand((B, Hkv, 6, d), 360)
+    vn = _rand((B, Hkv, 6, d), 361)
+    lens = [3, 9]
+    perm = np.random.default_rng(362).permutation(B * n_lp + 1)
+    table = perm[:B * n_lp].reshape(B, n_lp)
+    kp = np.zeros((B * n_lp + 1, Hkv, page, d))
+    vp = np.zeros((B * n_lp + 1, Hkv, page, d))
+    kc2, vc2 = o.cache_append(kn, vn, kc, vc, lens, rope_base=10000.0)
+    kp2, vp2 = o.cache_append_paged(kn, vn, kp, vp, table, lens, page, rope_base=10000.0)
+    for b in range(B):
+        for r in range(n_lp * page):
+            assert np.array_equal(kp2[table[b, r // page], :, r % page], kc2[b, :, r])
+            assert np.array_equal(vp2[table[b, r // page], :, r % page], vc2[b, :, r])
+
+
 def pin_degenerate_cases(o):
     q = _rand((1, 2, 1, 8), 90)
     k = _rand((1, 2, 1, 8), 91)
@@ -486,7 +542,8 @@ ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exa
             pin_chunk_equals_full_rows, pin_chunk_naive, pin_decode_is_chunk_of_one,
             pin_decode_step_appends_then_attends, pin_backward_finite_differences,
             pin_backward_autograd, pin_rope_transpose_inverts,
-            pin_decode_paged_equals_contiguous, pin_value_width]
+            pin_decode_paged_equals_contiguous, pin_value_width, pin_cache_append_positions,
+            pin_cache_append_matches_decode_step, pin_cache_append_paged_equals_contiguous]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -787,3 +844,39 @@ def test_planted_paged_offset_swapped():
 def test_planted_scale_from_value_width():
     """The default scale taken from v's width instead of the keys' fails a pin."""
     assert _fails(_Mutant(scale_from_v=True), [pin_value_width])
+
+
+def test_planted_cache_append_position_ignores_offset():
+    """Keys rotated at t instead of cache_lens[b] + t fail a pin."""
+    def bad(k_new, v_new, k_cache, v_cache, cache_lens, *, rope_base=0.0,
+            rope_layout="split_half", operand_dtype=None):
+        kc = np.array(k_cache, dtype=np.float64)
+        vc = np.array(v_cache, dtype=np.float64)
+        kn = np.asarray(k_new, dtype=np.float64)
+        Tn = kn.shape[2]
+        for b, L in enumerate(cache_lens):
+            kr = OA.rope_rotate(kn[b], np.arange(Tn), rope_base, rope_layout) if rope_base > 0 else kn[b]
+            kc[b, :, L:L + Tn] = OA.round_to(kr, operand_dtype)
+            vc[b, :, L:L + Tn] = np.asarray(v_new, dtype=np.float64)[b]
+        return kc, vc
+    assert _fails(_Mutant(cache_append=bad), [pin_cache_append_positions])
+
+
+def test_planted_paged_append_offset_swapped():
+    """Page and offset swapped in the paged append fail a pin."""
+    def bad(k_new, v_new, k_pages, v_pages, block_table, cache_lens, page_size, *,
+            rope_base=0.0, rope_layout="split_half", operand_dtype=None):
+        kp = np.array(k_pages, dtype=np.float64)
+        vp = np.array(v_pages, dtype=np.float64)
+        kn = np.asarray(k_new, dtype=np.float64)
+        vn = np.asarray(v_new, dtype=np.float64)
+        bt = np.asarray(block_table)
+        for b, L in enumerate(cache_lens):
+            kr = OA.rope_rotate(kn[b], L + np.arange(kn.shape[2]), rope_base, rope_layout)
+            for t in range(kn.shape[2]):
+                r = L + t
+                page, off = bt[b, r % page_size], r // page_size
+                kp[page, :, off] = kr[:, t]
+                vp[page, :, off] = vn[b, :, t]
+        return kp, vp
+    assert _fails(_Mutant(cache_append_paged=bad), [pin_cache_append_paged_equals_contiguous])
