@@ -550,6 +550,35 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
                      "frac": round(gbs / hbm_peak, 4), "traffic": None,
                      "kernel": "decode_bf16_kernel<128> (paged reads) + decode_combine_kernel"}}
     del kp, vp, table
+    # a 1024-token chunk of the llama_chunk_bf16 shape appended (keys rotated) at row 3072
+    # of contiguous caches; bytes = the chunk's K and V read once and written once
+    g.manual_seed(10)
+    kn = torch.randn(wc.B, wc.Hkv, 1024, wc.d, generator=g).to(torch.bfloat16).to(dev)
+    vn = torch.randn(wc.B, wc.Hkv, 1024, wc.d, generator=g).to(torch.bfloat16).to(dev)
+    kca = torch.zeros(wc.B, wc.Hkv, wc.Tk, wc.d, dtype=torch.bfloat16, device=dev)
+    vca = torch.zeros_like(kca)
+    at = torch.full((wc.B,), wc.q_offset, dtype=torch.int32, device=dev)
+    ts = []
+    for i in range(3 + reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csattn.cache_append(kn, vn, kca, vca, at, rope_base=wc.rope_base, stream=stream)
+        e1.record(stream)
+        if i >= 3:
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    csattn.check_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    abytes = 2.0 * 2 * kn.numel() * 2
+    gbs = abytes / (ms * 1e-3) / 1e9
+    out["cache_append"] = {
+        "workload": "1024-token chunk appended to contiguous caches (B=4, Hkv=8, d=128, "
+                    "Lmax=4096, rows 3072..4095), keys rotated (RoPE 1e4)",
+        "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": abytes,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "kernel": "cache_append_kernel"}}
+    del kn, vn, kca, vca
     # backward of the headline prefill (dq, dk, dv), FLOPs = 2.5x the forward's (the
     # convention for QK^T recomputation + dV + dP + dQ + dK)
     wp = W.WORKLOADS["llama_gqa_bf16"]

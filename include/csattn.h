@@ -297,6 +297,39 @@ int csattn_attn_decode_noalloc(const void* q, const void* k_cache, const void* v
                                int num_splits, void* stream);
 
 /*
+ * Appends Tn tokens per sequence to the KV caches (a prefill chunk written into
+ * the cache, "The Transformer architecture", "Hands-on": the cache grows a row per
+ * token and a token's key is rotated at its position).  For sequence b and
+ * t < Tn, row r = cache_lens[b] + t receives RoPE(k_new[b, :, t]) at position r
+ * (rounded to bf16 as csattn_rope_rotate rounds) and v_new[b, :, t].
+ *   k_new, v_new  [B, Hkv, Tn, d] bf16 (keys not rotated)
+ *   k_cache, v_cache  [B, Hkv, Lmax, d] bf16, written at rows cache_lens[b]..+Tn-1
+ *   cache_lens    device int32 [B]: rows already cached (not advanced here)
+ *   rope_base, rope_layout  as csattn_attn_fwd (rope_base <= 0: keys copied)
+ * Requirements: bf16, d in {64, 128}, B, Hkv >= 1, 1 <= Tn <= Lmax < 2^30,
+ * Tn < 2^20, Lmax <= 49152 with RoPE; pointers 16-byte aligned (cache_lens
+ * 4-byte).  A sequence with cache_lens[b] < 0 or cache_lens[b] + Tn > Lmax is
+ * left untouched and raises CSATTN_ERR_DEVICE_ARG in the status word.
+ * Asynchronous on `stream`.
+ */
+int csattn_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                        const int32_t* cache_lens, int B, int Hkv, int Tn, int Lmax, int d,
+                        int dtype, float rope_base, int rope_layout, void* stream);
+
+/*
+ * csattn_cache_append into paged caches [num_pages, Hkv, page_size, d]: row r of
+ * sequence b lives in page block_table[b * max_pages + r / page_size] at offset
+ * r % page_size (the layout csattn_attn_decode_paged reads); the cache of a
+ * sequence holds max_pages * page_size rows.  page_size is a multiple of 64.  A
+ * page index outside [0, num_pages) raises CSATTN_ERR_DEVICE_ARG and that row is
+ * not written.
+ */
+int csattn_cache_append_paged(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                              const int32_t* block_table, const int32_t* cache_lens, int B,
+                              int Hkv, int Tn, int page_size, int num_pages, int max_pages, int d,
+                              int dtype, float rope_base, int rope_layout, void* stream);
+
+/*
  * Synchronize `stream`, then read and clear this device's status word.
  * Returns CSATTN_OK, CSATTN_ERR_TIMEOUT (a kernel wait ran out of time),
  * CSATTN_ERR_DEVICE_ARG (a device-side argument check failed) or

@@ -184,6 +184,48 @@ def test_decode_paged_rejects_invalid_arguments(lib, kw, status):
 
 
 @pytest.mark.parametrize("kw,status", [
+    (dict(k_new=None), -1),
+    (dict(lens=FAKE + 2), -1),
+    (dict(Tn=0), -1),
+    (dict(Tn=300, Lmax=256), -1),
+    (dict(d=96), -2),
+    (dict(dtype=0), -2),
+    (dict(dtype=5), -1),
+    (dict(rope_layout=3), -1),
+    (dict(rope_base=10000.0, Lmax=60000, Tn=16), -2),
+])
+def test_cache_append_rejects_invalid_arguments(lib, kw, status):
+    a = dict(k_new=FAKE, v_new=FAKE, kc=FAKE, vc=FAKE, lens=FAKE, B=2, Hkv=2, Tn=16, Lmax=256,
+             d=128, dtype=1, rope_base=0.0, rope_layout=0)
+    a.update(kw)
+    rc = lib.csattn_cache_append(a["k_new"], a["v_new"], a["kc"], a["vc"], a["lens"], a["B"],
+                                 a["Hkv"], a["Tn"], a["Lmax"], a["d"], a["dtype"], a["rope_base"],
+                                 a["rope_layout"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"cache_append" in lib.csattn_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(table=None), -1),
+    (dict(page_size=96), -1),
+    (dict(num_pages=0), -1),
+    (dict(Tn=600), -1),
+    (dict(d=32), -2),
+])
+def test_cache_append_paged_rejects_invalid_arguments(lib, kw, status):
+    a = dict(k_new=FAKE, v_new=FAKE, kp=FAKE, vp=FAKE, table=FAKE, lens=FAKE, B=2, Hkv=2, Tn=16,
+             page_size=128, num_pages=8, max_pages=4, d=128, dtype=1, rope_base=0.0,
+             rope_layout=0)
+    a.update(kw)
+    rc = lib.csattn_cache_append_paged(a["k_new"], a["v_new"], a["kp"], a["vp"], a["table"],
+                                       a["lens"], a["B"], a["Hkv"], a["Tn"], a["page_size"],
+                                       a["num_pages"], a["max_pages"], a["d"], a["dtype"],
+                                       a["rope_base"], a["rope_layout"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"cache_append_paged" in lib.csattn_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
     (dict(q_new=None), -1),
     (dict(k_new=FAKE + 8), -1),
     (dict(rope_layout=7), -1),

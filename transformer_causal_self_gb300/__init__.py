@@ -55,6 +55,8 @@ _SIGNATURES = {
                                                                     _vp]),
     "csattn_attn_decode_paged": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _c_int, _c_int, _vp,
                                                                     _c_size, _vp]),
+    "csattn_cache_append": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _vp]),
+    "csattn_cache_append_paged": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _c_int, _vp]),
     "csattn_check_status": (_c_int, [_vp]),
     "csattn_selftest_bounded_wait": (_c_int, [_c_int, _vp]),
     "csattn_last_error": (ctypes.c_char_p, []),
@@ -353,6 +355,44 @@ def attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Ten
                                         int(num_splits), workspace.data_ptr(), workspace.numel(),
                                         _stream_handle(stream)))
     return out
+
+
+def cache_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, cache_lens: torch.Tensor, *, rope_base: float = 0.0,
+                 rope_layout: str = "split_half", stream=None) -> None:
+    """Append Tn tokens per sequence at rows cache_lens[b].. (C: csattn_cache_append).
+
+    k_new, v_new [B,Hkv,Tn,d] (keys not rotated); caches [B,Hkv,Lmax,d]; cache_lens
+    int32 [B] on the device, not advanced.
+    """
+    _need_cuda(k_new, v_new, k_cache, v_cache, cache_lens)
+    if cache_lens.dtype != torch.int32:
+        raise TypeError("cache_lens must be int32")
+    B, Hkv, Tn, d = k_new.shape
+    lib = load_library()
+    _check(lib.csattn_cache_append(k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+                                   v_cache.data_ptr(), cache_lens.data_ptr(), B, Hkv, Tn,
+                                   k_cache.shape[2], d, _dtype_code(k_new), float(rope_base),
+                                   _ROPE_LAYOUT[rope_layout], _stream_handle(stream)))
+
+
+def cache_append_paged(k_new: torch.Tensor, v_new: torch.Tensor, k_pages: torch.Tensor,
+                       v_pages: torch.Tensor, block_table: torch.Tensor, cache_lens: torch.Tensor,
+                       *, rope_base: float = 0.0, rope_layout: str = "split_half",
+                       stream=None) -> None:
+    """Append into paged caches [num_pages,Hkv,page_size,d] (C: csattn_cache_append_paged)."""
+    _need_cuda(k_new, v_new, k_pages, v_pages, block_table, cache_lens)
+    if block_table.dtype != torch.int32 or cache_lens.dtype != torch.int32:
+        raise TypeError("block_table and cache_lens must be int32")
+    B, Hkv, Tn, d = k_new.shape
+    num_pages, page_size = k_pages.shape[0], k_pages.shape[2]
+    lib = load_library()
+    _check(lib.csattn_cache_append_paged(k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(),
+                                         v_pages.data_ptr(), block_table.data_ptr(),
+                                         cache_lens.data_ptr(), B, Hkv, Tn, page_size, num_pages,
+                                         block_table.shape[1], d, _dtype_code(k_new),
+                                         float(rope_base), _ROPE_LAYOUT[rope_layout],
+                                         _stream_handle(stream)))
 
 
 def check_status(stream=None) -> None:

@@ -594,6 +594,88 @@ int csattn_attn_decode_step(const void* q_new, const void* k_new, const void* v_
                      scale, max_seq_len, num_splits, workspace, q_at, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Shared by the contiguous and the paged chunk append (block_table == nullptr: contiguous).
+int cache_append_impl(const char* fn, const void* k_new, const void* v_new, void* k_cache,
+                      void* v_cache, const int32_t* cache_lens, const int32_t* block_table, int B,
+                      int Hkv, int Tn, int Lmax, int d, int page_size, int num_pages,
+                      int max_pages, int dtype, float rope_base, int rope_layout, void* stream) {
+  if (k_new == nullptr || v_new == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      cache_lens == nullptr)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  if (B < 1 || Hkv < 1 || Tn < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: B=%d, Hkv=%d, Tn=%d must be >= 1", fn, B, Hkv, Tn);
+  if (dtype != CSATTN_F32 && dtype != CSATTN_BF16)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, dtype);
+  if (dtype != CSATTN_BF16)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: only bf16 is implemented (dtype %d)", fn, dtype);
+  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d", fn, d);
+  if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown rope_layout %d", fn, rope_layout);
+  if (!std::isfinite(rope_base))
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: rope_base must be finite", fn);
+  if (Lmax < Tn) return fail(CSATTN_ERR_INVALID_ARG, "%s: Tn=%d > cache rows %d", fn, Tn, Lmax);
+  if (Lmax >= (1 << 30) || Tn >= (1 << 20))
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: cache rows %d or Tn=%d too large", fn, Lmax, Tn);
+  if (rope_base > 0.f && Lmax > kMaxRopePositions)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: RoPE supports positions < %d, cache rows %d", fn,
+                kMaxRopePositions, Lmax);
+  RopeTable th{};
+  const int rope = rope_base > 0.f ? (rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2) : 0;
+  if (rope) rope_table(&th, d, static_cast<double>(rope_base));
+  uint32_t* status = nullptr;
+  int num_sms = 0;
+  int rc = device_info(&status, &num_sms);
+  if (rc != CSATTN_OK) return rc;
+  cudaError_t e = launch_cache_append_bf16(k_new, v_new, k_cache, v_cache, cache_lens,
+                                           block_table, B, Hkv, Tn, Lmax, d, page_size,
+                                           num_pages, max_pages, rope, th, status,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "cache append kernel launch");
+  return CSATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int csattn_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                        const int32_t* cache_lens, int B, int Hkv, int Tn, int Lmax, int d,
+                        int dtype, float rope_base, int rope_layout, void* stream) {
+  return cache_append_impl("cache_append", k_new, v_new, k_cache, v_cache, cache_lens, nullptr,
+                           B, Hkv, Tn, Lmax, d, 0, 0, 0, dtype, rope_base, rope_layout, stream);
+}
+
+int csattn_cache_append_paged(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                              const int32_t* block_table, const int32_t* cache_lens, int B,
+                              int Hkv, int Tn, int page_size, int num_pages, int max_pages, int d,
+                              int dtype, float rope_base, int rope_layout, void* stream) {
+  const char* fn = "cache_append_paged";
+  if (block_table == nullptr)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: block_table must be non-null", fn);
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: block_table must be 4-byte aligned", fn);
+  if (page_size < 64 || page_size % 64 != 0 || page_size > 65536)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: page_size=%d must be a multiple of 64 in [64, 65536]",
+                fn, page_size);
+  if (num_pages < 1 || max_pages < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: num_pages=%d and max_pages=%d must be >= 1", fn,
+                num_pages, max_pages);
+  if (Hkv >= 1 && static_cast<long long>(num_pages) * Hkv * page_size > (1LL << 40))
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: page pool too large", fn);
+  const long long lmax = static_cast<long long>(max_pages) * page_size;
+  if (lmax >= (1 << 30)) return fail(CSATTN_ERR_UNSUPPORTED, "%s: max_pages * page_size too large", fn);
+  return cache_append_impl(fn, k_new, v_new, k_pages, v_pages, cache_lens, block_table, B, Hkv, Tn,
+                           static_cast<int>(lmax), d, page_size, num_pages, max_pages, dtype,
+                           rope_base, rope_layout, stream);
+}
+
 int csattn_check_status(void* stream) {
   uint32_t* status = nullptr;
   int num_sms = 0;

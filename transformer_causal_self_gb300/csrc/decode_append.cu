@@ -112,6 +112,71 @@ __global__ void __launch_bounds__(kThreads) decode_append_kernel(
   }
 }
 
+// Append of Tn tokens per sequence (a prefill chunk): token t of sequence b sits
+// at row r = cache_lens[b] + t; its key is rotated at r and rounded to bf16, and
+// key and value go to row r of the caches, contiguous ([B, Hkv, Lmax, d]) or paged
+// (block_table != nullptr: [num_pages, Hkv, page_size, d], row r of sequence b in
+// page block_table[b * max_pages + r / page_size] at offset r % page_size).
+// Grid (B, token groups of kTokens); thread work item = (token, head, 16-channel
+// chunk) for the keys and (token, head, 8-channel chunk) for the values.
+constexpr int kTokens = 16;
+
+__global__ void __launch_bounds__(kThreads) cache_append_kernel(
+    const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
+    __nv_bfloat16* __restrict__ k_cache, __nv_bfloat16* __restrict__ v_cache,
+    const int32_t* __restrict__ cache_lens, const int32_t* __restrict__ block_table, int Hkv,
+    int Tn, int Lmax, int d, int page_size, int num_pages, int max_pages, int rope,
+    RopeTable theta, uint32_t* status) {
+  const int b = blockIdx.x;
+  const int t0 = blockIdx.y * kTokens;
+  const int nt = min(kTokens, Tn - t0);
+  const int L = cache_lens[b];
+  if (L < 0 || L > Lmax - Tn) {  // (no overflow: Lmax, Tn < 2^30)
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(status, kStatusDeviceArg);
+    return;
+  }
+  const int chunks = d / 16;
+  const int n_key = nt * Hkv * chunks;
+  const int n_all = n_key + nt * Hkv * (d / 8);
+  for (int it = threadIdx.x; it < n_all; it += blockDim.x) {
+    const bool key = it < n_key;
+    const int j = key ? it : it - n_key;
+    const int per_tok = Hkv * (key ? chunks : d / 8);
+    const int tt = j / per_tok, rem = j - tt * per_tok;
+    const int g = rem / (key ? chunks : d / 8), c = rem - g * (key ? chunks : d / 8);
+    const int t = t0 + tt, r = L + t;
+    size_t row;  // element offset of cache row r of head g
+    if (block_table != nullptr) {
+      const int page = block_table[static_cast<size_t>(b) * max_pages + r / page_size];
+      if (page < 0 || page >= num_pages) {
+        atomicOr(status, kStatusDeviceArg);
+        continue;
+      }
+      row = ((static_cast<size_t>(page) * Hkv + g) * page_size + r % page_size) * d;
+    } else {
+      row = ((static_cast<size_t>(b) * Hkv + g) * Lmax + r) * d;
+    }
+    const size_t src = ((static_cast<size_t>(b) * Hkv + g) * Tn + t) * d;
+    if (!key) {
+      *reinterpret_cast<uint4*>(v_cache + row + 8 * c) =
+          *reinterpret_cast<const uint4*>(v_new + src + 8 * c);
+      continue;
+    }
+    if (rope == 0) {
+      *reinterpret_cast<uint4*>(k_cache + row + 16 * c) =
+          *reinterpret_cast<const uint4*>(k_new + src + 16 * c);
+      *reinterpret_cast<uint4*>(k_cache + row + 16 * c + 8) =
+          *reinterpret_cast<const uint4*>(k_new + src + 16 * c + 8);
+      continue;
+    }
+    float cs[8], sn[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      rope_cos_sin<false>(r, theta.hi[8 * c + i], theta.lo[8 * c + i], cs[i], sn[i]);
+    rotate8(k_new + src, k_cache + row, d, c, rope, cs, sn);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_decode_append_bf16(const void* q_new, const void* k_new, const void* v_new,
@@ -124,6 +189,20 @@ cudaError_t launch_decode_append_bf16(const void* q_new, const void* k_new, cons
       static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(k_cache),
       static_cast<__nv_bfloat16*>(v_cache), cache_lens, static_cast<__nv_bfloat16*>(q_rot), Hq,
       Hkv, Lmax, d, max_pos, rope, theta, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cache_append_bf16(const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const int32_t* cache_lens,
+                                     const int32_t* block_table, int B, int Hkv, int Tn, int Lmax,
+                                     int d, int page_size, int num_pages, int max_pages, int rope,
+                                     const RopeTable& theta, uint32_t* status,
+                                     cudaStream_t stream) {
+  dim3 grid(B, (Tn + kTokens - 1) / kTokens);
+  cache_append_kernel<<<grid, kThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+      static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), cache_lens,
+      block_table, Hkv, Tn, Lmax, d, page_size, num_pages, max_pages, rope, theta, status);
   return cudaGetLastError();
 }
 

@@ -118,6 +118,16 @@ void* tensor_map_encoder();
 
 // 3-D bf16 tensor map over rows of `d` elements: dims {d, rows, planes},
 // box {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
+// Appends Tn rotated keys and values per sequence at rows cache_lens[b] + t of
+// contiguous caches [B, Hkv, Lmax, d] (block_table == nullptr) or paged caches
+// [num_pages, Hkv, page_size, d] with Lmax = max_pages * page_size.
+cudaError_t launch_cache_append_bf16(const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const int32_t* cache_lens,
+                                     const int32_t* block_table, int B, int Hkv, int Tn, int Lmax,
+                                     int d, int page_size, int num_pages, int max_pages, int rope,
+                                     const RopeTable& theta, uint32_t* status,
+                                     cudaStream_t stream);
+
 // Raises a kernel's dynamic shared-memory limit once per device (the attribute
 // lasts for the process), so repeated launches skip the driver call.
 struct SmemLimitOnce {
