@@ -138,7 +138,8 @@ int csattn_attn_fwd_ext(const void* q, const void* k, const void* v, void* out, 
 
 /*
  * Bytes of device workspace csattn_attn_bwd needs: fp32 rowsum(dout o out)
- * [B, Hq, T] plus, with RoPE, the rotated q and k (each block 256-byte aligned).
+ * [B, Hq, T] plus, with RoPE, the rotated q and k in the input dtype (each
+ * block 256-byte aligned).  0 for an unknown dtype or a size below 1.
  */
 size_t csattn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,
                                  float rope_base);
@@ -158,9 +159,11 @@ size_t csattn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype
  *   lse   fp32 [B, Hq, T] the forward's natural-log log-sum-exp (its lse output)
  *   dq [B, Hq, T, d], dk, dv [B, Hkv, T, d]  written, same dtype as q
  *   workspace  >= csattn_bwd_workspace_size() bytes, caller-owned
- * Requirements: bf16 (CSATTN_ERR_UNSUPPORTED for fp32), d in {64, 128},
- * Hq % Hkv == 0, T < 2^24 (T <= 49152 with RoPE); all pointers 16-byte aligned
- * (lse 4-byte).  Asynchronous on `stream`.
+ * Requirements: bf16 with d in {64, 128} (tcgen05 kernels) or fp32 with d in
+ * {16, 32, 64, 128} (SIMT kernels, fp32 throughout, RoPE with the accurate
+ * sine/cosine); other d CSATTN_ERR_UNSUPPORTED.  Hq % Hkv == 0, T < 2^24
+ * (T <= 49152 with RoPE); all pointers 16-byte aligned (lse 4-byte).
+ * Asynchronous on `stream`.
  */
 int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                     const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,

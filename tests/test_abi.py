@@ -253,11 +253,14 @@ def test_decode_step_rejects_invalid_arguments(lib, kw, status):
     (dict(lse=None), -1),
     (dict(T=0), -1),
     (dict(Hq=6, Hkv=4), -1),
-    (dict(dtype=0), -2),
+    (dict(dtype=7), -1),
     (dict(d=32), -2),
+    (dict(dtype=0, d=48), -2),
+    (dict(dtype=0, d=256), -2),
     (dict(causal=3), -1),
     (dict(dq=FAKE + 4), -1),
     (dict(rope_base=10000.0, T=50000), -2),
+    (dict(dtype=0, rope_base=10000.0, T=50000), -2),
     (dict(ws=None, ws_bytes=0), -5),
 ])
 def test_bwd_rejects_invalid_arguments(lib, kw, status):
@@ -278,7 +281,11 @@ def test_bwd_workspace_size(lib):
     assert lib.csattn_bwd_workspace_size(4, 32, 8, 4096, 128, 1, 0.0) == al(rows * 4)
     assert lib.csattn_bwd_workspace_size(4, 32, 8, 4096, 128, 1, 10000.0) == \
         al(rows * 4) + al(rows * 128 * 2) + al(4 * 8 * 4096 * 128 * 2)
-    assert lib.csattn_bwd_workspace_size(4, 32, 8, 4096, 128, 0, 10000.0) == 0
+    assert lib.csattn_bwd_workspace_size(4, 32, 8, 4096, 128, 0, 0.0) == al(rows * 4)
+    assert lib.csattn_bwd_workspace_size(4, 32, 8, 4096, 128, 0, 10000.0) == \
+        al(rows * 4) + al(rows * 128 * 4) + al(4 * 8 * 4096 * 128 * 4)
+    assert lib.csattn_bwd_workspace_size(4, 32, 8, 4096, 128, 7, 10000.0) == 0
+    assert lib.csattn_bwd_workspace_size(0, 32, 8, 4096, 128, 1, 10000.0) == 0
 
 
 def test_selftest_rejects_bad_limit(lib):

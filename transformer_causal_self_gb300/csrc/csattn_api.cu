@@ -273,12 +273,15 @@ int csattn_attn_fwd_ext(const void* q, const void* k, const void* v, void* out, 
 
 size_t csattn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,
                                  float rope_base) {
-  if (dtype != CSATTN_BF16 || B < 1 || Hq < 1 || Hkv < 1 || T < 1 || d < 1) return 0;
+  if ((dtype != CSATTN_BF16 && dtype != CSATTN_F32) || B < 1 || Hq < 1 || Hkv < 1 || T < 1 ||
+      d < 1)
+    return 0;
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t rows = static_cast<size_t>(B) * Hq * T;
+  const size_t esz = dtype == CSATTN_F32 ? 4 : 2;
   size_t bytes = al(rows * 4);  // rowsum(dout o out), fp32
   if (rope_base > 0.f)          // rotated q and k
-    bytes += al(rows * d * 2) + al(static_cast<size_t>(B) * Hkv * T * d * 2);
+    bytes += al(rows * d * esz) + al(static_cast<size_t>(B) * Hkv * T * d * esz);
   return bytes;
 }
 
@@ -296,10 +299,12 @@ int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out
                 Hkv, T);
   if (Hq % Hkv != 0)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: Hq=%d is not a multiple of Hkv=%d", fn, Hq, Hkv);
-  if (dtype != CSATTN_BF16)
-    return fail(dtype == CSATTN_F32 ? CSATTN_ERR_UNSUPPORTED : CSATTN_ERR_INVALID_ARG,
-                "%s: only bf16 is implemented (dtype %d)", fn, dtype);
-  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d not in {64,128}", fn, d);
+  if (dtype != CSATTN_BF16 && dtype != CSATTN_F32)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, dtype);
+  if (dtype == CSATTN_BF16 && d != 64 && d != 128)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: bf16 d=%d not in {64,128}", fn, d);
+  if (dtype == CSATTN_F32 && d != 16 && d != 32 && d != 64 && d != 128)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: fp32 d=%d not in {16,32,64,128}", fn, d);
   if (causal != 0 && causal != 1)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
   if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
@@ -349,11 +354,18 @@ int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out
   if (rc != CSATTN_OK) return rc;
   a.status = status;
   a.num_sms = num_sms;
-  if (d == 128 && tensor_map_encoder() == nullptr)
-    return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   a.qr = q;
   a.kr = k;
+  if (dtype == CSATTN_F32) {
+    void* qr = ws + al(rows * 4);
+    void* kr = static_cast<uint8_t*>(qr) + al(rows * d * 4);
+    cudaError_t e = launch_bwd_f32(a, qr, kr, st);
+    if (e != cudaSuccess) return fail_cuda(e, "attn_bwd: fp32 kernel launch");
+    return CSATTN_OK;
+  }
+  if (d == 128 && tensor_map_encoder() == nullptr)
+    return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
   if (a.rope) {
     void* qr = ws + al(rows * 4);
     void* kr = static_cast<uint8_t*>(qr) + al(rows * d * 2);

@@ -44,7 +44,7 @@ cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, in
 cudaError_t launch_fwd_sm103a(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
 cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
 
-// Backward (bf16, d in {64, 128}): dq, dk, dv of sum(out * dout).  qr, kr are the
+// Backward (bf16 d in {64, 128}; fp32 d in {16, 32, 64, 128}): dq, dk, dv of sum(out * dout).  qr, kr are the
 // rotated operands of the forward; dvec is fp32 scratch [B, Hq, Tq] for
 // rowsum(dout o out); lse is the forward's natural-log log-sum-exp.
 struct BwdArgs {
@@ -68,6 +68,10 @@ struct BwdArgs {
 };
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream);
+// fp32 backward on the SIMT cores (d in {16,32,64,128}, square T, q_off = 0).
+// a.qr, a.kr are q and k as given; with RoPE they are rotated into q_rot, k_rot
+// (fp32 scratch of q's and k's sizes) first.
+cudaError_t launch_bwd_f32(const BwdArgs& a, void* q_rot, void* k_rot, cudaStream_t stream);
 // dK, dV for d = 128 on tcgen05 (square T, q_off = 0); called by launch_bwd_bf16
 cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream);
 // dQ for d = 128 on tcgen05 (square T, q_off = 0); called by launch_bwd_bf16
