@@ -425,6 +425,8 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
 
     chunked_prefill: llama_chunk_bf16 (1024 queries after a 3072-token cache) through
     csattn_attn_fwd_ext, L2 flushed before each launch (its inputs are ~L2-sized).
+    prefill_paged: the same chunk with the cache in 256-row pages of a shuffled pool
+    (csattn_attn_prefill_paged), L2 flushed before each launch.
     rectangular: llama_cross_bf16 (1024 queries against 4096 keys, no mask), the same
     entry point, L2 flushed before each launch.
     decode_step: the decode_bf16 batch with the new token appended at row L_b - 1 and
@@ -463,7 +465,34 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
                      "kernel": "fwd_d128_kernel"}}
-    del q, k, v, k_rot, o
+    # the same chunk over a paged cache: rows 0..4095 in 256-row pages of a shuffled pool,
+    # cache_lens = 3072 (csattn_attn_prefill_paged)
+    kp, vp, table = W.page_cache(k_rot, v, [wc.Tk] * wc.B, 256, seed=12)
+    clen = torch.full((wc.B,), wc.q_offset, dtype=torch.int32, device=dev)
+    ts = []
+    for i in range(3 + reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csattn.attn_prefill_paged(q, kp, vp, table, clen, o, causal=True, rope_base=wc.rope_base,
+                                  scale=wc.scale, stream=stream)
+        e1.record(stream)
+        if i >= 3:
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    csattn.check_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    tf = wc.flops() / (ms * 1e-3) / 1e12
+    out["prefill_paged"] = {
+        "workload": "llama_chunk_bf16 (B=4, Hq=32, Hkv=8, Tq=1024 after 3072 cached rows, "
+                    "d=128, RoPE 1e4) with the rotated K/V cache in 256-row pages of a "
+                    "shuffled pool",
+        "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+        "flops": wc.flops(), "l2": "flushed before each launch",
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
+                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                     "kernel": "fwd_d128_kernel (paged K/V)"}}
+    del q, k, v, k_rot, o, kp, vp, table, clen
 
     # rectangular, unmasked (cross-attention shaped): 1024 queries x 4096 keys per head
     wx = W.WORKLOADS["llama_cross_bf16"]

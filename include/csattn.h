@@ -300,6 +300,34 @@ int csattn_attn_decode_noalloc(const void* q, const void* k_cache, const void* v
                                int num_splits, void* stream);
 
 /*
+ * Prefill of a chunk over a paged KV cache (chunked prefill, "The Transformer
+ * architecture", "Hands-on": the query at position p sees the cached keys 0..p;
+ * the cache stored in fixed-size pages as for csattn_attn_decode_paged).  The
+ * chunk's own keys and values are in the cache already (csattn_cache_append_paged
+ * with the same cache_lens writes them).  For sequence b with L = cache_lens[b],
+ * query row i sits at position L + i and, causally, sees cache rows 0..L + i
+ * (all L + Tq rows with causal = 0).
+ *   q          [B, Hq, Tq, d] bf16, not rotated (RoPE at positions L + i)
+ *   k_pages, v_pages [num_pages, Hkv, page_size, d] bf16, keys already rotated
+ *   block_table device int32 [B, max_pages]; cache_lens device int32 [B]
+ *   out        [B, Hq, Tq, d] bf16;  lse NULL or fp32 [B, Hq, Tq] (natural log)
+ *   rope_base, rope_layout, scale  as csattn_attn_fwd (applied to q only)
+ * Requirements: bf16, d = 128, Hq % Hkv == 0, page_size a multiple of 64 in
+ * [64, 65536], 1 <= Tq <= max_pages * page_size < 2^24 (<= 49152 with RoPE);
+ * q, pages and out 16-byte aligned, block_table, cache_lens and lse 4-byte.
+ * Device-side errors (CSATTN_ERR_DEVICE_ARG in the status word): a cache_lens[b]
+ * outside [0, max_pages * page_size - Tq] (that sequence then runs as if L = 0),
+ * a page index outside [0, num_pages) for a row < L + Tq (those rows read as
+ * zeros).  Cache rows at or past L + Tq are never used, whatever they hold.
+ * Asynchronous on `stream`; no workspace.
+ */
+int csattn_attn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, const int32_t* cache_lens, void* out,
+                              int B, int Hq, int Hkv, int Tq, int page_size, int num_pages,
+                              int max_pages, int d, int dtype, int causal, float rope_base,
+                              int rope_layout, float scale, float* lse, void* stream);
+
+/*
  * Appends Tn tokens per sequence to the KV caches (a prefill chunk written into
  * the cache, "The Transformer architecture", "Hands-on": the cache grows a row per
  * token and a token's key is rotated at its position).  For sequence b and

@@ -50,7 +50,7 @@ __all__ = [
     "round_to_bf16", "expand_kv_heads", "causal_additive_mask", "attention_scores",
     "attention", "attention_rows", "attention_lse", "attention_backward", "decode",
     "decode_paged", "decode_step", "merge_partials", "split_partials", "rope_rotate_transpose",
-    "cache_append", "cache_append_paged"]
+    "cache_append", "cache_append_paged", "prefill_paged"]
 
 _BF16_MAX = float.fromhex("0x1.fep127")
 
@@ -363,6 +363,42 @@ def cache_append_paged(k_new, v_new, k_pages, v_pages, block_table, cache_lens, 
             kp[page, :, off] = kr[:, t]
             vp[page, :, off] = v_new[b, :, t]
     return kp, vp
+
+
+def prefill_paged(q, k_pages, v_pages, block_table, cache_lens, page_size: int, *, causal=True,
+                  rope_base=0.0, scale=None, rope_layout="split_half", operand_dtype=None,
+                  lse=False):
+    """Chunk prefill over a paged cache of rotated keys ("The Transformer
+    architecture", "Hands-on"): for sequence b with L = cache_lens[b], cache rows
+    0..L+Tq-1 (the prefix, then the chunk's own rows) are gathered from the pages
+    (row t in page block_table[b][t // page_size] at offset t % page_size); query
+    i is rotated at position L + i (rounded to ``operand_dtype``), the keys are used
+    as stored, and the attention definition with that query offset applies.
+    Returns out [B, Hq, Tq, d] (and the natural-log lse [B, Hq, Tq] with lse=True).
+    """
+    q = np.asarray(_as_np(q), dtype=np.float64)
+    kp = np.asarray(_as_np(k_pages), dtype=np.float64)
+    vp = np.asarray(_as_np(v_pages), dtype=np.float64)
+    bt = np.asarray(_as_np(block_table)).astype(np.int64)
+    lens = [int(x) for x in np.asarray(_as_np(cache_lens)).reshape(-1)]
+    B, Hq, Tq, d = q.shape
+    Hkv = kp.shape[1]
+    out = np.empty((B, Hq, Tq, vp.shape[-1]), dtype=np.float64)
+    lses = np.empty((B, Hq, Tq), dtype=np.float64)
+    for b, L in enumerate(lens):
+        Tk = L + Tq
+        kc = np.empty((1, Hkv, Tk, d))
+        vc = np.empty((1, Hkv, Tk, vp.shape[-1]))
+        for t in range(Tk):
+            page, off = bt[b, t // page_size], t % page_size
+            kc[0, :, t] = kp[page, :, off]
+            vc[0, :, t] = vp[page, :, off]
+        qr = _rotated(q[b:b + 1], rope_base, rope_layout, operand_dtype, L + np.arange(Tq))
+        out[b] = attention(qr, kc, vc, causal=causal, rope_base=0.0, scale=scale, q_offset=L)[0]
+        if lse:
+            lses[b] = attention_lse(qr, kc, causal=causal, rope_base=0.0, scale=scale,
+                                    q_offset=L)[0]
+    return (out, lses) if lse else out
 
 
 def rope_rotate_transpose(x, positions, base: float, layout: str = "split_half"):

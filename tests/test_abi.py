@@ -184,6 +184,42 @@ def test_decode_paged_rejects_invalid_arguments(lib, kw, status):
 
 
 @pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1),
+    (dict(table=None), -1),
+    (dict(lens=None), -1),
+    (dict(Tq=0), -1),
+    (dict(Hq=6, Hkv=4), -1),
+    (dict(dtype=0), -2),
+    (dict(dtype=4), -1),
+    (dict(d=64), -2),
+    (dict(causal=2), -1),
+    (dict(rope_layout=0x100), -1),
+    (dict(page_size=96), -1),
+    (dict(page_size=32), -1),
+    (dict(num_pages=0), -1),
+    (dict(max_pages=0), -1),
+    (dict(Tq=600, max_pages=4, page_size=128), -1),
+    (dict(max_pages=1 << 17, page_size=128), -2),
+    (dict(rope_base=10000.0, max_pages=400, page_size=128), -2),
+    (dict(lens=FAKE + 2), -1),
+    (dict(lse=FAKE + 2), -1),
+    (dict(out=FAKE + 8), -1),
+])
+def test_prefill_paged_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, table=FAKE, lens=FAKE, out=FAKE, B=2, Hq=8, Hkv=2, Tq=256,
+             page_size=128, num_pages=16, max_pages=4, d=128, dtype=1, causal=1, rope_base=0.0,
+             rope_layout=0, scale=0.0, lse=None)
+    a.update(kw)
+    rc = lib.csattn_attn_prefill_paged(a["q"], a["k"], a["v"], a["table"], a["lens"], a["out"],
+                                       a["B"], a["Hq"], a["Hkv"], a["Tq"], a["page_size"],
+                                       a["num_pages"], a["max_pages"], a["d"], a["dtype"],
+                                       a["causal"], a["rope_base"], a["rope_layout"], a["scale"],
+                                       a["lse"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"attn_prefill_paged" in lib.csattn_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
     (dict(k_new=None), -1),
     (dict(lens=FAKE + 2), -1),
     (dict(Tn=0), -1),

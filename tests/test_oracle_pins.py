@@ -263,6 +263,38 @@ def pin_cache_append_paged_equals_contiguous(o):
             assert np.array_equal(vp2[table[b, r // page], :, r % page], vc2[b, :, r])
 
 
+def pin_prefill_paged_equals_chunk(o):
+    """A chunk over a paged cache of rotated keys (shuffled pages, NaN in every row
+    past a sequence's end) equals the chunk of the contiguous definition: query i at
+    position L_b + i over keys 0..L_b + i, per sequence, RoPE on both sides."""
+    B, Hq, Hkv, d, Tq, page, n_lp = 3, 4, 2, 8, 4, 4, 5
+    lens = [0, 5, 11]
+    q = _rand((B, Hq, Tq, d), 370)
+    k = _rand((B, Hkv, n_lp * page, d), 371)
+    v = _rand((B, Hkv, n_lp * page, d), 372)
+    kr = o.round_to_bf16(o.rope_rotate(k, np.arange(n_lp * page), 10000.0))
+    perm = np.random.default_rng(373).permutation(B * n_lp + 2)
+    table = perm[:B * n_lp].reshape(B, n_lp)
+    kp = np.full((B * n_lp + 2, Hkv, page, d), np.nan)
+    vp = np.full((B * n_lp + 2, Hkv, page, d), np.nan)
+    for b, L in enumerate(lens):
+        for t in range(L + Tq):
+            kp[table[b, t // page], :, t % page] = kr[b, :, t]
+            vp[table[b, t // page], :, t % page] = v[b, :, t]
+    for causal in (True, False):
+        got, got_lse = o.prefill_paged(q, kp, vp, table, lens, page, causal=causal,
+                                       rope_base=10000.0, operand_dtype="bf16", lse=True)
+        assert got.shape == (B, Hq, Tq, d)
+        for b, L in enumerate(lens):
+            sl = slice(0, L + Tq)
+            want = o.attention(q[b:b + 1], k[b:b + 1, :, sl], v[b:b + 1, :, sl], causal=causal,
+                               rope_base=10000.0, operand_dtype="bf16", q_offset=L)
+            assert np.max(np.abs(got[b] - want[0])) < 1e-12, (causal, b)
+            want_lse = o.attention_lse(q[b:b + 1], k[b:b + 1, :, sl], causal=causal,
+                                       rope_base=10000.0, operand_dtype="bf16", q_offset=L)
+            assert np.max(np.abs(got_lse[b] - want_lse[0])) < 1e-12, (causal, b)
+
+
 def pin_degenerate_cases(o):
     q = _rand((1, 2, 1, 8), 90)
     k = _rand((1, 2, 1, 8), 91)
@@ -543,7 +575,8 @@ ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exa
             pin_decode_step_appends_then_attends, pin_backward_finite_differences,
             pin_backward_autograd, pin_rope_transpose_inverts,
             pin_decode_paged_equals_contiguous, pin_value_width, pin_cache_append_positions,
-            pin_cache_append_matches_decode_step, pin_cache_append_paged_equals_contiguous]
+            pin_cache_append_matches_decode_step, pin_cache_append_paged_equals_contiguous,
+            pin_prefill_paged_equals_chunk]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -880,3 +913,22 @@ def test_planted_paged_append_offset_swapped():
                 vp[page, :, off] = vn[b, :, t]
         return kp, vp
     assert _fails(_Mutant(cache_append_paged=bad), [pin_cache_append_paged_equals_contiguous])
+
+
+def test_planted_paged_prefill_positions_ignore_prefix():
+    """Queries rotated at i instead of cache_lens[b] + i in the paged prefill fail a pin."""
+    def bad(q, k_pages, v_pages, block_table, cache_lens, page_size, *, causal=True,
+            rope_base=0.0, scale=None, rope_layout="split_half", operand_dtype=None, lse=False):
+        qz = np.asarray(q, np.float64)
+        Tq = qz.shape[2]
+        res = []
+        for b, L in enumerate(cache_lens):
+            qr = OA.round_to(OA.rope_rotate(qz[b:b + 1], np.arange(Tq), rope_base, rope_layout),
+                             operand_dtype)
+            o_b = OA.prefill_paged(qr, k_pages, v_pages, block_table[b:b + 1], [L], page_size,
+                                   causal=causal, rope_base=0.0, scale=scale, lse=lse)
+            res.append(o_b)
+        if lse:
+            return (np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res]))
+        return np.concatenate(res)
+    assert _fails(_Mutant(prefill_paged=bad), [pin_prefill_paged_equals_chunk])

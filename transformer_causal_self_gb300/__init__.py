@@ -55,6 +55,8 @@ _SIGNATURES = {
                                                                     _vp]),
     "csattn_attn_decode_paged": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _c_int, _c_int, _vp,
                                                                     _c_size, _vp]),
+    "csattn_attn_prefill_paged": (_c_int, [_vp] * 6 + [_c_int] * 10 + [_c_float, _c_int, _c_float,
+                                                                     _vp, _vp]),
     "csattn_cache_append": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _vp]),
     "csattn_cache_append_paged": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _c_int, _vp]),
     "csattn_check_status": (_c_int, [_vp]),
@@ -354,6 +356,38 @@ def attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Ten
                                         _dtype_code(q), float(scale), int(max_seq_len),
                                         int(num_splits), workspace.data_ptr(), workspace.numel(),
                                         _stream_handle(stream)))
+    return out
+
+
+def attn_prefill_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                       block_table: torch.Tensor, cache_lens: torch.Tensor,
+                       out: Optional[torch.Tensor] = None, *, causal: bool = True,
+                       rope_base: float = 0.0, scale: float = 0.0,
+                       rope_layout: str = "split_half", lse: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """Chunk prefill over a paged cache (C: csattn_attn_prefill_paged).
+
+    q [B,Hq,Tq,d] (not rotated; row i of sequence b sits at cache_lens[b] + i);
+    k_pages/v_pages [num_pages,Hkv,page_size,d] holding rotated keys, the chunk's own
+    rows included; block_table int32 [B,max_pages] and cache_lens int32 [B] on the device.
+    """
+    _need_cuda(q, k_pages, v_pages, block_table, cache_lens)
+    if block_table.dtype != torch.int32 or cache_lens.dtype != torch.int32:
+        raise TypeError("block_table and cache_lens must be int32")
+    B, Hq, Tq, d = q.shape
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    max_pages = block_table.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda(out)
+    lib = load_library()
+    _check(lib.csattn_attn_prefill_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                         block_table.data_ptr(), cache_lens.data_ptr(),
+                                         out.data_ptr(), B, Hq, Hkv, Tq, page_size, num_pages,
+                                         max_pages, d, _dtype_code(q), int(bool(causal)),
+                                         float(rope_base), _ROPE_LAYOUT[rope_layout],
+                                         float(scale), lse.data_ptr() if lse is not None else None,
+                                         _stream_handle(stream)))
     return out
 
 

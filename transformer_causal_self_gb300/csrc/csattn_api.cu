@@ -555,6 +555,89 @@ int csattn_attn_decode_paged(const void* q, const void* k_pages, const void* v_p
                      block_table, page_size, num_pages, max_pages);
 }
 
+int csattn_attn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, const int32_t* cache_lens, void* out,
+                              int B, int Hq, int Hkv, int Tq, int page_size, int num_pages,
+                              int max_pages, int d, int dtype, int causal, float rope_base,
+                              int rope_layout, float scale, float* lse, void* stream) {
+  const char* fn = "attn_prefill_paged";
+  if (q == nullptr || k_pages == nullptr || v_pages == nullptr || block_table == nullptr ||
+      cache_lens == nullptr || out == nullptr)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: null pointer argument", fn);
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: B=%d Hq=%d Hkv=%d Tq=%d must be >= 1", fn, B, Hq,
+                Hkv, Tq);
+  if (Hq % Hkv != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: Hq=%d is not a multiple of Hkv=%d", fn, Hq, Hkv);
+  if (dtype != CSATTN_BF16)
+    return fail(dtype == CSATTN_F32 ? CSATTN_ERR_UNSUPPORTED : CSATTN_ERR_INVALID_ARG,
+                "%s: only bf16 is implemented (dtype %d)", fn, dtype);
+  if (d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d (only 128)", fn, d);
+  if (causal != 0 && causal != 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
+  if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown rope_layout %d", fn, rope_layout);
+  if (!std::isfinite(rope_base) || !std::isfinite(scale))
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: rope_base and scale must be finite", fn);
+  if (page_size < 64 || page_size % 64 != 0 || page_size > 65536)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: page_size=%d must be a multiple of 64 in [64, 65536]",
+                fn, page_size);
+  if (num_pages < 1 || max_pages < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: num_pages=%d and max_pages=%d must be >= 1", fn,
+                num_pages, max_pages);
+  if (static_cast<long long>(num_pages) * Hkv > (1LL << 31) - 1)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: num_pages * Hkv too large", fn);
+  const long long lmax = static_cast<long long>(max_pages) * page_size;
+  if (lmax >= (1 << 24))
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: max_pages * page_size must be < 2^24", fn);
+  if (Tq > lmax)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: Tq=%d exceeds max_pages * page_size = %lld", fn, Tq,
+                lmax);
+  if (rope_base > 0.f && lmax > kMaxRopePositions)
+    return fail(CSATTN_ERR_UNSUPPORTED,
+                "%s: RoPE supports positions < %d (max_pages * page_size = %lld)", fn,
+                kMaxRopePositions, lmax);
+  if (static_cast<long long>(B) * Hq > (1LL << 31) - 1)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: B*Hq too large", fn);
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+
+  FwdArgs a{};
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.out = out;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.dv = d;
+  a.Tq = Tq;
+  a.Tk = Tq;
+  a.q_off = 0;
+  a.causal = causal;
+  a.rope = rope_base > 0.f ? (rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2) : 0;
+  a.rope_k = 0;  // the cache holds rotated keys
+  a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  if (a.rope) rope_table(&a.theta, d, static_cast<double>(rope_base));
+  a.cache_lens = cache_lens;
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages;
+  int rc = device_info(&a.status, &a.num_sms);
+  if (rc != CSATTN_OK) return rc;
+  if (tensor_map_encoder() == nullptr)
+    return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
+  cudaError_t e = launch_fwd_sm103a_d128(a, k_pages, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "attn_prefill_paged: kernel launch");
+  return CSATTN_OK;
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 size_t csattn_decode_step_workspace_size(int B, int Hq, int Lmax, int d, int num_splits) {

@@ -182,10 +182,12 @@ __device__ __forceinline__ bool bar_or_wg(int id, bool pred) {
 }
 
 // O^T += V^T P for 128 keys: eight MMAs, M=128 (d), N=256 (queries), K=16
+template <bool LIMITED = false>
 __device__ __forceinline__ void issue_pvt(uint32_t d_tmem, uint32_t v_smem, uint32_t p_smem,
-                                          bool accumulate) {
+                                          bool accumulate, int k_steps = BN / 16) {
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
+    if (LIMITED && kk >= k_steps) break;
     const uint64_t a = smem_desc_sw128(v_smem + 2048u * kk, BM * 128, 1024);
     const uint64_t b = smem_desc_sw128(
         p_smem + static_cast<uint32_t>((kk >> 2) * (2 * BM * 128) + (kk & 3) * 32), 16, 1024);
@@ -194,7 +196,8 @@ __device__ __forceinline__ void issue_pvt(uint32_t d_tmem, uint32_t v_smem, uint
 }
 
 // DK: head size of q and k (64 or 128); v and out have D = 128 channels.
-template <int DK>
+// PAGED: K/V from a paged cache with per-sequence lengths (see Params).
+template <int DK, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_d128_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t nq[2] = {0, 0};
       bool ok = true;
       // one K (DK channels) or V (D channels) tile into the next ring stage
-      auto load = [&](const CUtensorMap* m, int width, int j, int z) {
+      auto load = [&](const CUtensorMap* m, int width, int j, const Unit& un) {
         const uint32_t s = fill % NS, use = fill / NS;
         if (use > 0 && !mbar_wait(&kv_empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) {
           ok = false;
@@ -276,19 +279,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(&kv_full[s], static_cast<uint32_t>(BN * width * 2));
         uint8_t* dst = sKV + s * TILE_BYTES;
-        for (int kb = 0; kb < width / 64; ++kb)
-          tma_load_3d(dst + kb * BLOCK_BYTES, m, &kv_full[s], kb * 64, j * BN, z);
+        if constexpr (!PAGED) {
+          const int z = un.b * p.Hkv + un.kvh;
+          for (int kb = 0; kb < width / 64; ++kb)
+            tma_load_3d(dst + kb * BLOCK_BYTES, m, &kv_full[s], kb * 64, j * BN, z);
+        } else {
+          // paged: a box of box_rows rows never crosses a page; a box past the
+          // sequence, or a page index outside the pool (reported), reads zeros (its
+          // plane coordinate is past the tensor map)
+          for (int r0 = 0; r0 < BN; r0 += p.box_rows) {
+            const int t = j * BN + r0;
+            int plane = p.num_pages * p.Hkv, prow = 0;
+            if (t < un.Tk) {
+              const int page = p.block_table[static_cast<size_t>(un.b) * p.max_pages +
+                                             t / p.page_size];
+              if (page >= 0 && page < p.num_pages)
+                plane = page * p.Hkv + un.kvh;
+              else
+                atomicOr(p.status, kStatusDeviceArg);
+              prow = t % p.page_size;
+            }
+            for (int kb = 0; kb < width / 64; ++kb)
+              tma_load_3d(dst + kb * BLOCK_BYTES + r0 * 128, m, &kv_full[s], kb * 64, prow,
+                          plane);
+          }
+        }
         ++fill;
       };
       for (int i = 0; ok; ++i) {
         const int u = unit_index(i);
         if (u >= p.nUnits) break;
-        const Unit un = decode_unit(p, u);
+        const Unit un = decode_unit<PAGED>(p, u);
         {
           // the next unit's Q tiles go to L2 now; their loads at the end of this unit hit it
           const int u2 = unit_index(i + 1);
           if (u2 < p.nUnits) {
-            const Unit un2 = decode_unit(p, u2);
+            const Unit un2 = decode_unit<PAGED>(p, u2);
             for (int x = 0; x < 2; ++x)
               if (un2.n[x] > 0)
                 for (int kb = 0; kb < DK / 64; ++kb)
@@ -311,13 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (PAGED && un.bad_len) atomicOr(p.status, kStatusDeviceArg);
         // K leads V by one tile: K_0, then (K_{j+1}, V_j) for each j
         const int n = un.n[1];
-        const int z = un.b * p.Hkv + un.kvh;
-        if (ok) load(&tm_k, DK, 0, z);
+        if (ok) load(&tm_k, DK, 0, un);
         for (int j = 0; j < n && ok; ++j) {
-          if (j + 1 < n) load(&tm_k, DK, j + 1, z);
-          if (ok) load(&tm_v, D, j, z);
+          if (j + 1 < n) load(&tm_k, DK, j + 1, un);
+          if (ok) load(&tm_v, D, j, un);
         }
       }
       if (*abort_flag) {
@@ -348,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok; ++i) {
         const int u = unit_index(i);
         if (u >= p.nUnits) break;
-        const Unit un = decode_unit(p, u);
+        const Unit un = decode_unit<PAGED>(p, u);
         const int n = un.n[1];
         // S(0) for both tiles (an absent tile A still runs: its rows are masked to P = 0)
         const uint32_t fK0 = fill++;
@@ -393,7 +419,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait(p_full, cp & 1)) break;
           ++cp;
           if (j == 0 && units > 0 && !wait(o_empty, (units - 1) & 1)) break;
-          issue_pvt(tO, stage(fV), sP0, j > 0);
+          int k_steps = BN / 16;
+          if (PAGED && (j + 1) * BN > un.Tk) {
+            // paged cache rows past the sequence may hold anything (NaN included) and
+            // P = 0 there would not cancel them: skip the 16-key steps past the end and
+            // zero the rows of the last step that lie past it
+            const int nvalid = un.Tk - j * BN;  // 1..BN-1
+            k_steps = (nvalid + 15) / 16;
+            uint8_t* vt = sKV + (fV % NS) * TILE_BYTES;
+            for (int kb = 0; kb < D / 64; ++kb)
+              for (int r = nvalid; r < 16 * k_steps; ++r)
+                for (int c = 0; c < 8; ++c)
+                  *reinterpret_cast<uint4*>(vt + kb * BLOCK_BYTES + r * 128 + c * 16) =
+                      make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+          }
+          issue_pvt<PAGED>(tO, stage(fV), sP0, j > 0, k_steps);
           tc_commit(pv_done);
           tc_commit(&kv_empty[fV % NS]);
         }
@@ -428,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i2 = i_from;; ++i2) {
         const int u2 = unit_index(i2);
         if (u2 >= p.nUnits) return;
-        const Unit un2 = decode_unit(p, u2);
+        const Unit un2 = decode_unit<PAGED>(p, u2);
         const bool shared_pos = un2.n[0] > 0 && un2.q0[0] == un2.q0[1];
         if (shared_pos) {
           if (fail || !warp_wait(&q_full[0], cqa & 1, abort_flag, p.status, kWaitNs) ||
@@ -439,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++cqa;
           ++cqb;
           if (p.rope) {
-            rotate_chunks<DK>(sQ[0], sQ[1], row, p.q_off + un2.q0[0] + row, p.rope, p.theta,
+            rotate_chunks<DK>(sQ[0], sQ[1], row, (PAGED ? un2.q_off : p.q_off) + un2.q0[0] + row, p.rope, p.theta,
                               x * (DK / 32), (x + 1) * (DK / 32));
             fence_proxy_async_smem();
           }
@@ -460,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++cq;
         if (p.rope) {
-          rotate_chunks<DK>(x ? sQ[1] : sQ[0], nullptr, row, p.q_off + (x ? un2.q0[1] : un2.q0[0]) + row,
+          rotate_chunks<DK>(x ? sQ[1] : sQ[0], nullptr, row, (PAGED ? un2.q_off : p.q_off) + (x ? un2.q0[1] : un2.q0[0]) + row,
                         p.rope, p.theta,
                         0, DK / 16);
           fence_proxy_async_smem();
@@ -479,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0;; ++i) {
       const int u = unit_index(i);
       if (u >= p.nUnits) break;
-      const Unit un = decode_unit(p, u);
+      const Unit un = decode_unit<PAGED>(p, u);
       const int n = un.n[1];                       // both tiles step through tile B's keys
       const bool present = (x ? un.n[1] : un.n[0]) > 0;
       const int hx = x ? un.h[1] : un.h[0];
@@ -506,8 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_free[x]);
           int lim = BN - 1;
-          if (p.causal) lim = min(lim, p.q_off + qpos - j * BN);
-          lim = min(lim, p.Tk - 1 - j * BN);
+          if (p.causal) lim = min(lim, (PAGED ? un.q_off : p.q_off) + qpos - j * BN);
+          lim = min(lim, (PAGED ? un.Tk : p.Tk) - 1 - j * BN);
           if (!present) lim = -1;
           if (lim < BN - 1) {
 #pragma unroll
@@ -664,20 +705,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DK>
+template <int DK, bool PAGED>
 cudaError_t launch_dk(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
   const Params p = make_params(a);
   alignas(64) CUtensorMap tq, tk, tv, to;
+  // K/V tensor maps: [B*Hkv planes, Tk rows], or the page pool [num_pages*Hkv, page_size]
+  const bool paged = a.block_table != nullptr;
+  const int kv_rows = paged ? a.page_size : a.Tk;
+  const int kv_planes = paged ? a.num_pages * a.Hkv : a.B * a.Hkv;
   if (!make_tmap_bf16_3d(&tq, a.q, DK, a.Tq, a.B * a.Hq, BM) ||
-      !make_tmap_bf16_3d(&tk, k_eff, DK, a.Tk, a.B * a.Hkv, BN) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BN) ||
+      !make_tmap_bf16_3d(&tk, k_eff, DK, kv_rows, kv_planes, p.box_rows) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, kv_rows, kv_planes, p.box_rows) ||
       !make_tmap_bf16_3d(&to, a.out, D, a.Tq, a.B * a.Hq, BM))
     return cudaErrorInvalidValue;
   static SmemLimitOnce smem_limit;
-  cudaError_t e = smem_limit.set(fwd_d128_kernel<DK>, SMEM_BYTES);
+  cudaError_t e = smem_limit.set(fwd_d128_kernel<DK, PAGED>, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = p.nUnits < a.num_sms ? p.nUnits : a.num_sms;
-  fwd_d128_kernel<DK><<<grid, kThreads, SMEM_BYTES, stream>>>(p, tq, tk, tv, to);
+  fwd_d128_kernel<DK, PAGED><<<grid, kThreads, SMEM_BYTES, stream>>>(p, tq, tk, tv, to);
   return cudaGetLastError();
 }
 
@@ -685,8 +730,10 @@ cudaError_t launch_dk(const FwdArgs& a, const void* k_eff, cudaStream_t stream) 
 
 // v and out with 128 channels; q and k with a.d = 64 or 128
 cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
-  if (a.d == 128) return launch_dk<128>(a, k_eff, stream);
-  if (a.d == 64) return launch_dk<64>(a, k_eff, stream);
+  if (a.block_table != nullptr)
+    return a.d == 128 ? launch_dk<128, true>(a, k_eff, stream) : cudaErrorInvalidValue;
+  if (a.d == 128) return launch_dk<128, false>(a, k_eff, stream);
+  if (a.d == 64) return launch_dk<64, false>(a, k_eff, stream);
   return cudaErrorInvalidValue;
 }
 

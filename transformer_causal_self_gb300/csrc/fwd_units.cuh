@@ -43,21 +43,52 @@ struct Params {
   int nUnits;   // all units
   float scale_log2;
   RopeTable theta;
+  // Paged KV cache (d = 128 kernel only; block_table == nullptr otherwise): keys and
+  // values of sequence b at rows 0..L_b+Tq-1 with L_b = cache_lens[b] (the cached
+  // prefix, then the chunk's own rows); row t lives in page block_table[b * max_pages
+  // + t / page_size] at offset t % page_size; K/V tensor maps span the page pool
+  // with planes page * Hkv + kv head.  Query row i of sequence b sits at L_b + i.
+  const int32_t* cache_lens;
+  const int32_t* block_table;
+  int page_size, num_pages, max_pages;
+  int box_rows;  // rows per K/V TMA box: 128, or 64 when page_size is an odd multiple of 64
 };
 
 struct Unit {
   int b, kvh;
   int h[2], q0[2], n[2];  // per tile: head, first row, number of key tiles (n[0] <= n[1])
+  int q_off, Tk;          // position of query row 0 and key rows of this sequence
+  bool bad_len;           // paged: cache_lens[b] out of range (run as L_b = 0, reported)
 };
 
 // Key tiles query tile qt reads: all of them, or (causal) up to the tile that holds
 // the position of its last row.  Never 0 (key 0 is visible to every query).
-__device__ __forceinline__ int key_tiles(const Params& p, int qt) {
-  if (!p.causal) return p.n_kt;
-  const int last = min(qt * BM + BM, p.Tq) - 1 + p.q_off;
-  return min(p.n_kt, last / BN + 1);
+__device__ __forceinline__ int key_tiles(const Params& p, int qt, int q_off, int n_kt) {
+  if (!p.causal) return n_kt;
+  const int last = min(qt * BM + BM, p.Tq) - 1 + q_off;
+  return min(n_kt, last / BN + 1);
 }
 
+// Position of query row 0 and key count of sequence b: the call's, or from the
+// paged cache's lengths (a length outside [0, max_pages * page_size - Tq] runs as 0).
+template <bool PAGED>
+__device__ __forceinline__ void seq_extent(const Params& p, Unit& r) {
+  r.q_off = p.q_off;
+  r.Tk = p.Tk;
+  r.bad_len = false;
+  if constexpr (PAGED) {
+    int L = p.cache_lens[r.b];
+    if (L < 0 || L > p.max_pages * p.page_size - p.Tq) {
+      r.bad_len = true;
+      L = 0;
+    }
+    r.q_off = L;
+    r.Tk = L + p.Tq;
+  }
+}
+
+// PAGED: per-sequence extents from the paged cache's lengths; otherwise the call's.
+template <bool PAGED = false>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   Unit r;
   if (u < p.nP) {
@@ -72,7 +103,8 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     r.h[0] = r.kvh * p.rep + 2 * pp;
     r.h[1] = r.h[0] + 1;
     r.q0[0] = r.q0[1] = qt * BM;
-    r.n[0] = r.n[1] = key_tiles(p, qt);
+    seq_extent<PAGED>(p, r);
+    r.n[0] = r.n[1] = key_tiles(p, qt, r.q_off, PAGED ? (r.Tk + BN - 1) / BN : p.n_kt);
   } else {
     const int u2 = u - p.nP;
     const int npairs = (p.n_qt + 1) / 2;
@@ -83,17 +115,18 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     r.b = rem / p.Hkv;
     r.kvh = rem - r.b * p.Hkv;
     r.h[0] = r.h[1] = r.kvh * p.rep + p.rep - 1;
+    seq_extent<PAGED>(p, r);
     const int t0 = 2 * m, t1 = 2 * m + 1;
     if (t1 < p.n_qt) {
       r.q0[0] = t0 * BM;
-      r.n[0] = key_tiles(p, t0);
+      r.n[0] = key_tiles(p, t0, r.q_off, PAGED ? (r.Tk + BN - 1) / BN : p.n_kt);
       r.q0[1] = t1 * BM;
-      r.n[1] = key_tiles(p, t1);
+      r.n[1] = key_tiles(p, t1, r.q_off, PAGED ? (r.Tk + BN - 1) / BN : p.n_kt);
     } else {
       r.q0[0] = 0;
       r.n[0] = 0;
       r.q0[1] = t0 * BM;
-      r.n[1] = key_tiles(p, t0);
+      r.n[1] = key_tiles(p, t0, r.q_off, PAGED ? (r.Tk + BN - 1) / BN : p.n_kt);
     }
   }
   return r;
@@ -224,6 +257,12 @@ inline Params make_params(const FwdArgs& a) {
   p.nUnits = p.nP + nC;
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   p.theta = a.theta;
+  p.cache_lens = a.block_table != nullptr ? a.cache_lens : nullptr;
+  p.block_table = a.block_table;
+  p.page_size = a.page_size;
+  p.num_pages = a.num_pages;
+  p.max_pages = a.max_pages;
+  p.box_rows = (a.block_table != nullptr && a.page_size % BN != 0) ? 64 : BN;
   return p;
 }
 

@@ -29,6 +29,13 @@ struct FwdArgs {
   RopeTable theta;   // valid when rope != 0
   uint32_t* status;  // device status word
   int num_sms;
+  // Paged K/V (bf16, d = dv = 128; block_table == nullptr: k, v are [B, Hkv, Tk, d]).
+  // k, v are pools [num_pages, Hkv, page_size, d] of rotated keys and values; sequence
+  // b has cache_lens[b] + Tq rows (Tk and q_off unused), its query row i sits at
+  // cache_lens[b] + i; page_size is a multiple of 64.
+  const int32_t* cache_lens;
+  const int32_t* block_table;
+  int page_size, num_pages, max_pages;
 };
 
 // fp32 SIMT path (d and dv each in {16,32,64,128}).
