@@ -195,6 +195,23 @@ __device__ __forceinline__ void issue_pvt(uint32_t d_tmem, uint32_t v_smem, uint
   }
 }
 
+// O^T += V^T P^T for a paged sequence's last key tile, whose rows past the end
+// (nvalid..BN-1) may hold anything, NaN included, which P = 0 would not cancel:
+// the 16-key steps past the end are skipped and the rows of the last step that lie
+// past it are zeroed first.  Kept out of line so that the MMA thread's loop stays as
+// compact as the contiguous kernel's (inlined, it cost the paged kernel 3 %).
+__device__ __noinline__ void pvt_tail(uint32_t d_tmem, uint32_t v_smem, uint8_t* v_tile,
+                                      uint32_t p_smem, bool accumulate, int nvalid) {
+  const int k_steps = (nvalid + 15) / 16;
+  for (int kb = 0; kb < D / 64; ++kb)
+    for (int r = nvalid; r < 16 * k_steps; ++r)
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(v_tile + kb * BLOCK_BYTES + r * 128 + c * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  issue_pvt<true>(d_tmem, v_smem, p_smem, accumulate, k_steps);
+}
+
 // DK: head size of q and k (64 or 128); v and out have D = 128 channels.
 // PAGED: K/V from a paged cache with per-sequence lengths (see Params).
 template <int DK, bool PAGED>
@@ -419,22 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait(p_full, cp & 1)) break;
           ++cp;
           if (j == 0 && units > 0 && !wait(o_empty, (units - 1) & 1)) break;
-          int k_steps = BN / 16;
-          if (PAGED && (j + 1) * BN > un.Tk) {
-            // paged cache rows past the sequence may hold anything (NaN included) and
-            // P = 0 there would not cancel them: skip the 16-key steps past the end and
-            // zero the rows of the last step that lie past it
-            const int nvalid = un.Tk - j * BN;  // 1..BN-1
-            k_steps = (nvalid + 15) / 16;
-            uint8_t* vt = sKV + (fV % NS) * TILE_BYTES;
-            for (int kb = 0; kb < D / 64; ++kb)
-              for (int r = nvalid; r < 16 * k_steps; ++r)
-                for (int c = 0; c < 8; ++c)
-                  *reinterpret_cast<uint4*>(vt + kb * BLOCK_BYTES + r * 128 + c * 16) =
-                      make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async_smem();
-          }
-          issue_pvt<PAGED>(tO, stage(fV), sP0, j > 0, k_steps);
+          if (PAGED && (j + 1) * BN > un.Tk)
+            pvt_tail(tO, stage(fV), sKV + (fV % NS) * TILE_BYTES, sP0, j > 0, un.Tk - j * BN);
+          else
+            issue_pvt(tO, stage(fV), sP0, j > 0);
           tc_commit(pv_done);
           tc_commit(&kv_empty[fV % NS]);
         }
@@ -525,6 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool present = (x ? un.n[1] : un.n[0]) > 0;
       const int hx = x ? un.h[1] : un.h[0];
       const int qpos = (x ? un.q0[1] : un.q0[0]) + row;
+      // paged: the last visible key of this row relative to tile 0, one register for the
+      // whole unit (the causal bound and the sequence's end both shift by j * BN)
+      const int lim0 = PAGED ? min(p.causal ? un.q_off + qpos : un.Tk - 1, un.Tk - 1) : 0;
       float m_used = -INFINITY, l = 0.f;
       bool leave = false;
       for (int j = 0; j < n; ++j) {
@@ -547,8 +555,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_free[x]);
           int lim = BN - 1;
-          if (p.causal) lim = min(lim, (PAGED ? un.q_off : p.q_off) + qpos - j * BN);
-          lim = min(lim, (PAGED ? un.Tk : p.Tk) - 1 - j * BN);
+          if constexpr (PAGED) {
+            lim = min(lim, lim0 - j * BN);
+          } else {
+            if (p.causal) lim = min(lim, p.q_off + qpos - j * BN);
+            lim = min(lim, p.Tk - 1 - j * BN);
+          }
           if (!present) lim = -1;
           if (lim < BN - 1) {
 #pragma unroll
