@@ -87,6 +87,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Wait of a single-thread role (TMA producer, MMA issuer): one try_wait inline, the
+// bounded retry loop out of line so that those roles' loops stay compact (measured:
+// 2 % of the d = 128 prefill).  Not for code that runs after setmaxnreg.inc: a call
+// there fails register allocation.
+static __device__ __noinline__ bool ctl_wait_slow(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, uint32_t* status,
+                                                  uint64_t limit_ns) {
+  return mbar_wait(bar, parity, abort, status, limit_ns);
+}
+__device__ __forceinline__ bool ctl_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         uint32_t* status, uint64_t limit_ns) {
+  return mbar_try_wait(bar, parity) || ctl_wait_slow(bar, parity, abort, status, limit_ns);
+}
+
 // --------------------------------------------------------------------------
 // TMA (tensor maps are __grid_constant__ kernel parameters)
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kThreads)
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % NS, use = t / NS;
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) break;
+        if (use > 0 && !ctl_wait(&empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) break;
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         uint8_t* kdst = smem + s * C::STAGE_BYTES;
         uint8_t* vdst = kdst + C::TILE_BYTES;

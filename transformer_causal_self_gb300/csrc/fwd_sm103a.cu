@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 2; ++x) {
           if (ok && un.n[x] > 0) {
             if (nq[x] > 0 &&
-                !mbar_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, p.status, kWaitNs)) {
+                !ctl_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, p.status, kWaitNs)) {
               ok = false;
             } else {
               mbar_arrive_expect_tx(&q_full[x], C::Q_BYTES);
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < un.n[1] && ok; ++j) {
           for (int t = 0; t < 2; ++t) {
             const uint32_t s = fill % C::NS, use = fill / C::NS;
-            if (use > 0 && !mbar_wait(&kv_empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) {
+            if (use > 0 && !ctl_wait(&kv_empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) {
               ok = false;
               break;
             }
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (!ok) return false;
-        ok = mbar_wait(bar, parity, abort_flag, p.status, kWaitNs);
+        ok = ctl_wait(bar, parity, abort_flag, p.status, kWaitNs);
         tc_fence_after();
         return ok;
       };

@@ -195,17 +195,6 @@ __device__ __forceinline__ void issue_pvt(uint32_t d_tmem, uint32_t v_smem, uint
   }
 }
 
-// Barrier wait of the single-thread roles (producer, MMA issuer): one try_wait inline,
-// the bounded retry loop out of line so that their loops stay compact.
-__device__ __noinline__ bool ctl_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                           uint32_t* status) {
-  return mbar_wait(bar, parity, abort, status, kWaitNs);
-}
-__device__ __forceinline__ bool ctl_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                         uint32_t* status) {
-  return mbar_try_wait(bar, parity) || ctl_wait_slow(bar, parity, abort, status);
-}
-
 // O^T += V^T P^T for a paged sequence's last key tile, whose rows past the end
 // (nvalid..BN-1) may hold anything, NaN included, which P = 0 would not cancel:
 // the 16-key steps past the end are skipped and the rows of the last step that lie
@@ -301,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one K (DK channels) or V (D channels) tile into the next ring stage
       auto load = [&](const CUtensorMap* m, int width, int j, const Unit& un) {
         const uint32_t s = fill % NS, use = fill / NS;
-        if (use > 0 && !ctl_wait(&kv_empty[s], (use - 1) & 1, abort_flag, p.status)) {
+        if (use > 0 && !ctl_wait(&kv_empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) {
           ok = false;
           return;
         }
@@ -353,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 2; ++x) {
           if (ok && un.n[x] > 0) {
             if (nq[x] > 0 &&
-                !ctl_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, p.status)) {
+                !ctl_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, p.status, kWaitNs)) {
               ok = false;
             } else {
               mbar_arrive_expect_tx(&q_full[x], static_cast<uint32_t>(BM * DK * 2));
@@ -394,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (!ok) return false;
-        ok = ctl_wait(bar, parity, abort_flag, p.status);
+        ok = ctl_wait(bar, parity, abort_flag, p.status, kWaitNs);
         tc_fence_after();
         return ok;
       };
