@@ -338,16 +338,18 @@ def run_gpu(args):
         d2h = ho.numel() * ho.element_size() + hod.numel() * hod.element_size()
         e_steps = max(1, min(args.steps, 5))
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e_steps)]
+        # the prefill through csattn_attn_fwd_host: copies in, kernels and copies out
+        # pipelined over 8 chunks of (sequence, KV head) pairs inside the call (the default)
+        ws_host = torch.empty(csattn.fwd_host_workspace_size(wp.B, wp.Hq, wp.Hkv, wp.T, wp.d,
+                                                             torch.bfloat16, wp.rope_base),
+                              dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
-        for i in range(e_steps):
-            ev[i][0].record(stream)
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            csattn.attn_fwd(q, k, v, out, causal=True, rope_base=wp.rope_base, scale=wp.scale,
-                            workspace=k_rot.view(torch.uint8).view(-1), stream=stream)
-            ho.copy_(out, non_blocking=True)
-            ev[i][1].record(stream)
+        for i in range(e_steps + 1):  # the first call creates the library's streams: untimed
+            j = max(i - 1, 0)
+            ev[j][0].record(stream)
+            csattn.attn_fwd_host(hq, hk, hv, ho, causal=True, rope_base=wp.rope_base,
+                                 scale=wp.scale, workspace=ws_host, stream=stream)
+            ev[j][1].record(stream)
             qd.copy_(hqd, non_blocking=True)
             kc.copy_(hkc, non_blocking=True)
             vc.copy_(hvc, non_blocking=True)
@@ -355,7 +357,7 @@ def run_gpu(args):
             csattn.attn_decode(qd, kc, vc, lens, outd, scale=wd.scale, max_seq_len=max_len,
                                workspace=ws_dec, stream=stream)
             hod.copy_(outd, non_blocking=True)
-            ev[i][2].record(stream)
+            ev[j][2].record(stream)
         torch.cuda.synchronize()
         csattn.check_status(stream)
         e_pre = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
@@ -365,8 +367,10 @@ def run_gpu(args):
                "ms_per_step": round(e_pre + e_dec, 3),
                "decode": {"value": round(world * dbytes / (e_dec * 1e-3) / 1e9, 1),
                           "unit": "GB/s"},
-               "note": "pinned host buffers; H2D of q,k,v (+ decode q, K/V cache, seq_lens) "
-                       "and D2H of both outputs inside each timed step"}
+               "note": "pinned host buffers; prefill through csattn_attn_fwd_host (H2D of "
+                       "q, k, v, the kernels and D2H of out pipelined over 8 chunks inside the "
+                       "call); decode: H2D of q, the K/V cache and seq_lens, then D2H of its "
+                       "output, inside each timed step"}
 
     rows = None
     if rank == 0 and not args.no_rows:

@@ -101,6 +101,39 @@ int csattn_attn_fwd(const void* q, const void* k, const void* v, void* out, int 
                     size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of device workspace csattn_attn_fwd_host needs: device copies of q, k, v,
+ * out and lse, and the rotated keys (each block 256-byte aligned).  0 for an
+ * unknown dtype or a size below 1.
+ */
+size_t csattn_fwd_host_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,
+                                      float rope_base);
+
+/*
+ * csattn_attn_fwd on HOST buffers: q, k, v are read from host memory and out (and
+ * lse, if non-NULL) written to host memory, all in the layouts of csattn_attn_fwd.
+ * The problem is cut into num_chunks chunks of consecutive (sequence, KV head)
+ * pairs (a pair owns its Hq / Hkv query heads, so a chunk is contiguous in every
+ * tensor); each chunk's inputs are copied in, its attention computed and its output
+ * copied out on three internal streams of the current device, so that the copies of
+ * one chunk overlap the kernels and the opposite-direction copies of the others.
+ * The results equal csattn_attn_fwd's bit for bit.
+ *   q_h, k_h, v_h, out_h, lse_h  host pointers; page-locked memory (cudaHostAlloc or
+ *                cudaHostRegister) lets the copies run asynchronously
+ *   num_chunks   0: automatic (8, at most B * Hkv); otherwise 1..16 (capped at B*Hkv)
+ *   workspace    device buffer of >= csattn_fwd_host_workspace_size() bytes,
+ *                16-byte aligned, in use until the call's work on `stream` completes
+ * Other arguments, checks and return codes as csattn_attn_fwd (messages name
+ * attn_fwd_host).  Every check runs before the first copy is enqueued.  Asynchronous
+ * on `stream`: the internal streams wait for the work already on `stream`, and
+ * `stream` waits for the last copy out; the host buffers must stay valid until then.
+ * Concurrent calls from several host threads are serialised while they enqueue.
+ */
+int csattn_attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* out_h, int B,
+                         int Hq, int Hkv, int T, int d, int dtype, int causal, float rope_base,
+                         int rope_layout, float scale, float* lse_h, int num_chunks,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace csattn_attn_fwd_ext needs: the rotated keys,
  * B*Hkv*Tk*d*2, for bf16 with RoPE (unless k is given rotated); 0 otherwise.
  */

@@ -185,6 +185,50 @@ def test_decode_paged_rejects_invalid_arguments(lib, kw, status):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(q=None), -1),
+    (dict(out=None), -1),
+    (dict(B=0), -1),
+    (dict(Hq=6, Hkv=4), -1),
+    (dict(dtype=7), -1),
+    (dict(chunks=-1), -1),
+    (dict(chunks=17), -1),
+    (dict(ws=None), -5),
+    (dict(ws_bytes=1024), -5),
+    (dict(ws=FAKE + 8), -5),
+    (dict(d=48), -2),
+    (dict(d=32), -2),
+    (dict(causal=3), -1),
+    (dict(rope_layout=5), -1),
+    (dict(rope_base=10000.0, T=50000), -2),
+])
+def test_fwd_host_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=2, Hq=8, Hkv=2, T=256, d=128, dtype=1, causal=1,
+             rope_base=0.0, rope_layout=0, scale=0.0, lse=None, chunks=0, ws=FAKE,
+             ws_bytes=1 << 40)
+    a.update(kw)
+    rc = lib.csattn_attn_fwd_host(a["q"], a["k"], a["v"], a["out"], a["B"], a["Hq"], a["Hkv"],
+                                  a["T"], a["d"], a["dtype"], a["causal"], a["rope_base"],
+                                  a["rope_layout"], a["scale"], a["lse"], a["chunks"], a["ws"],
+                                  a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"attn_fwd_host" in lib.csattn_last_error()
+
+
+def test_fwd_host_workspace_size(lib):
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    q, k = 4 * 32 * 4096 * 128 * 2, 4 * 8 * 4096 * 128 * 2
+    lse = 4 * 32 * 4096 * 4
+    assert lib.csattn_fwd_host_workspace_size(4, 32, 8, 4096, 128, 1, 0.0) == \
+        2 * al(q) + 2 * al(k) + al(lse)
+    assert lib.csattn_fwd_host_workspace_size(4, 32, 8, 4096, 128, 1, 10000.0) == \
+        2 * al(q) + 3 * al(k) + al(lse)
+    assert lib.csattn_fwd_host_workspace_size(4, 32, 8, 4096, 128, 0, 10000.0) == \
+        2 * al(2 * q) + 2 * al(2 * k) + al(lse)
+    assert lib.csattn_fwd_host_workspace_size(4, 32, 8, 4096, 128, 5, 0.0) == 0
+    assert lib.csattn_fwd_host_workspace_size(0, 32, 8, 4096, 128, 1, 0.0) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1),
     (dict(table=None), -1),
     (dict(lens=None), -1),
     (dict(Tq=0), -1),

@@ -14,7 +14,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "CsattnError", "library_path", "load_library", "attn_fwd", "attn_decode", "rope_rotate",
+    "CsattnError", "library_path", "load_library", "attn_fwd", "attn_fwd_host", "attn_decode",
+    "rope_rotate", "fwd_host_workspace_size",
     "fwd_workspace_size", "decode_workspace_size", "check_status",
     "selftest_bounded_wait", "EXPORTED_SYMBOLS",
 ]
@@ -36,6 +37,9 @@ _SIGNATURES = {
     "csattn_fwd_workspace_size": (_c_size, [_c_int] * 6 + [_c_float]),
     "csattn_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _c_float,
                                                                         _vp, _vp, _c_size, _vp]),
+    "csattn_fwd_host_workspace_size": (_c_size, [_c_int] * 6 + [_c_float]),
+    "csattn_attn_fwd_host": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_c_float, _c_int, _c_float, _vp,
+                                                                 _c_int, _vp, _c_size, _vp]),
     "csattn_fwd_ext_workspace_size": (_c_size, [_c_int] * 7 + [_c_float]),
     "csattn_attn_fwd_ext": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 10 + [_c_float, _c_int,
                                                                             _c_float, _vp, _vp,
@@ -192,6 +196,53 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: Optional[to
                                float(scale),
                                lse.data_ptr() if lse is not None else None, ws_ptr, ws_bytes,
                                _stream_handle(stream)))
+    return out
+
+
+def _need_host(*ts):
+    for t in ts:
+        if t.device.type != "cpu":
+            raise ValueError("host tensors expected")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def fwd_host_workspace_size(B, Hq, Hkv, T, d, dtype: torch.dtype, rope_base: float) -> int:
+    code = CSATTN_BF16 if dtype == torch.bfloat16 else CSATTN_F32
+    return int(load_library().csattn_fwd_host_workspace_size(B, Hq, Hkv, T, d, code,
+                                                             float(rope_base)))
+
+
+def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                  out: Optional[torch.Tensor] = None, *, causal: bool = True,
+                  rope_base: float = 0.0, scale: float = 0.0, rope_layout: str = "split_half",
+                  lse: Optional[torch.Tensor] = None, num_chunks: int = 0,
+                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """attn_fwd on host tensors (C: csattn_attn_fwd_host): copies in, attention and
+    copies out pipelined over chunks of (sequence, KV head) pairs on the current
+    device.  q, k, v, out (and lse) are CPU tensors, pinned for asynchronous copies;
+    out is allocated pinned when not given.  Asynchronous on `stream`: synchronize
+    before reading out.
+    """
+    _need_host(q, k, v)
+    B, Hq, T, d = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    _need_host(out)
+    if lse is not None:
+        _need_host(lse)
+    if workspace is None:
+        workspace = torch.empty(fwd_host_workspace_size(B, Hq, Hkv, T, d, q.dtype, rope_base),
+                                dtype=torch.uint8, device=torch.device("cuda",
+                                                                       torch.cuda.current_device()))
+    lib = load_library()
+    _check(lib.csattn_attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B,
+                                    Hq, Hkv, T, d, _dtype_code(q), int(bool(causal)),
+                                    float(rope_base), _ROPE_LAYOUT[rope_layout], float(scale),
+                                    lse.data_ptr() if lse is not None else None, int(num_chunks),
+                                    workspace.data_ptr(), workspace.numel(),
+                                    _stream_handle(stream)))
     return out
 
 

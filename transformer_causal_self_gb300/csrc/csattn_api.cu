@@ -159,10 +159,12 @@ size_t csattn_fwd_ext_workspace_size(int B, int Hq, int Hkv, int Tq, int Tk, int
 namespace {
 
 // Shared by csattn_attn_fwd (Tq = Tk = T, q_offset = 0) and csattn_attn_fwd_ext.
+// check_only: stop after the argument checks (the workspace is not checked) and return OK.
 int attn_fwd_impl(const char* fn, const void* q, const void* k, const void* v, void* out, int B,
                   int Hq, int Hkv, int Tq, int Tk, int q_offset, int d, int dv, int dtype,
                   int causal, float rope_base, int rope_layout, float scale, float* lse,
-                  void* workspace, size_t workspace_bytes, void* stream) {
+                  void* workspace, size_t workspace_bytes, void* stream,
+                  bool check_only = false) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: q, k, v and out must be non-null", fn);
   if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1)
@@ -201,6 +203,7 @@ int attn_fwd_impl(const char* fn, const void* q, const void* k, const void* v, v
     return fail(CSATTN_ERR_INVALID_ARG, "%s: q, k, v, out must be 16-byte aligned", fn);
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: lse must be 4-byte aligned", fn);
+  if (check_only) return CSATTN_OK;
   const size_t need =
       k_prerotated ? 0 : csattn_fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, dtype, rope_base);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
@@ -251,6 +254,14 @@ int attn_fwd_impl(const char* fn, const void* q, const void* k, const void* v, v
 }
 
 }  // namespace
+
+int csattn::attn_fwd_check(const char* fn, int B, int Hq, int Hkv, int T, int d, int dtype,
+                           int causal, float rope_base, int rope_layout, float scale) {
+  alignas(16) static const uint8_t dummy[16] = {};
+  void* x = const_cast<uint8_t*>(dummy);
+  return attn_fwd_impl(fn, x, x, x, x, B, Hq, Hkv, T, T, 0, d, d, dtype, causal, rope_base,
+                       rope_layout, scale, nullptr, nullptr, 0, nullptr, true);
+}
 
 extern "C" {
 

@@ -124,6 +124,11 @@ cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream
 // Replace the calling thread's csattn_last_error() message.
 void set_last_error(const char* msg);
 
+// The argument checks of csattn_attn_fwd (all but the pointers and the workspace), with
+// its return codes and error messages prefixed by fn.
+int attn_fwd_check(const char* fn, int B, int Hq, int Hkv, int T, int d, int dtype, int causal,
+                   float rope_base, int rope_layout, float scale);
+
 // Driver entry point for cuTensorMapEncodeTiled (nullptr if unavailable).
 void* tensor_map_encoder();
 
