@@ -334,7 +334,8 @@ def run_gpu(args):
         hq, hk, hv = pin(q_h), pin(k_h), pin(v_h)
         hqd, hkc, hvc, hl = pin(qd_h), pin(kc_h), pin(vc_h), pin(lens_h)
         ho, hod = torch.empty_like(hq).pin_memory(), torch.empty_like(hqd).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hkc, hvc, hl))
+        # the decode leg copies q, seq_lens and only the cache rows it reads (dbytes)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hl)) + int(dbytes)
         d2h = ho.numel() * ho.element_size() + hod.numel() * hod.element_size()
         e_steps = max(1, min(args.steps, 5))
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e_steps)]
@@ -343,6 +344,9 @@ def run_gpu(args):
         ws_host = torch.empty(csattn.fwd_host_workspace_size(wp.B, wp.Hq, wp.Hkv, wp.T, wp.d,
                                                              torch.bfloat16, wp.rope_base),
                               dtype=torch.uint8, device=dev)
+        ws_dec_host = torch.empty(csattn.decode_host_workspace_size(wd.B, wd.Hq, wd.Hkv, wd.Lmax,
+                                                                    wd.d), dtype=torch.uint8,
+                                  device=dev)
         torch.cuda.synchronize()
         for i in range(e_steps + 1):  # the first call creates the library's streams: untimed
             j = max(i - 1, 0)
@@ -350,13 +354,8 @@ def run_gpu(args):
             csattn.attn_fwd_host(hq, hk, hv, ho, causal=True, rope_base=wp.rope_base,
                                  scale=wp.scale, workspace=ws_host, stream=stream)
             ev[j][1].record(stream)
-            qd.copy_(hqd, non_blocking=True)
-            kc.copy_(hkc, non_blocking=True)
-            vc.copy_(hvc, non_blocking=True)
-            lens.copy_(hl, non_blocking=True)
-            csattn.attn_decode(qd, kc, vc, lens, outd, scale=wd.scale, max_seq_len=max_len,
-                               workspace=ws_dec, stream=stream)
-            hod.copy_(outd, non_blocking=True)
+            csattn.attn_decode_host(hqd, hkc, hvc, hl, hod, scale=wd.scale, workspace=ws_dec_host,
+                                    stream=stream)
             ev[j][2].record(stream)
         torch.cuda.synchronize()
         csattn.check_status(stream)
@@ -369,8 +368,9 @@ def run_gpu(args):
                           "unit": "GB/s"},
                "note": "pinned host buffers; prefill through csattn_attn_fwd_host (H2D of "
                        "q, k, v, the kernels and D2H of out pipelined over 8 chunks inside the "
-                       "call); decode: H2D of q, the K/V cache and seq_lens, then D2H of its "
-                       "output, inside each timed step"}
+                       "call); decode through csattn_attn_decode_host (H2D of q, seq_lens and "
+                       "the K/V rows below seq_lens, the kernels and D2H of out, pipelined "
+                       "over 4 chunks of sequences), inside each timed step"}
 
     rows = None
     if rank == 0 and not args.no_rows:
@@ -431,6 +431,8 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
     csattn_attn_fwd_ext, L2 flushed before each launch (its inputs are ~L2-sized).
     prefill_paged: the same chunk with the cache in 256-row pages of a shuffled pool
     (csattn_attn_prefill_paged), L2 flushed before each launch.
+    long_context, gpt2: the prefill (RoPE pass + attention) of long_gqa_bf16 (T=32768)
+    and gpt2_bf16 (d=64, L2 flushed before each launch) through csattn_attn_fwd.
     rectangular: llama_cross_bf16 (1024 queries against 4096 keys, no mask), the same
     entry point, L2 flushed before each launch.
     decode_step: the decode_bf16 batch with the new token appended at row L_b - 1 and
@@ -497,6 +499,43 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
                      "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
                      "kernel": "fwd_d128_kernel (paged K/V)"}}
     del q, k, v, k_rot, o, kp, vp, table, clen
+
+    # the other prefill configurations: long-context GQA (T=32768, RoPE 5e5; > 400 MB of
+    # inputs, no flush needed) and GPT-2-shaped MHA (d=64, no RoPE; L2 flushed)
+    for name, wl, flush_it in (("long_context", "long_gqa_bf16", False),
+                               ("gpt2", "gpt2_bf16", True)):
+        wq = W.WORKLOADS[wl]
+        q, k, v = (t.to(dev) for t in W.make_prefill_inputs(wq))
+        o = torch.empty_like(q)
+        ws_f = torch.empty(max(16, csattn.fwd_workspace_size(wq.B, wq.Hq, wq.Hkv, wq.T, wq.d,
+                                                            q.dtype, wq.rope_base)),
+                           dtype=torch.uint8, device=dev)
+        ts = []
+        n_rep = max(3, reps // 3) if wl == "long_gqa_bf16" else reps
+        for i in range(3 + n_rep):
+            if flush_it:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            csattn.attn_fwd(q, k, v, o, causal=True, rope_base=wq.rope_base, scale=wq.scale,
+                            workspace=ws_f, stream=stream)
+            e1.record(stream)
+            if i >= 3:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        csattn.check_status(stream)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+        tf = wq.flops() / (ms * 1e-3) / 1e12
+        out[name] = {
+            "workload": f"{wl} (B={wq.B}, Hq={wq.Hq}, Hkv={wq.Hkv}, T={wq.T}, d={wq.d}, "
+                        f"RoPE {wq.rope_base:g}; RoPE pass + attention kernel)",
+            "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+            "flops": wq.flops(),
+            "l2": "flushed before each launch" if flush_it else "inputs larger than L2",
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
+                         "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                         "kernel": "fwd_d128_kernel" if wq.d == 128 else "fwd_sm103a_kernel<64>"}}
+        del q, k, v, o, ws_f
 
     # rectangular, unmasked (cross-attention shaped): 1024 queries x 4096 keys per head
     wx = W.WORKLOADS["llama_cross_bf16"]

@@ -245,6 +245,35 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of device workspace csattn_attn_decode_host needs: device copies of q, the
+ * two caches (full [B, Hkv, Lmax, d] layout, only the visible rows written), the
+ * lengths and out, and the split partials of csattn_decode_workspace_size().
+ */
+size_t csattn_decode_host_workspace_size(int B, int Hq, int Hkv, int Lmax, int d,
+                                         int num_splits);
+
+/*
+ * csattn_attn_decode on HOST buffers: q [B, Hq, 1, d], the caches [B, Hkv, Lmax, d]
+ * and seq_lens [B] (int32) in host memory, out [B, Hq, 1, d] written to host memory.
+ * Only the rows the decode reads cross the host link: rows 0..seq_lens[b]-1 of every
+ * KV head of sequence b (one strided copy per sequence and cache).  The sequences are
+ * cut into num_chunks chunks (0: 4; at most 16 and at most B); each chunk's copies in,
+ * decode and copy out run on the internal streams of csattn_attn_fwd_host, so copies
+ * and kernels of different chunks overlap.
+ *   seq_lens_h  read by the host during the call (each in [1, Lmax], else
+ *               CSATTN_ERR_INVALID_ARG) and copied to the device asynchronously
+ *   workspace   >= csattn_decode_host_workspace_size() bytes, 16-byte aligned
+ * Other arguments, checks and return codes as csattn_attn_decode (max_seq_len is
+ * the largest seq_lens).  Asynchronous on `stream` as csattn_attn_fwd_host; the host
+ * buffers must stay valid until the work on `stream` completes.
+ */
+int csattn_attn_decode_host(const void* q_h, const void* k_cache_h, const void* v_cache_h,
+                            const int32_t* seq_lens_h, void* out_h, int B, int Hq, int Hkv,
+                            int Lmax, int d, int dtype, float scale, int num_splits,
+                            int num_chunks, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * KV-cache decode over a paged cache (the appended cache of "The Transformer
  * architecture", section "Hands-on", stored in fixed-size pages):
  *   k_pages, v_pages [num_pages, Hkv, page_size, d] bf16 (keys already rotated)

@@ -213,6 +213,45 @@ def test_fwd_host_rejects_invalid_arguments(lib, kw, status):
     assert b"attn_fwd_host" in lib.csattn_last_error()
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1),
+    (dict(lens=None), -1),
+    (dict(B=0), -1),
+    (dict(lens_v=(0, 5)), -1),
+    (dict(lens_v=(5, 300)), -1),
+    (dict(chunks=17), -1),
+    (dict(Hq=6, Hkv=4), -1),
+    (dict(dtype=0), -2),
+    (dict(d=96), -2),
+    (dict(Hq=34, Hkv=2), -2),
+    (dict(splits=-1), -1),
+    (dict(ws=None), -5),
+    (dict(ws_bytes=100), -5),
+])
+def test_decode_host_rejects_invalid_arguments(lib, kw, status):
+    import ctypes
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=2, Hq=8, Hkv=2, Lmax=256, d=128, dtype=1,
+             scale=0.0, splits=0, chunks=0, ws=FAKE, ws_bytes=1 << 40, lens_v=(5, 256))
+    a.update(kw)
+    lens = (ctypes.c_int32 * len(a["lens_v"]))(*a["lens_v"])
+    if "lens" in kw:
+        lens = None
+    rc = lib.csattn_attn_decode_host(a["q"], a["k"], a["v"], lens, a["out"], a["B"], a["Hq"],
+                                     a["Hkv"], a["Lmax"], a["d"], a["dtype"], a["scale"],
+                                     a["splits"], a["chunks"], a["ws"], a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"attn_decode_host" in lib.csattn_last_error()
+
+
+def test_decode_host_workspace_size(lib):
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    q, c = 64 * 32 * 128 * 2, 64 * 8 * 8192 * 128 * 2
+    part = lib.csattn_decode_workspace_size(64, 32, 8192, 128, 0)
+    assert lib.csattn_decode_host_workspace_size(64, 32, 8, 8192, 128, 0) == \
+        2 * al(q) + 2 * al(c) + al(64 * 4) + al(part)
+    assert lib.csattn_decode_host_workspace_size(0, 32, 8, 8192, 128, 0) == 0
+
+
 def test_fwd_host_workspace_size(lib):
     al = lambda x: (x + 255) // 256 * 256  # noqa: E731
     q, k = 4 * 32 * 4096 * 128 * 2, 4 * 8 * 4096 * 128 * 2

@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "CsattnError", "library_path", "load_library", "attn_fwd", "attn_fwd_host", "attn_decode",
-    "rope_rotate", "fwd_host_workspace_size",
+    "attn_decode_host", "rope_rotate", "fwd_host_workspace_size", "decode_host_workspace_size",
     "fwd_workspace_size", "decode_workspace_size", "check_status",
     "selftest_bounded_wait", "EXPORTED_SYMBOLS",
 ]
@@ -40,6 +40,9 @@ _SIGNATURES = {
     "csattn_fwd_host_workspace_size": (_c_size, [_c_int] * 6 + [_c_float]),
     "csattn_attn_fwd_host": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_c_float, _c_int, _c_float, _vp,
                                                                  _c_int, _vp, _c_size, _vp]),
+    "csattn_decode_host_workspace_size": (_c_size, [_c_int] * 6),
+    "csattn_attn_decode_host": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp,
+                                                                    _c_size, _vp]),
     "csattn_fwd_ext_workspace_size": (_c_size, [_c_int] * 7 + [_c_float]),
     "csattn_attn_fwd_ext": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 10 + [_c_float, _c_int,
                                                                             _c_float, _vp, _vp,
@@ -243,6 +246,41 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                     lse.data_ptr() if lse is not None else None, int(num_chunks),
                                     workspace.data_ptr(), workspace.numel(),
                                     _stream_handle(stream)))
+    return out
+
+
+def decode_host_workspace_size(B, Hq, Hkv, Lmax, d, num_splits=0) -> int:
+    return int(load_library().csattn_decode_host_workspace_size(B, Hq, Hkv, Lmax, d,
+                                                                int(num_splits)))
+
+
+def attn_decode_host(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     seq_lens: torch.Tensor, out: Optional[torch.Tensor] = None, *,
+                     scale: float = 0.0, num_splits: int = 0, num_chunks: int = 0,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """attn_decode on host tensors (C: csattn_attn_decode_host): only the cache rows
+    below seq_lens cross to the device, pipelined with the decode over chunks of
+    sequences.  seq_lens is an int32 CPU tensor read during the call.  Asynchronous on
+    `stream`: synchronize before reading out.
+    """
+    _need_host(q, k_cache, v_cache, seq_lens)
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    B, Hq, _, d = q.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    _need_host(out)
+    if workspace is None:
+        workspace = torch.empty(decode_host_workspace_size(B, Hq, Hkv, Lmax, d, num_splits),
+                                dtype=torch.uint8,
+                                device=torch.device("cuda", torch.cuda.current_device()))
+    lib = load_library()
+    _check(lib.csattn_attn_decode_host(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                       seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lmax, d,
+                                       _dtype_code(q), float(scale), int(num_splits),
+                                       int(num_chunks), workspace.data_ptr(), workspace.numel(),
+                                       _stream_handle(stream)))
     return out
 
 

@@ -465,6 +465,18 @@ int decode_check(const char* fn, const void* q, const void* k_cache, const void*
   return CSATTN_OK;
 }
 
+}  // namespace
+
+int csattn::attn_decode_check(const char* fn, int B, int Hq, int Hkv, int Lmax, int d,
+                              int dtype, float scale, int max_seq_len, int num_splits) {
+  alignas(16) static const uint8_t dummy[16] = {};
+  const void* x = dummy;
+  return decode_check(fn, x, x, x, reinterpret_cast<const int32_t*>(dummy), x, B, Hq, Hkv,
+                      Lmax, d, dtype, scale, max_seq_len, num_splits);
+}
+
+namespace {
+
 // Shared by csattn_attn_decode (len_add 0) and csattn_attn_decode_step (len_add 1:
 // the appended row).
 int decode_impl(const char* fn, const void* q, const void* k_cache, const void* v_cache,

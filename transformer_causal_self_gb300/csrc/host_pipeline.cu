@@ -202,4 +202,111 @@ int csattn_attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void
   return CSATTN_OK;
 }
 
+size_t csattn_decode_host_workspace_size(int B, int Hq, int Hkv, int Lmax, int d,
+                                         int num_splits) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || d < 1 || num_splits < 0) return 0;
+  const size_t qb = static_cast<size_t>(B) * Hq * d * 2;
+  const size_t cb = static_cast<size_t>(B) * Hkv * Lmax * d * 2;
+  return al256(qb) + 2 * al256(cb) + al256(static_cast<size_t>(B) * 4) + al256(qb) +
+         al256(csattn_decode_workspace_size(B, Hq, Lmax, d, num_splits));
+}
+
+int csattn_attn_decode_host(const void* q_h, const void* k_cache_h, const void* v_cache_h,
+                            const int32_t* seq_lens_h, void* out_h, int B, int Hq, int Hkv,
+                            int Lmax, int d, int dtype, float scale, int num_splits,
+                            int num_chunks, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  const char* fn = "attn_decode_host";
+  if (q_h == nullptr || k_cache_h == nullptr || v_cache_h == nullptr || seq_lens_h == nullptr ||
+      out_h == nullptr)
+    return hfail(CSATTN_ERR_INVALID_ARG, "%s: null pointer argument", fn);
+  if (B < 1 || Lmax < 1)
+    return hfail(CSATTN_ERR_INVALID_ARG, "%s: B=%d Lmax=%d must be >= 1", fn, B, Lmax);
+  if (num_chunks < 0 || num_chunks > kMaxChunks)
+    return hfail(CSATTN_ERR_INVALID_ARG, "%s: num_chunks=%d not in [0, %d]", fn, num_chunks,
+                 kMaxChunks);
+  // the lengths are read here, on the host, so they are checked here too
+  int max_len = 0;
+  for (int b = 0; b < B; ++b) {
+    const int L = seq_lens_h[b];
+    if (L < 1 || L > Lmax)
+      return hfail(CSATTN_ERR_INVALID_ARG, "%s: seq_lens[%d]=%d not in [1, Lmax=%d]", fn, b, L,
+                   Lmax);
+    if (L > max_len) max_len = L;
+  }
+  int rc = attn_decode_check(fn, B, Hq, Hkv, Lmax, d, dtype, scale, max_len, num_splits);
+  if (rc != CSATTN_OK) return rc;
+  const size_t need = csattn_decode_host_workspace_size(B, Hq, Hkv, Lmax, d, num_splits);
+  if (workspace == nullptr || need == 0 || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+    return hfail(CSATTN_ERR_WORKSPACE, "%s: needs a 16-byte aligned workspace of %zu bytes (got %zu)",
+                 fn, need, workspace_bytes);
+  const size_t esz = 2;
+  const size_t q_seq = static_cast<size_t>(Hq) * d * esz;          // q (or out) bytes per sequence
+  const size_t row = static_cast<size_t>(d) * esz;                  // one cache row
+  const size_t c_head = static_cast<size_t>(Lmax) * row;            // one head's cache
+  const size_t c_seq = static_cast<size_t>(Hkv) * c_head;           // one sequence's cache
+  uint8_t* dq = static_cast<uint8_t*>(workspace);
+  uint8_t* dk = dq + al256(q_seq * B);
+  uint8_t* dv = dk + al256(c_seq * B);
+  int32_t* dlens = reinterpret_cast<int32_t*>(dv + al256(c_seq * B));
+  uint8_t* dout = reinterpret_cast<uint8_t*>(dlens) + al256(static_cast<size_t>(B) * 4);
+  uint8_t* dpart = dout + al256(q_seq * B);
+  const size_t part_bytes = csattn_decode_workspace_size(B, Hq, Lmax, d, num_splits);
+  int n = num_chunks > 0 ? num_chunks : 4;
+  if (n > B) n = B;
+
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  Pipe* pp = nullptr;
+  rc = pipe_of_device(&pp);
+  if (rc != CSATTN_OK) return rc;
+  Pipe& p = *pp;
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = cudaEventRecord(p.start, caller)) != cudaSuccess) return hfail_cuda(e, "event record");
+  for (cudaStream_t s : {p.h2d, p.cmp, p.d2h})
+    if ((e = cudaStreamWaitEvent(s, p.start, 0)) != cudaSuccess)
+      return hfail_cuda(e, "stream wait");
+  for (int c = 0; c < n; ++c) {
+    const int b0 = static_cast<int>(static_cast<long long>(B) * c / n);
+    const int b1 = static_cast<int>(static_cast<long long>(B) * (c + 1) / n);
+    const int nb = b1 - b0;
+    int chunk_max = 0;
+    if ((e = cudaMemcpyAsync(dq + q_seq * b0, static_cast<const uint8_t*>(q_h) + q_seq * b0,
+                             q_seq * nb, cudaMemcpyHostToDevice, p.h2d)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dlens + b0, seq_lens_h + b0, static_cast<size_t>(nb) * 4,
+                             cudaMemcpyHostToDevice, p.h2d)) != cudaSuccess)
+      return hfail_cuda(e, "host-to-device copy");
+    // only the rows the decode reads: rows 0..L_b-1 of every KV head of sequence b
+    for (int b = b0; b < b1; ++b) {
+      const int L = seq_lens_h[b];
+      if (L > chunk_max) chunk_max = L;
+      const size_t off = c_seq * b;
+      if ((e = cudaMemcpy2DAsync(dk + off, c_head, static_cast<const uint8_t*>(k_cache_h) + off,
+                                 c_head, row * L, Hkv, cudaMemcpyHostToDevice, p.h2d)) !=
+              cudaSuccess ||
+          (e = cudaMemcpy2DAsync(dv + off, c_head, static_cast<const uint8_t*>(v_cache_h) + off,
+                                 c_head, row * L, Hkv, cudaMemcpyHostToDevice, p.h2d)) !=
+              cudaSuccess)
+        return hfail_cuda(e, "host-to-device copy (cache rows)");
+    }
+    if ((e = cudaEventRecord(p.in[c], p.h2d)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(p.cmp, p.in[c], 0)) != cudaSuccess)
+      return hfail_cuda(e, "event");
+    rc = csattn_attn_decode(dq + q_seq * b0, dk + c_seq * b0, dv + c_seq * b0, dlens + b0,
+                            dout + q_seq * b0, nb, Hq, Hkv, Lmax, d, dtype, scale, chunk_max,
+                            num_splits, dpart, part_bytes, p.cmp);
+    if (rc != CSATTN_OK) return rc;
+    if ((e = cudaEventRecord(p.done[c], p.cmp)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(p.d2h, p.done[c], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(static_cast<uint8_t*>(out_h) + q_seq * b0, dout + q_seq * b0,
+                             q_seq * nb, cudaMemcpyDeviceToHost, p.d2h)) != cudaSuccess)
+      return hfail_cuda(e, "device-to-host copy");
+  }
+  if ((e = cudaEventRecord(p.end, p.d2h)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(caller, p.end, 0)) != cudaSuccess)
+    return hfail_cuda(e, "final wait");
+  return CSATTN_OK;
+}
+
 }  // extern "C"

@@ -129,6 +129,10 @@ void set_last_error(const char* msg);
 int attn_fwd_check(const char* fn, int B, int Hq, int Hkv, int T, int d, int dtype, int causal,
                    float rope_base, int rope_layout, float scale);
 
+// The host-side argument checks of csattn_attn_decode (all but the pointers).
+int attn_decode_check(const char* fn, int B, int Hq, int Hkv, int Lmax, int d, int dtype,
+                      float scale, int max_seq_len, int num_splits);
+
 // Driver entry point for cuTensorMapEncodeTiled (nullptr if unavailable).
 void* tensor_map_encoder();
 
