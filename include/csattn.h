@@ -374,7 +374,7 @@ int csattn_attn_decode_noalloc(const void* q, const void* k_cache, const void* v
  *   block_table device int32 [B, max_pages]; cache_lens device int32 [B]
  *   out        [B, Hq, Tq, d] bf16;  lse NULL or fp32 [B, Hq, Tq] (natural log)
  *   rope_base, rope_layout, scale  as csattn_attn_fwd (applied to q only)
- * Requirements: bf16, d = 128, Hq % Hkv == 0, page_size a multiple of 64 in
+ * Requirements: bf16, d in {64, 128}, Hq % Hkv == 0, page_size a multiple of 64 in
  * [64, 65536], 1 <= Tq <= max_pages * page_size < 2^24 (<= 49152 with RoPE);
  * q, pages and out 16-byte aligned, block_table, cache_lens and lse 4-byte.
  * Device-side errors (CSATTN_ERR_DEVICE_ARG in the status word): a cache_lens[b]

@@ -274,7 +274,7 @@ def test_fwd_host_workspace_size(lib):
     (dict(Hq=6, Hkv=4), -1),
     (dict(dtype=0), -2),
     (dict(dtype=4), -1),
-    (dict(d=64), -2),
+    (dict(d=32), -2),
     (dict(causal=2), -1),
     (dict(rope_layout=0x100), -1),
     (dict(page_size=96), -1),

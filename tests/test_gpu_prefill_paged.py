@@ -77,13 +77,40 @@ def test_prefill_paged_parity(B, Hq, Hkv, Tq, page, lens, base, layout, causal):
     assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-2
 
 
-@pytest.mark.parametrize("page", [64, 128, 384])
-def test_prefill_paged_bit_exact_with_contiguous_chunk(page):
+D64_CASES = [
+    # (B, Hq, Hkv, Tq, page, lens, rope_base, layout, causal): head size 64
+    (2, 4, 4, 200, 64, [0, 150], 10000.0, "split_half", True),
+    (3, 12, 12, 129, 128, [77, 0, 300], 0.0, "split_half", True),
+    (2, 8, 2, 64, 192, [5, 250], 10000.0, "adjacent", False),
+    (1, 6, 2, 1, 64, [500], 10000.0, "split_half", True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tq,page,lens,base,layout,causal", D64_CASES)
+def test_prefill_paged_parity_d64(B, Hq, Hkv, Tq, page, lens, base, layout, causal):
+    d = 64
+    q, _, _, kp, vp, table = _paged_inputs(B, Hq, Hkv, Tq, d, page, lens, base, layout,
+                                           seed=3 * Tq + page + sum(lens))
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=dev())
+    lse = torch.empty(B, Hq, Tq, dtype=torch.float32, device=dev())
+    out = csattn.attn_prefill_paged(q.to(dev()), kp.to(dev()), vp.to(dev()), table.to(dev()),
+                                    lens_d, causal=causal, rope_base=base, rope_layout=layout,
+                                    scale=1.0 / math.sqrt(d), lse=lse)
+    csattn.check_status()
+    ref, ref_lse = OA.prefill_paged(q, kp.double().numpy(), vp.double().numpy(), table.numpy(),
+                                    lens, page, causal=causal, rope_base=base, rope_layout=layout,
+                                    scale=1.0 / math.sqrt(d), operand_dtype="bf16", lse=True)
+    assert_bf16_close(to_np(out), ref, "paged prefill d=64")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-2
+
+
+@pytest.mark.parametrize("page,d", [(64, 128), (128, 128), (384, 128), (64, 64), (256, 64)])
+def test_prefill_paged_bit_exact_with_contiguous_chunk(page, d):
     """Same rows in pages and in a contiguous cache: the paged chunk equals the
     contiguous chunked prefill (keys given rotated) bit for bit."""
-    B, Hq, Hkv, Tq, d, L = 2, 8, 2, 300, 128, 229
+    B, Hq, Hkv, Tq, L = 2, 8, 2, 300, 229
     q, kr, v, kp, vp, table = _paged_inputs(B, Hq, Hkv, Tq, d, page, [L, L], 10000.0,
-                                            "split_half", seed=page)
+                                            "split_half", seed=page + d)
     lens_d = torch.tensor([L, L], dtype=torch.int32, device=dev())
     out_p = csattn.attn_prefill_paged(q.to(dev()), kp.to(dev()), vp.to(dev()), table.to(dev()),
                                       lens_d, rope_base=10000.0)
@@ -119,3 +146,24 @@ def test_prefill_paged_bad_page_and_length_set_device_error():
         csattn.check_status()
     assert e.value.status == -6
     csattn.check_status()
+
+
+def test_prefill_paged_chunk_workload_sampled_rows():
+    """The bench's paged row at full size: llama_chunk_bf16 (1024 queries after 3072
+    cached rows) with the rotated cache in 256-row pages of a shuffled pool; sampled
+    rows of three heads against the contiguous definition."""
+    w = W.WORKLOADS["llama_chunk_bf16"]
+    q, k, v = W.make_chunk_inputs(w)
+    kr = OA.round_to_bf16(OA.rope_rotate(k.double().numpy(), np.arange(w.Tk), w.rope_base))
+    kp, vp, table = W.page_cache(torch.from_numpy(kr).to(torch.bfloat16), v, [w.Tk] * w.B, 256,
+                                 seed=21, spare=3)
+    lens = torch.full((w.B,), w.q_offset, dtype=torch.int32, device=dev())
+    out = csattn.attn_prefill_paged(q.to(dev()), kp.to(dev()), vp.to(dev()), table.to(dev()),
+                                    lens, rope_base=w.rope_base, scale=w.scale)
+    csattn.check_status()
+    oc = out.cpu()
+    for b, h in ((0, 5), (2, 18), (3, 31)):
+        rows = W.sample_query_rows(w.Tq, 96, seed=b * 100 + h + 7)
+        ref = OA.attention_rows(q, k, v, b, h, rows, causal=True, rope_base=w.rope_base,
+                                scale=w.scale, operand_dtype="bf16", q_offset=w.q_offset)
+        assert_bf16_close(oc[b, h, rows].double().numpy(), ref, f"paged chunk b={b} h={h}")

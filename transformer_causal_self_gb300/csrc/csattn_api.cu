@@ -595,7 +595,7 @@ int csattn_attn_prefill_paged(const void* q, const void* k_pages, const void* v_
   if (dtype != CSATTN_BF16)
     return fail(dtype == CSATTN_F32 ? CSATTN_ERR_UNSUPPORTED : CSATTN_ERR_INVALID_ARG,
                 "%s: only bf16 is implemented (dtype %d)", fn, dtype);
-  if (d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d (only 128)", fn, d);
+  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d not in {64,128}", fn, d);
   if (causal != 0 && causal != 1)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
   if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
@@ -656,7 +656,7 @@ int csattn_attn_prefill_paged(const void* q, const void* k_pages, const void* v_
   if (rc != CSATTN_OK) return rc;
   if (tensor_map_encoder() == nullptr)
     return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
-  cudaError_t e = launch_fwd_sm103a_d128(a, k_pages, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fwd_sm103a(a, k_pages, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "attn_prefill_paged: kernel launch");
   return CSATTN_OK;
 }

@@ -54,17 +54,40 @@ struct Cfg {
 };
 
 // O (+)= P V: M=128, N=D, K=128 keys; P from TMEM, V MN-major (rows = keys).
-template <int DK, int D>
+// LIMITED: only the first k_steps 16-key steps.
+template <int DK, int D, bool LIMITED = false>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
-                                         bool accumulate) {
+                                         bool accumulate, int k_steps = BN / 16) {
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
+    if (LIMITED && kk >= k_steps) break;
     umma_ts(d_tmem, p_tmem + 8u * kk, smem_desc_sw128(v_smem + 2048u * kk, BM * 128, 1024),
             Cfg<DK, D>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
+// A paged sequence's last key tile (paged kernel only): its rows past the end
+// (nvalid..BN-1) may hold anything, NaN included, which P = 0 would not cancel.  The
+// rows of the last 16-key step that lie past the end are zeroed here (the steps after
+// it are not issued), out of line so that the MMA thread's loop stays compact.
+template <int D>
+__device__ __noinline__ void v_tail_zero(uint8_t* v_tile, int nvalid) {
+  const int end = 16 * ((nvalid + 15) / 16);
+  for (int kb = 0; kb < D / 64; ++kb)
+    for (int r = nvalid; r < end; ++r)
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(v_tile + kb * BM * 128 + r * 128 + c * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+}
 template <int DK, int D>
+__device__ __noinline__ void pv_tail(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                     bool accumulate, int nvalid) {
+  issue_pv<DK, D, true>(d_tmem, p_tmem, v_smem, accumulate, (nvalid + 15) / 16);
+}
+
+// PAGED: K/V from a paged cache with per-sequence lengths (Params in fwd_units.cuh).
+template <int DK, int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103a_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -130,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok; ++i) {
         const int u = unit_index(i);
         if (u >= p.nUnits) break;
-        const Unit un = decode_unit(p, u);
+        const Unit un = decode_unit<PAGED>(p, u);
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (ok && un.n[x] > 0) {
@@ -147,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (PAGED && un.bad_len) atomicOr(p.status, kStatusDeviceArg);
         for (int j = 0; j < un.n[1] && ok; ++j) {
           for (int t = 0; t < 2; ++t) {
             const uint32_t s = fill % C::NS, use = fill / C::NS;
@@ -156,9 +180,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive_expect_tx(&kv_full[s], t == 0 ? C::Q_BYTES : C::V_BYTES);
             uint8_t* dst = sKV + s * C::TILE_BYTES;
-            for (int kb = 0; kb < (t == 0 ? DK : D) / 64; ++kb)
-              tma_load_3d(dst + kb * C::BLOCK_BYTES, t == 0 ? &tm_k : &tm_v, &kv_full[s], kb * 64,
-                          j * BN, un.b * p.Hkv + un.kvh);
+            if constexpr (!PAGED) {
+              for (int kb = 0; kb < (t == 0 ? DK : D) / 64; ++kb)
+                tma_load_3d(dst + kb * C::BLOCK_BYTES, t == 0 ? &tm_k : &tm_v, &kv_full[s],
+                            kb * 64, j * BN, un.b * p.Hkv + un.kvh);
+            } else {
+              // paged: a box of box_rows rows never crosses a page; a box past the
+              // sequence, or a page index outside the pool (reported), reads zeros
+              for (int r0 = 0; r0 < BN; r0 += p.box_rows) {
+                const int tr = j * BN + r0;
+                int plane = p.num_pages * p.Hkv, prow = 0;
+                if (tr < un.Tk) {
+                  const int page = p.block_table[static_cast<size_t>(un.b) * p.max_pages +
+                                                 tr / p.page_size];
+                  if (page >= 0 && page < p.num_pages)
+                    plane = page * p.Hkv + un.kvh;
+                  else
+                    atomicOr(p.status, kStatusDeviceArg);
+                  prow = tr % p.page_size;
+                }
+                for (int kb = 0; kb < (t == 0 ? DK : D) / 64; ++kb)
+                  tma_load_3d(dst + kb * C::BLOCK_BYTES + r0 * 128, t == 0 ? &tm_k : &tm_v,
+                              &kv_full[s], kb * 64, prow, plane);
+              }
+            }
             ++fill;
           }
         }
@@ -191,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok; ++i) {
         const int u = unit_index(i);
         if (u >= p.nUnits) break;
-        const Unit un = decode_unit(p, u);
+        const Unit un = decode_unit<PAGED>(p, u);
         // first score tiles: S_X(0) = Q_X K_0^T
         const uint32_t s0 = fill % C::NS;
         bool k0_ready = false;
@@ -217,9 +262,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int x = 0; x < 2; ++x) {
             if (j < un.n[x] && wait(&p_full[x], cp[x] & 1)) {
               ++cp[x];
-              if (!v_ready) v_ready = wait(&kv_full[sV], (fV / C::NS) & 1);
+              const bool tail = PAGED && (j + 1) * BN > un.Tk;
+              if (!v_ready) {
+                v_ready = wait(&kv_full[sV], (fV / C::NS) & 1);
+                if (tail && v_ready) v_tail_zero<D>(sKV + sV * C::TILE_BYTES, un.Tk - j * BN);
+              }
               if (v_ready && (j > 0 || cu[x] == 0 || wait(&o_empty[x], (cu[x] - 1) & 1))) {
-                issue_pv<DK, D>(tO[x], tS[x], sKV0 + sV * C::TILE_BYTES, j > 0);
+                if (tail)
+                  pv_tail<DK, D>(tO[x], tS[x], sKV0 + sV * C::TILE_BYTES, j > 0, un.Tk - j * BN);
+                else
+                  issue_pv<DK, D>(tO[x], tS[x], sKV0 + sV * C::TILE_BYTES, j > 0);
                 if (x == 1) tc_commit(&kv_empty[sV]);
                 if (j == un.n[x] - 1) tc_commit(&o_full[x]);
                 if (j + 1 < un.n[x]) {
@@ -265,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i2 = i_from;; ++i2) {
         const int u2 = unit_index(i2);
         if (u2 >= p.nUnits) return;
-        const Unit un2 = decode_unit(p, u2);
+        const Unit un2 = decode_unit<PAGED>(p, u2);
         if ((x ? un2.n[1] : un2.n[0]) == 0) continue;
         if (!warp_wait(&q_full[x], cq & 1, abort_flag, p.status, kWaitNs)) {
           ok = false;
@@ -273,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++cq;
         if (p.rope) {
-          rotate_q_row<DK>(x ? sQ[1] : sQ[0], row, p.q_off + (x ? un2.q0[1] : un2.q0[0]) + row, p.rope,
+          rotate_q_row<DK>(x ? sQ[1] : sQ[0], row,
+                           (PAGED ? un2.q_off : p.q_off) + (x ? un2.q0[1] : un2.q0[0]) + row, p.rope,
                           p.theta);
           fence_proxy_async_smem();
         }
@@ -286,11 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; ok; ++i) {
       const int u = unit_index(i);
       if (u >= p.nUnits) break;
-      const Unit un = decode_unit(p, u);
+      const Unit un = decode_unit<PAGED>(p, u);
       const int n = x ? un.n[1] : un.n[0];
       if (n == 0) continue;
       const int hx = x ? un.h[1] : un.h[0];
       const int qpos = (x ? un.q0[1] : un.q0[0]) + row;
+      // paged: the last visible key of this row relative to tile 0 (one register)
+      const int lim0 = PAGED ? min(p.causal ? un.q_off + qpos : un.Tk - 1, un.Tk - 1) : 0;
 
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
@@ -309,8 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // causal diagonal and ragged tail: keys beyond the row's limit get -inf
         int lim = BN - 1;
-        if (p.causal) lim = min(lim, p.q_off + qpos - j * BN);
-        lim = min(lim, p.Tk - 1 - j * BN);
+        if constexpr (PAGED) {
+          lim = min(lim, lim0 - j * BN);
+        } else {
+          if (p.causal) lim = min(lim, p.q_off + qpos - j * BN);
+          lim = min(lim, p.Tk - 1 - j * BN);
+        }
         if (lim < BN - 1) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
@@ -412,21 +471,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DK>
+template <int DK, bool PAGED>
 cudaError_t launch_v64(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
   constexpr int D = 64;
   using C = Cfg<DK, D>;
   const Params p = make_params(a);
   alignas(64) CUtensorMap tq, tk, tv;
+  // K/V tensor maps: [B*Hkv planes, Tk rows], or the page pool [num_pages*Hkv, page_size]
+  const int kv_rows = PAGED ? a.page_size : a.Tk;
+  const int kv_planes = PAGED ? a.num_pages * a.Hkv : a.B * a.Hkv;
   if (!make_tmap_bf16_3d(&tq, a.q, DK, a.Tq, a.B * a.Hq, BM) ||
-      !make_tmap_bf16_3d(&tk, k_eff, DK, a.Tk, a.B * a.Hkv, BN) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BN))
+      !make_tmap_bf16_3d(&tk, k_eff, DK, kv_rows, kv_planes, p.box_rows) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, kv_rows, kv_planes, p.box_rows))
     return cudaErrorInvalidValue;
   static SmemLimitOnce smem_limit;
-  cudaError_t e = smem_limit.set(fwd_sm103a_kernel<DK, D>, C::SMEM_BYTES);
+  cudaError_t e = smem_limit.set(fwd_sm103a_kernel<DK, D, PAGED>, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = p.nUnits < a.num_sms ? p.nUnits : a.num_sms;
-  fwd_sm103a_kernel<DK, D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv);
+  fwd_sm103a_kernel<DK, D, PAGED><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
 
@@ -437,8 +499,10 @@ cudaError_t launch_v64(const FwdArgs& a, const void* k_eff, cudaStream_t stream)
 cudaError_t launch_fwd_sm103a(const FwdArgs& a, const void* k_eff, cudaStream_t stream) {
   if (a.dv == 128) return launch_fwd_sm103a_d128(a, k_eff, stream);
   if (a.dv != 64) return cudaErrorInvalidValue;
-  if (a.d == 64) return launch_v64<64>(a, k_eff, stream);
-  if (a.d == 128) return launch_v64<128>(a, k_eff, stream);
+  if (a.block_table != nullptr)
+    return a.d == 64 ? launch_v64<64, true>(a, k_eff, stream) : cudaErrorInvalidValue;
+  if (a.d == 64) return launch_v64<64, false>(a, k_eff, stream);
+  if (a.d == 128) return launch_v64<128, false>(a, k_eff, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -43,7 +43,7 @@ struct Params {
   int nUnits;   // all units
   float scale_log2;
   RopeTable theta;
-  // Paged KV cache (d = 128 kernel only; block_table == nullptr otherwise): keys and
+  // Paged KV cache (the kernels' paged instances; block_table == nullptr otherwise): keys and
   // values of sequence b at rows 0..L_b+Tq-1 with L_b = cache_lens[b] (the cached
   // prefix, then the chunk's own rows); row t lives in page block_table[b * max_pages
   // + t / page_size] at offset t % page_size; K/V tensor maps span the page pool

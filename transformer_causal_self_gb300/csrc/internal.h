@@ -29,7 +29,7 @@ struct FwdArgs {
   RopeTable theta;   // valid when rope != 0
   uint32_t* status;  // device status word
   int num_sms;
-  // Paged K/V (bf16, d = dv = 128; block_table == nullptr: k, v are [B, Hkv, Tk, d]).
+  // Paged K/V (bf16, d = dv in {64, 128}; block_table == nullptr: k, v are [B, Hkv, Tk, d]).
   // k, v are pools [num_pages, Hkv, page_size, d] of rotated keys and values; sequence
   // b has cache_lens[b] + Tq rows (Tk and q_off unused), its query row i sits at
   // cache_lens[b] + i; page_size is a multiple of 64.
