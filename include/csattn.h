@@ -125,8 +125,10 @@ size_t csattn_fwd_host_workspace_size(int B, int Hq, int Hkv, int T, int d, int 
  * Other arguments, checks and return codes as csattn_attn_fwd (messages name
  * attn_fwd_host).  Every check runs before the first copy is enqueued.  Asynchronous
  * on `stream`: the internal streams wait for the work already on `stream`, and
- * `stream` waits for the last copy out; the host buffers must stay valid until then.
- * Concurrent calls from several host threads are serialised while they enqueue.
+ * `stream` waits for the last copy out; the host buffers must stay valid until then
+ * (also after an error returned once copies were enqueued: `stream` then waits for
+ * everything already enqueued).  Concurrent calls from several host threads are
+ * serialised while they enqueue.
  */
 int csattn_attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* out_h, int B,
                          int Hq, int Hkv, int T, int d, int dtype, int causal, float rope_base,

@@ -80,6 +80,15 @@ int pipe_of_device(Pipe** out) {
   return CSATTN_OK;
 }
 
+// After a failure part-way through a call's enqueue: the caller's stream still waits
+// for everything already enqueued on the internal streams (so the buffers stay in use
+// until that work is done, as after a successful call), and the error code is returned.
+int abandon(Pipe& p, cudaStream_t caller, int rc) {
+  for (cudaStream_t s : {p.h2d, p.cmp, p.d2h})
+    if (cudaEventRecord(p.end, s) == cudaSuccess) (void)cudaStreamWaitEvent(caller, p.end, 0);
+  return rc;
+}
+
 size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 size_t elem_size(int dtype) {
@@ -160,7 +169,7 @@ int csattn_attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void
   if ((e = cudaEventRecord(p.start, caller)) != cudaSuccess) return hfail_cuda(e, "event record");
   for (cudaStream_t s : {p.h2d, p.cmp, p.d2h})
     if ((e = cudaStreamWaitEvent(s, p.start, 0)) != cudaSuccess)
-      return hfail_cuda(e, "stream wait");
+      return abandon(p, caller, hfail_cuda(e, "stream wait"));
   const size_t q_pair = static_cast<size_t>(rep) * T * d * esz;  // bytes of q (or out) per pair
   const size_t k_pair = static_cast<size_t>(T) * d * esz;        // bytes of k (or v) per pair
   const size_t l_pair = static_cast<size_t>(rep) * T * 4;        // bytes of lse per pair
@@ -179,26 +188,26 @@ int csattn_attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void
                              cudaMemcpyHostToDevice, p.h2d)) != cudaSuccess ||
         (e = cudaEventRecord(p.in[c], p.h2d)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(p.cmp, p.in[c], 0)) != cudaSuccess)
-      return hfail_cuda(e, "host-to-device copy");
+      return abandon(p, caller, hfail_cuda(e, "host-to-device copy"));
     const size_t wsz = csattn_fwd_workspace_size(np, rep, 1, T, d, dtype, rope_base);
     rc = csattn_attn_fwd(dq + qo, dk + ko, dv + ko, dout + qo, np, rep, 1, T, d, dtype, causal,
                          rope_base, rope_layout, scale, lse_h != nullptr ? dlse + lo / 4 : nullptr,
                          wsz > 0 ? dkrot + ko : nullptr, wsz, p.cmp);
-    if (rc != CSATTN_OK) return rc;
+    if (rc != CSATTN_OK) return abandon(p, caller, rc);
     if ((e = cudaEventRecord(p.done[c], p.cmp)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(p.d2h, p.done[c], 0)) != cudaSuccess ||
         (e = cudaMemcpyAsync(static_cast<uint8_t*>(out_h) + qo, dout + qo, qs,
                              cudaMemcpyDeviceToHost, p.d2h)) != cudaSuccess)
-      return hfail_cuda(e, "device-to-host copy");
+      return abandon(p, caller, hfail_cuda(e, "device-to-host copy"));
     if (lse_h != nullptr &&
         (e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_h) + lo,
                              reinterpret_cast<uint8_t*>(dlse) + lo, ls, cudaMemcpyDeviceToHost,
                              p.d2h)) != cudaSuccess)
-      return hfail_cuda(e, "device-to-host copy (lse)");
+      return abandon(p, caller, hfail_cuda(e, "device-to-host copy (lse)"));
   }
   if ((e = cudaEventRecord(p.end, p.d2h)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(caller, p.end, 0)) != cudaSuccess)
-    return hfail_cuda(e, "final wait");
+    return abandon(p, caller, hfail_cuda(e, "final wait"));
   return CSATTN_OK;
 }
 
@@ -266,7 +275,7 @@ int csattn_attn_decode_host(const void* q_h, const void* k_cache_h, const void* 
   if ((e = cudaEventRecord(p.start, caller)) != cudaSuccess) return hfail_cuda(e, "event record");
   for (cudaStream_t s : {p.h2d, p.cmp, p.d2h})
     if ((e = cudaStreamWaitEvent(s, p.start, 0)) != cudaSuccess)
-      return hfail_cuda(e, "stream wait");
+      return abandon(p, caller, hfail_cuda(e, "stream wait"));
   for (int c = 0; c < n; ++c) {
     const int b0 = static_cast<int>(static_cast<long long>(B) * c / n);
     const int b1 = static_cast<int>(static_cast<long long>(B) * (c + 1) / n);
@@ -276,7 +285,7 @@ int csattn_attn_decode_host(const void* q_h, const void* k_cache_h, const void* 
                              q_seq * nb, cudaMemcpyHostToDevice, p.h2d)) != cudaSuccess ||
         (e = cudaMemcpyAsync(dlens + b0, seq_lens_h + b0, static_cast<size_t>(nb) * 4,
                              cudaMemcpyHostToDevice, p.h2d)) != cudaSuccess)
-      return hfail_cuda(e, "host-to-device copy");
+      return abandon(p, caller, hfail_cuda(e, "host-to-device copy"));
     // only the rows the decode reads: rows 0..L_b-1 of every KV head of sequence b
     for (int b = b0; b < b1; ++b) {
       const int L = seq_lens_h[b];
@@ -288,24 +297,24 @@ int csattn_attn_decode_host(const void* q_h, const void* k_cache_h, const void* 
           (e = cudaMemcpy2DAsync(dv + off, c_head, static_cast<const uint8_t*>(v_cache_h) + off,
                                  c_head, row * L, Hkv, cudaMemcpyHostToDevice, p.h2d)) !=
               cudaSuccess)
-        return hfail_cuda(e, "host-to-device copy (cache rows)");
+        return abandon(p, caller, hfail_cuda(e, "host-to-device copy (cache rows)"));
     }
     if ((e = cudaEventRecord(p.in[c], p.h2d)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(p.cmp, p.in[c], 0)) != cudaSuccess)
-      return hfail_cuda(e, "event");
+      return abandon(p, caller, hfail_cuda(e, "event"));
     rc = csattn_attn_decode(dq + q_seq * b0, dk + c_seq * b0, dv + c_seq * b0, dlens + b0,
                             dout + q_seq * b0, nb, Hq, Hkv, Lmax, d, dtype, scale, chunk_max,
                             num_splits, dpart, part_bytes, p.cmp);
-    if (rc != CSATTN_OK) return rc;
+    if (rc != CSATTN_OK) return abandon(p, caller, rc);
     if ((e = cudaEventRecord(p.done[c], p.cmp)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(p.d2h, p.done[c], 0)) != cudaSuccess ||
         (e = cudaMemcpyAsync(static_cast<uint8_t*>(out_h) + q_seq * b0, dout + q_seq * b0,
                              q_seq * nb, cudaMemcpyDeviceToHost, p.d2h)) != cudaSuccess)
-      return hfail_cuda(e, "device-to-host copy");
+      return abandon(p, caller, hfail_cuda(e, "device-to-host copy"));
   }
   if ((e = cudaEventRecord(p.end, p.d2h)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(caller, p.end, 0)) != cudaSuccess)
-    return hfail_cuda(e, "final wait");
+    return abandon(p, caller, hfail_cuda(e, "final wait"));
   return CSATTN_OK;
 }
 
