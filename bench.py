@@ -22,7 +22,6 @@ import csv
 import hashlib
 import io
 import json
-import math
 import os
 import statistics
 import subprocess

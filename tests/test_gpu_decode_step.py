@@ -1,6 +1,5 @@
 """Decode with the cache append fused in (csattn_attn_decode_step) against the
 float64 oracle's decode_step, plus the cache rows it writes and leaves alone."""
-import math
 
 import numpy as np
 import pytest

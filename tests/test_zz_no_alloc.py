@@ -11,7 +11,6 @@ next).  The file is named to be collected last.
 """
 import math
 
-import numpy as np
 import pytest
 import torch
 
