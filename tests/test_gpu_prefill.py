@@ -193,3 +193,26 @@ def test_long_workload_sampled():
     w = W.WORKLOADS["long_gqa_bf16"]
     got, ref = _sampled(w, heads=[(0, 0), (0, 13), (0, 30)], n_rows=400)
     assert_bf16_close(got, ref, "long")
+
+
+# ------------------------------------------------------------------ largest sizes
+
+def test_bf16_at_the_largest_rope_position():
+    """T = 49152, the longest sequence RoPE accepts (positions up to 49151, angles up to
+    49151 rad for the first channel pair): sampled rows, the last row included."""
+    w = W.PrefillWorkload("maxpos", B=1, Hq=2, Hkv=1, T=49152, d=128, dtype="bf16",
+                          rope_base=10000.0, scale=1.0 / math.sqrt(128), seed=17)
+    got, ref = _sampled(w, heads=[(0, 0), (0, 1)], n_rows=96)
+    assert_bf16_close(got, ref, "T=49152")
+
+
+def test_fp32_at_the_largest_rope_position():
+    w = W.PrefillWorkload("maxpos32", B=1, Hq=2, Hkv=1, T=49152, d=16, dtype="f32",
+                          rope_base=10000.0, scale=0.25, causal=True, seed=18)
+    q, k, v = W.make_prefill_inputs(w)
+    out = _run(q, k, v, causal=True, rope_base=w.rope_base, scale=w.scale).cpu()
+    for h in (0, 1):
+        rows = W.sample_query_rows(w.T, 64, seed=h + 3)
+        ref = OA.attention_rows(q, k, v, 0, h, rows, causal=True, rope_base=w.rope_base,
+                                scale=w.scale, operand_dtype="f32")
+        assert_f32_close(out[0, h, rows].double().numpy(), ref, f"fp32 T=49152 h={h}")
