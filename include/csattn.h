@@ -285,8 +285,9 @@ int csattn_attn_decode_host(const void* q_h, const void* k_cache_h, const void* 
  *              <= max_pages * page_size
  *   workspace  >= csattn_decode_workspace_size(B, Hq, max_pages * page_size, d,
  *              num_splits) bytes
- * page_size is a multiple of 64 (one decode tile never crosses a page).  Pages
- * are read only for rows < seq_lens[b]; a page index outside [0, num_pages)
+ * page_size is 16, 32 (the page is one TMA box) or a multiple of 64 up to 65536
+ * (a 64-row decode tile never crosses a page).  Pages are read only for rows
+ * < seq_lens[b]; a page index outside [0, num_pages)
  * raises CSATTN_ERR_DEVICE_ARG in the status word and those rows read as zeros.
  * Other errors and requirements as csattn_attn_decode.
  */
@@ -376,8 +377,8 @@ int csattn_attn_decode_noalloc(const void* q, const void* k_cache, const void* v
  *   block_table device int32 [B, max_pages]; cache_lens device int32 [B]
  *   out        [B, Hq, Tq, d] bf16;  lse NULL or fp32 [B, Hq, Tq] (natural log)
  *   rope_base, rope_layout, scale  as csattn_attn_fwd (applied to q only)
- * Requirements: bf16, d in {64, 128}, Hq % Hkv == 0, page_size a multiple of 64 in
- * [64, 65536], 1 <= Tq <= max_pages * page_size < 2^24 (<= 49152 with RoPE);
+ * Requirements: bf16, d in {64, 128}, Hq % Hkv == 0, page_size 16, 32 or a multiple
+ * of 64 in [64, 65536], 1 <= Tq <= max_pages * page_size < 2^24 (<= 49152 with RoPE);
  * q, pages and out 16-byte aligned, block_table, cache_lens and lse 4-byte.
  * Device-side errors (CSATTN_ERR_DEVICE_ARG in the status word): a cache_lens[b]
  * outside [0, max_pages * page_size - Tq] (that sequence then runs as if L = 0),
@@ -415,7 +416,8 @@ int csattn_cache_append(const void* k_new, const void* v_new, void* k_cache, voi
  * csattn_cache_append into paged caches [num_pages, Hkv, page_size, d]: row r of
  * sequence b lives in page block_table[b * max_pages + r / page_size] at offset
  * r % page_size (the layout csattn_attn_decode_paged reads); the cache of a
- * sequence holds max_pages * page_size rows.  page_size is a multiple of 64.  A
+ * sequence holds max_pages * page_size rows.  page_size is 16, 32 or a multiple of
+ * 64 in [64, 65536].  A
  * page index outside [0, num_pages) raises CSATTN_ERR_DEVICE_ARG and that row is
  * not written.
  */

@@ -162,6 +162,7 @@ def test_decode_rejects_invalid_arguments(lib, kw, status):
     (dict(table=FAKE + 2), -1),
     (dict(page_size=0), -1),
     (dict(page_size=96), -1),
+    (dict(page_size=24), -1),
     (dict(num_pages=0), -1),
     (dict(max_pages=0), -1),
     (dict(max_len=4 * 128 + 1), -1),
@@ -278,7 +279,8 @@ def test_fwd_host_workspace_size(lib):
     (dict(causal=2), -1),
     (dict(rope_layout=0x100), -1),
     (dict(page_size=96), -1),
-    (dict(page_size=32), -1),
+    (dict(page_size=48), -1),
+    (dict(page_size=8), -1),
     (dict(num_pages=0), -1),
     (dict(max_pages=0), -1),
     (dict(Tq=600, max_pages=4, page_size=128), -1),
@@ -327,6 +329,7 @@ def test_cache_append_rejects_invalid_arguments(lib, kw, status):
 @pytest.mark.parametrize("kw,status", [
     (dict(table=None), -1),
     (dict(page_size=96), -1),
+    (dict(page_size=20), -1),
     (dict(num_pages=0), -1),
     (dict(Tn=600), -1),
     (dict(d=32), -2),

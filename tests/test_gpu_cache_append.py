@@ -65,11 +65,12 @@ def test_cache_append_contiguous(d, Hkv, Tn, base, layout):
     _check_rows(kc_d.cpu(), vc_d.cpu(), wk, wv, written)
 
 
-def test_cache_append_paged_then_decode():
+@pytest.mark.parametrize("page", [128, 16])
+def test_cache_append_paged_then_decode(page):
     """A 1024-token prompt appended in three chunks into shuffled pages, then a paged
     decode over ragged prefixes of it equals the oracle's decode over the same pages."""
-    B, Hq, Hkv, d, page = 3, 16, 4, 128, 128
-    n_lp = 8
+    B, Hq, Hkv, d = 3, 16, 4, 128
+    n_lp = 1024 // page
     g = _g(11)
     k = torch.randn(B, Hkv, 1024, d, generator=g).to(torch.bfloat16)
     v = torch.randn(B, Hkv, 1024, d, generator=g).to(torch.bfloat16)

@@ -48,6 +48,8 @@ def _paged(B, Hq, Hkv, d, page, n_lp, lens, spare, seed):
     (128, 32, 8, 128, 6),
     (64, 6, 2, 256, 3),
     (128, 16, 1, 64, 20),
+    (128, 8, 2, 16, 50),     # 16-row pages: four pages per 64-row tile
+    (64, 4, 4, 32, 21),      # 32-row pages, a logical cache that ends mid-tile
 ])
 def test_decode_paged_parity(d, Hq, Hkv, page, n_lp):
     B = 6

@@ -56,6 +56,8 @@ CASES = [
     (2, 4, 2, 100, 128, [30, 129], 500000.0, "split_half", False),
     (4, 32, 8, 256, 256, [0, 511, 1024, 1777], 10000.0, "split_half", True),
     (2, 3, 1, 300, 64, [17, 0], 10000.0, "split_half", True),
+    (2, 4, 2, 150, 16, [33, 200], 10000.0, "split_half", True),   # 16-row pages
+    (2, 8, 2, 97, 32, [0, 131], 10000.0, "adjacent", False),      # 32-row pages
 ]
 
 
@@ -83,6 +85,7 @@ D64_CASES = [
     (3, 12, 12, 129, 128, [77, 0, 300], 0.0, "split_half", True),
     (2, 8, 2, 64, 192, [5, 250], 10000.0, "adjacent", False),
     (1, 6, 2, 1, 64, [500], 10000.0, "split_half", True),
+    (2, 4, 2, 130, 16, [70, 3], 10000.0, "split_half", True),
 ]
 
 
@@ -104,7 +107,8 @@ def test_prefill_paged_parity_d64(B, Hq, Hkv, Tq, page, lens, base, layout, caus
     assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-2
 
 
-@pytest.mark.parametrize("page,d", [(64, 128), (128, 128), (384, 128), (64, 64), (256, 64)])
+@pytest.mark.parametrize("page,d", [(64, 128), (128, 128), (384, 128), (64, 64), (256, 64),
+                                    (16, 128), (32, 64)])
 def test_prefill_paged_bit_exact_with_contiguous_chunk(page, d):
     """Same rows in pages and in a contiguous cache: the paged chunk equals the
     contiguous chunked prefill (keys given rotated) bit for bit."""

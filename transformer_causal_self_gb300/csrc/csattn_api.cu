@@ -68,6 +68,13 @@ int device_info(uint32_t** status, int* num_sms) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Page sizes of the paged caches: 16 or 32 rows (one TMA box per page), or a
+// multiple of 64 rows up to 65536 (boxes of 64 or 128 rows inside a page).
+bool valid_page_size(int page_size) {
+  return page_size == 16 || page_size == 32 ||
+         (page_size >= 64 && page_size % 64 == 0 && page_size <= 65536);
+}
+
 // theta_p = base^(-2p/d), p < d/2, split into float hi + lo (hi + lo = theta
 // to about 2^-48 relative).
 void rope_table(RopeTable* t, int d, double base) {
@@ -561,9 +568,10 @@ int csattn_attn_decode_paged(const void* q, const void* k_pages, const void* v_p
     return fail(CSATTN_ERR_INVALID_ARG, "%s: block_table must be non-null", fn);
   if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: block_table must be 4-byte aligned", fn);
-  if (page_size < 64 || page_size % 64 != 0 || page_size > 65536)
-    return fail(CSATTN_ERR_INVALID_ARG, "%s: page_size=%d must be a multiple of 64 in [64, 65536]",
-                fn, page_size);
+  if (!valid_page_size(page_size))
+    return fail(CSATTN_ERR_INVALID_ARG,
+                "%s: page_size=%d must be 16, 32 or a multiple of 64 in [64, 65536]", fn,
+                page_size);
   if (num_pages < 1 || max_pages < 1)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: num_pages=%d and max_pages=%d must be >= 1", fn,
                 num_pages, max_pages);
@@ -602,9 +610,10 @@ int csattn_attn_prefill_paged(const void* q, const void* k_pages, const void* v_
     return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown rope_layout %d", fn, rope_layout);
   if (!std::isfinite(rope_base) || !std::isfinite(scale))
     return fail(CSATTN_ERR_INVALID_ARG, "%s: rope_base and scale must be finite", fn);
-  if (page_size < 64 || page_size % 64 != 0 || page_size > 65536)
-    return fail(CSATTN_ERR_INVALID_ARG, "%s: page_size=%d must be a multiple of 64 in [64, 65536]",
-                fn, page_size);
+  if (!valid_page_size(page_size))
+    return fail(CSATTN_ERR_INVALID_ARG,
+                "%s: page_size=%d must be 16, 32 or a multiple of 64 in [64, 65536]", fn,
+                page_size);
   if (num_pages < 1 || max_pages < 1)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: num_pages=%d and max_pages=%d must be >= 1", fn,
                 num_pages, max_pages);
@@ -779,9 +788,10 @@ int csattn_cache_append_paged(const void* k_new, const void* v_new, void* k_page
     return fail(CSATTN_ERR_INVALID_ARG, "%s: block_table must be non-null", fn);
   if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: block_table must be 4-byte aligned", fn);
-  if (page_size < 64 || page_size % 64 != 0 || page_size > 65536)
-    return fail(CSATTN_ERR_INVALID_ARG, "%s: page_size=%d must be a multiple of 64 in [64, 65536]",
-                fn, page_size);
+  if (!valid_page_size(page_size))
+    return fail(CSATTN_ERR_INVALID_ARG,
+                "%s: page_size=%d must be 16, 32 or a multiple of 64 in [64, 65536]", fn,
+                page_size);
   if (num_pages < 1 || max_pages < 1)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: num_pages=%d and max_pages=%d must be >= 1", fn,
                 num_pages, max_pages);

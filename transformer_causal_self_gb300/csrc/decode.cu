@@ -47,6 +47,7 @@ struct DParams {
   int len_add;
   const int32_t* block_table;  // paged cache, or nullptr
   int page_size, num_pages, max_pages;
+  int box_rows;                // paged: rows per TMA box (min(64, page_size))
   float* part_o;
   float* part_ml;
   uint32_t* status;
@@ -137,22 +138,35 @@ __global__ void __launch_bounds__(kThreads)
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         uint8_t* kdst = smem + s * C::STAGE_BYTES;
         uint8_t* vdst = kdst + C::TILE_BYTES;
-        int row = k_begin + t * KT, zz = z;
-        if (p.block_table != nullptr) {
-          // a 64-row tile never crosses a page (page_size and the tile start are
-          // multiples of 64); a page index outside the pool reads zeros (the plane
-          // coordinate is past the tensor map) and is reported
-          int page = p.block_table[static_cast<size_t>(b) * p.max_pages + row / p.page_size];
-          if (page < 0 || page >= p.num_pages) {
-            atomicOr(p.status, kStatusDeviceArg);
-            page = p.num_pages;
+        const int row = k_begin + t * KT;
+        if (p.block_table == nullptr) {
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &full[s], kb * 64, row, z);
+            tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &full[s], kb * 64, row, z);
           }
-          zz = page * p.Hkv + kvh;
-          row = row % p.page_size;
-        }
-        for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &full[s], kb * 64, row, zz);
-          tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &full[s], kb * 64, row, zz);
+        } else {
+          // paged: boxes of box_rows rows (64, or the page size when it is 16 or 32)
+          // never cross a page; a box past the sequence, or a page index outside the
+          // pool (reported), reads zeros (its plane coordinate is past the tensor map)
+          for (int r0 = 0; r0 < KT; r0 += p.box_rows) {
+            const int tr = row + r0;
+            int plane = p.num_pages * p.Hkv, prow = 0;
+            if (tr < L) {
+              const int page =
+                  p.block_table[static_cast<size_t>(b) * p.max_pages + tr / p.page_size];
+              if (page >= 0 && page < p.num_pages)
+                plane = page * p.Hkv + kvh;
+              else
+                atomicOr(p.status, kStatusDeviceArg);
+              prow = tr % p.page_size;
+            }
+            for (int kb = 0; kb < C::KB; ++kb) {
+              tma_load_3d(kdst + kb * C::BLOCK_BYTES + r0 * 128, &tm_k, &full[s], kb * 64, prow,
+                          plane);
+              tma_load_3d(vdst + kb * C::BLOCK_BYTES + r0 * 128, &tm_v, &full[s], kb * 64, prow,
+                          plane);
+            }
+          }
         }
         ++issued;
       }
@@ -387,6 +401,7 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   p.page_size = a.page_size;
   p.num_pages = a.num_pages;
   p.max_pages = a.max_pages;
+  p.box_rows = a.page_size > 0 && a.page_size < KT ? a.page_size : KT;
   p.part_o = a.part_o;
   p.part_ml = a.part_ml;
   p.status = a.status;
@@ -403,8 +418,9 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   alignas(64) CUtensorMap tk, tv;
   const int rows = a.block_table != nullptr ? a.page_size : a.Lmax;
   const int planes = a.block_table != nullptr ? a.num_pages * a.Hkv : a.B * a.Hkv;
-  if (!make_tmap_bf16_3d(&tk, a.k_cache, D, rows, planes, KT) ||
-      !make_tmap_bf16_3d(&tv, a.v_cache, D, rows, planes, KT))
+  const int box = a.block_table != nullptr ? p.box_rows : KT;
+  if (!make_tmap_bf16_3d(&tk, a.k_cache, D, rows, planes, box) ||
+      !make_tmap_bf16_3d(&tv, a.v_cache, D, rows, planes, box))
     return cudaErrorInvalidValue;
   static SmemLimitOnce smem_limit;
   cudaError_t e = smem_limit.set(decode_bf16_kernel<D>, C::SMEM_BYTES);

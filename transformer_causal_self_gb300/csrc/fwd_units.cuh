@@ -51,7 +51,7 @@ struct Params {
   const int32_t* cache_lens;
   const int32_t* block_table;
   int page_size, num_pages, max_pages;
-  int box_rows;  // rows per K/V TMA box: 128, or 64 when page_size is an odd multiple of 64
+  int box_rows;  // rows per K/V TMA box: 128, 64, or the page size (16, 32)
 };
 
 struct Unit {
@@ -262,7 +262,10 @@ inline Params make_params(const FwdArgs& a) {
   p.page_size = a.page_size;
   p.num_pages = a.num_pages;
   p.max_pages = a.max_pages;
-  p.box_rows = (a.block_table != nullptr && a.page_size % BN != 0) ? 64 : BN;
+  // rows per K/V box: 128, 64 for an odd multiple of 64, else the page (16 or 32 rows)
+  p.box_rows = a.block_table == nullptr || a.page_size % BN == 0
+                   ? BN
+                   : (a.page_size % 64 == 0 ? 64 : a.page_size);
   return p;
 }
 
