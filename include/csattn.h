@@ -381,16 +381,31 @@ int csattn_attn_decode_noalloc(const void* q, const void* k_cache, const void* v
  * of 64 in [64, 65536], 1 <= Tq <= max_pages * page_size < 2^24 (<= 49152 with RoPE);
  * q, pages and out 16-byte aligned, block_table, cache_lens and lse 4-byte.
  * Device-side errors (CSATTN_ERR_DEVICE_ARG in the status word): a cache_lens[b]
- * outside [0, max_pages * page_size - Tq] (that sequence then runs as if L = 0),
- * a page index outside [0, num_pages) for a row < L + Tq (those rows read as
- * zeros).  Cache rows at or past L + Tq are never used, whatever they hold.
- * Asynchronous on `stream`; no workspace.
+ * outside [0, max_pages * page_size - Tq] (that sequence's output is then not
+ * meaningful; nothing is read or written out of bounds), a page index outside
+ * [0, num_pages) for a row < L + Tq (those rows read as zeros).  Cache rows at or
+ * past L + Tq are never used, whatever they hold.
+ *   workspace  >= csattn_prefill_paged_workspace_size() bytes, 16-byte aligned
+ *              (may be NULL when that is 0, i.e. for pages of 64 rows or more);
+ *              16- and 32-row pages are gathered into it first, because a 128-row
+ *              tile of such pages would take 4 or 8 TMA boxes in the kernel.
+ * Asynchronous on `stream`.
  */
 int csattn_attn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
                               const int32_t* block_table, const int32_t* cache_lens, void* out,
                               int B, int Hq, int Hkv, int Tq, int page_size, int num_pages,
                               int max_pages, int d, int dtype, int causal, float rope_base,
-                              int rope_layout, float scale, float* lse, void* stream);
+                              int rope_layout, float scale, float* lse, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of device workspace csattn_attn_prefill_paged needs: 0 for pages of 64 rows
+ * or more; for 16- and 32-row pages two contiguous pools [B, Hkv, Lpad, d] bf16
+ * (Lpad = max_pages * page_size rounded up to 128) and a B-entry block table, into
+ * which each sequence's rows are gathered before the prefill kernel runs.
+ */
+size_t csattn_prefill_paged_workspace_size(int B, int Hkv, int page_size, int max_pages,
+                                           int d);
 
 /*
  * Appends Tn tokens per sequence to the KV caches (a prefill chunk written into

@@ -289,17 +289,20 @@ def test_fwd_host_workspace_size(lib):
     (dict(lens=FAKE + 2), -1),
     (dict(lse=FAKE + 2), -1),
     (dict(out=FAKE + 8), -1),
+    (dict(B=70000, Hq=2, Hkv=2), -2),
+    (dict(page_size=16, max_pages=32), -5),
+    (dict(page_size=32, max_pages=16, ws=FAKE, ws_bytes=1024), -5),
 ])
 def test_prefill_paged_rejects_invalid_arguments(lib, kw, status):
     a = dict(q=FAKE, k=FAKE, v=FAKE, table=FAKE, lens=FAKE, out=FAKE, B=2, Hq=8, Hkv=2, Tq=256,
              page_size=128, num_pages=16, max_pages=4, d=128, dtype=1, causal=1, rope_base=0.0,
-             rope_layout=0, scale=0.0, lse=None)
+             rope_layout=0, scale=0.0, lse=None, ws=None, ws_bytes=0)
     a.update(kw)
     rc = lib.csattn_attn_prefill_paged(a["q"], a["k"], a["v"], a["table"], a["lens"], a["out"],
                                        a["B"], a["Hq"], a["Hkv"], a["Tq"], a["page_size"],
                                        a["num_pages"], a["max_pages"], a["d"], a["dtype"],
                                        a["causal"], a["rope_base"], a["rope_layout"], a["scale"],
-                                       a["lse"], None)
+                                       a["lse"], a["ws"], a["ws_bytes"], None)
     assert rc == status, lib.csattn_last_error()
     assert b"attn_prefill_paged" in lib.csattn_last_error()
 
@@ -423,3 +426,13 @@ def test_product_path_does_not_import_oracle():
                 with open(os.path.join(dirpath, f)) as fh:
                     src = fh.read()
                 assert "oracle" not in re.findall(r"^\s*(?:from|import)\s+(\w+)", src, re.M), f
+
+
+def test_prefill_paged_workspace_size(lib):
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert lib.csattn_prefill_paged_workspace_size(4, 8, 128, 32, 128) == 0
+    assert lib.csattn_prefill_paged_workspace_size(4, 8, 64, 32, 128) == 0
+    lpad = (100 * 16 + 127) // 128 * 128
+    assert lib.csattn_prefill_paged_workspace_size(4, 8, 16, 100, 128) == \
+        2 * al(4 * 8 * lpad * 128 * 2) + al(16)
+    assert lib.csattn_prefill_paged_workspace_size(0, 8, 16, 100, 128) == 0

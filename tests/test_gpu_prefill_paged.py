@@ -126,8 +126,9 @@ def test_prefill_paged_bit_exact_with_contiguous_chunk(page, d):
     assert torch.equal(out_p, out_c), float((out_p.float() - out_c.float()).abs().max())
 
 
-def test_prefill_paged_bad_page_and_length_set_device_error():
-    B, Hq, Hkv, Tq, d, page = 3, 4, 2, 100, 128, 128
+@pytest.mark.parametrize("page", [128, 16])
+def test_prefill_paged_bad_page_and_length_set_device_error(page):
+    B, Hq, Hkv, Tq, d = 3, 4, 2, 100, 128
     lens = [50, 200, 10]
     q, _, _, kp, vp, table = _paged_inputs(B, Hq, Hkv, Tq, d, page, lens, 0.0, "split_half",
                                            seed=11)

@@ -63,7 +63,8 @@ _SIGNATURES = {
     "csattn_attn_decode_paged": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _c_int, _c_int, _vp,
                                                                     _c_size, _vp]),
     "csattn_attn_prefill_paged": (_c_int, [_vp] * 6 + [_c_int] * 10 + [_c_float, _c_int, _c_float,
-                                                                     _vp, _vp]),
+                                                                     _vp, _vp, _c_size, _vp]),
+    "csattn_prefill_paged_workspace_size": (_c_size, [_c_int] * 5),
     "csattn_cache_append": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _vp]),
     "csattn_cache_append_paged": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _c_int, _vp]),
     "csattn_check_status": (_c_int, [_vp]),
@@ -453,7 +454,7 @@ def attn_prefill_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Te
                        out: Optional[torch.Tensor] = None, *, causal: bool = True,
                        rope_base: float = 0.0, scale: float = 0.0,
                        rope_layout: str = "split_half", lse: Optional[torch.Tensor] = None,
-                       stream=None) -> torch.Tensor:
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Chunk prefill over a paged cache (C: csattn_attn_prefill_paged).
 
     q [B,Hq,Tq,d] (not rotated; row i of sequence b sits at cache_lens[b] + i);
@@ -470,12 +471,17 @@ def attn_prefill_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Te
         out = torch.empty_like(q)
     _need_cuda(out)
     lib = load_library()
+    need = int(lib.csattn_prefill_paged_workspace_size(B, Hkv, page_size, max_pages, d))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(lib.csattn_attn_prefill_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
                                          block_table.data_ptr(), cache_lens.data_ptr(),
                                          out.data_ptr(), B, Hq, Hkv, Tq, page_size, num_pages,
                                          max_pages, d, _dtype_code(q), int(bool(causal)),
                                          float(rope_base), _ROPE_LAYOUT[rope_layout],
                                          float(scale), lse.data_ptr() if lse is not None else None,
+                                         workspace.data_ptr() if workspace is not None else None,
+                                         workspace.numel() if workspace is not None else 0,
                                          _stream_handle(stream)))
     return out
 

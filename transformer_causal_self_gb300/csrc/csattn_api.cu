@@ -68,6 +68,8 @@ int device_info(uint32_t** status, int* num_sms) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 // Page sizes of the paged caches: 16 or 32 rows (one TMA box per page), or a
 // multiple of 64 rows up to 65536 (boxes of 64 or 128 rows inside a page).
 bool valid_page_size(int page_size) {
@@ -586,11 +588,20 @@ int csattn_attn_decode_paged(const void* q, const void* k_pages, const void* v_p
                      block_table, page_size, num_pages, max_pages);
 }
 
+size_t csattn_prefill_paged_workspace_size(int B, int Hkv, int page_size, int max_pages,
+                                           int d) {
+  if (B < 1 || Hkv < 1 || max_pages < 1 || d < 1 || page_size < 1 || page_size >= 64) return 0;
+  const size_t lpad = (static_cast<size_t>(max_pages) * page_size + 127) / 128 * 128;
+  const size_t pool = static_cast<size_t>(B) * Hkv * lpad * d * 2;
+  return 2 * align256(pool) + align256(static_cast<size_t>(B) * 4);
+}
+
 int csattn_attn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
                               const int32_t* block_table, const int32_t* cache_lens, void* out,
                               int B, int Hq, int Hkv, int Tq, int page_size, int num_pages,
                               int max_pages, int d, int dtype, int causal, float rope_base,
-                              int rope_layout, float scale, float* lse, void* stream) {
+                              int rope_layout, float scale, float* lse, void* workspace,
+                              size_t workspace_bytes, void* stream) {
   const char* fn = "attn_prefill_paged";
   if (q == nullptr || k_pages == nullptr || v_pages == nullptr || block_table == nullptr ||
       cache_lens == nullptr || out == nullptr)
@@ -629,13 +640,18 @@ int csattn_attn_prefill_paged(const void* q, const void* k_pages, const void* v_
     return fail(CSATTN_ERR_UNSUPPORTED,
                 "%s: RoPE supports positions < %d (max_pages * page_size = %lld)", fn,
                 kMaxRopePositions, lmax);
-  if (static_cast<long long>(B) * Hq > (1LL << 31) - 1)
-    return fail(CSATTN_ERR_UNSUPPORTED, "%s: B*Hq too large", fn);
+  if (static_cast<long long>(B) * Hq > (1LL << 31) - 1 || B > 65535)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: B=%d too large", fn, B);
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(block_table) & 3u) != 0 ||
       (reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0 ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  const size_t need = csattn_prefill_paged_workspace_size(B, Hkv, page_size, max_pages, d);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return fail(CSATTN_ERR_WORKSPACE,
+                "%s: %d-row pages need a 16-byte aligned workspace of %zu bytes (got %zu)", fn,
+                page_size, need, workspace_bytes);
 
   FwdArgs a{};
   a.q = q;
@@ -665,12 +681,30 @@ int csattn_attn_prefill_paged(const void* q, const void* k_pages, const void* v_
   if (rc != CSATTN_OK) return rc;
   if (tensor_map_encoder() == nullptr)
     return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
-  cudaError_t e = launch_fwd_sm103a(a, k_pages, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (need > 0) {
+    // small pages: gather each sequence's rows into one page of its own first
+    const int lpad = static_cast<int>((lmax + 127) / 128 * 128);
+    const size_t pool = static_cast<size_t>(B) * Hkv * lpad * d * 2;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* kg = ws;
+    void* vg = ws + align256(pool);
+    int32_t* ident = reinterpret_cast<int32_t*>(ws + 2 * align256(pool));
+    cudaError_t e = launch_gather_pages_bf16(k_pages, v_pages, block_table, cache_lens, kg, vg,
+                                             ident, B, Hkv, Tq, d, page_size, num_pages,
+                                             max_pages, lpad, a.status, st);
+    if (e != cudaSuccess) return fail_cuda(e, "attn_prefill_paged: gather kernel launch");
+    a.k = kg;
+    a.v = vg;
+    a.block_table = ident;
+    a.page_size = lpad;
+    a.num_pages = B;
+    a.max_pages = 1;
+  }
+  cudaError_t e = launch_fwd_sm103a(a, a.k, st);
   if (e != cudaSuccess) return fail_cuda(e, "attn_prefill_paged: kernel launch");
   return CSATTN_OK;
 }
-
-static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 size_t csattn_decode_step_workspace_size(int B, int Hq, int Lmax, int d, int num_splits) {
   const size_t part = csattn_decode_workspace_size(B, Hq, Lmax, d, num_splits);

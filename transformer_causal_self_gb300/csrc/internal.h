@@ -148,6 +148,15 @@ cudaError_t launch_cache_append_bf16(const void* k_new, const void* v_new, void*
                                      const RopeTable& theta, uint32_t* status,
                                      cudaStream_t stream);
 
+// Copies rows 0..cache_lens[b]+Tq-1 of each sequence's KV heads from a paged pool
+// [num_pages, Hkv, page_size, d] into page b of contiguous pools [B, Hkv, Lpad, d] and
+// writes the identity block table ident[b] = b (the paged prefill over small pages).
+cudaError_t launch_gather_pages_bf16(const void* k_pages, const void* v_pages,
+                                     const int32_t* block_table, const int32_t* cache_lens,
+                                     void* k_out, void* v_out, int32_t* ident, int B, int Hkv,
+                                     int Tq, int d, int page_size, int num_pages, int max_pages,
+                                     int Lpad, uint32_t* status, cudaStream_t stream);
+
 // Raises a kernel's dynamic shared-memory limit once per device (the attribute
 // lasts for the process), so repeated launches skip the driver call.
 struct SmemLimitOnce {
