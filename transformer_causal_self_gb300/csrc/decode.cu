@@ -127,6 +127,59 @@ __global__ void __launch_bounds__(kThreads)
 
   if (warp == kComputeWarps) {
     // ------------------------------------------------------------ producer
+    if (p.block_table != nullptr && p.box_rows < KT) {
+      // pages of 16 or 32 rows: 4 or 2 boxes per tile, one per lane, so that their
+      // table reads and copies are issued side by side; lane 0 waits and arms the
+      // stage's barrier before the other lanes' copies (ordered by __syncwarp)
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+      }
+      const int nbox = KT / p.box_rows;
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % NS, use = t / NS;
+        int okw = 1;
+        if (lane == 0) {
+          if (use > 0 && !ctl_wait(&empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs))
+            okw = 0;
+          else
+            mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        }
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) break;
+        __syncwarp();
+        if (lane < nbox) {
+          uint8_t* kdst = smem + s * C::STAGE_BYTES;
+          uint8_t* vdst = kdst + C::TILE_BYTES;
+          const int r0 = lane * p.box_rows, tr = k_begin + t * KT + r0;
+          int plane = p.num_pages * p.Hkv, prow = 0;
+          if (tr < L) {
+            const int page =
+                p.block_table[static_cast<size_t>(b) * p.max_pages + tr / p.page_size];
+            if (page >= 0 && page < p.num_pages)
+              plane = page * p.Hkv + kvh;
+            else
+              atomicOr(p.status, kStatusDeviceArg);
+            prow = tr % p.page_size;
+          }
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(kdst + kb * C::BLOCK_BYTES + r0 * 128, &tm_k, &full[s], kb * 64, prow,
+                        plane);
+            tma_load_3d(vdst + kb * C::BLOCK_BYTES + r0 * 128, &tm_v, &full[s], kb * 64, prow,
+                        plane);
+          }
+        }
+        __syncwarp();
+        ++issued;
+      }
+      if (lane == 0 && *abort_flag) {
+        const int first = issued > NS ? issued - NS : 0;
+        for (int t = first; t < issued; ++t)
+          mbar_wait(&full[t % NS], (t / NS) & 1, nullptr, p.status, kDrainNs);
+      }
+      return;
+    }
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
