@@ -439,6 +439,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
     as the headline decode; its cache is > 2 GB, so no flush.
     decode_paged: the headline decode over the same rows stored in 128-row pages of a
     shuffled pool (csattn_attn_decode_paged); > 1 GB of pages, no flush.
+    decode_paged_16: the same with 16-row pages.
     Each: 3 warm-up launches, then `reps` launches, each bracketed by CUDA events on the
     launching stream; the mean is reported."""
     out = {}
@@ -620,6 +621,33 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(gbs / hbm_peak, 4), "traffic": None,
                      "kernel": "decode_bf16_kernel<128> (paged reads) + decode_combine_kernel"}}
+    del kp, vp, table
+    # the same decode over 16-row pages (the block size of vLLM-style caches)
+    kp, vp, table = W.page_cache(kc, vc, lens_h, 16, seed=10)
+    od = torch.empty_like(qn)
+    ws = torch.empty(csattn.decode_workspace_size(wd.B, wd.Hq, table.shape[1] * 16, wd.d, 0),
+                     dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(3 + reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csattn.attn_decode_paged(qn, kp, vp, table, lens, od, scale=wd.scale,
+                                 max_seq_len=max_len, workspace=ws, stream=stream)
+        e1.record(stream)
+        if i >= 3:
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    csattn.check_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    gbs = dbytes / (ms * 1e-3) / 1e9
+    out["decode_paged_16"] = {
+        "workload": "decode_bf16 (B=64, Hq=32, Hkv=8, d=128, L~U[512,8192]) with the cache in "
+                    "16-row pages of a shuffled pool",
+        "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": dbytes,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "kernel": "decode_bf16_kernel<128> (paged reads, one box per lane) + "
+                               "decode_combine_kernel"}}
     del kp, vp, table
     # a 1024-token chunk of the llama_chunk_bf16 shape appended (keys rotated) at row 3072
     # of contiguous caches; bytes = the chunk's K and V read once and written once
