@@ -20,7 +20,7 @@ from __future__ import annotations
 import math
 from fractions import Fraction
 
-__all__ = ["naive_attention", "naive_round_bf16", "naive_decode"]
+__all__ = ["naive_attention", "naive_lse", "naive_round_bf16", "naive_decode"]
 
 
 def naive_round_bf16(x: float) -> float:
@@ -101,6 +101,54 @@ def naive_attention(q, k, v, causal=True, rope_base=0.0, scale=None,
                     row.append(acc / z)
                 oh.append(row)
             ob.append(oh)
+        out.append(ob)
+    return out
+
+
+def naive_lse(q, k, causal=True, rope_base=0.0, scale=None, rope_layout="split_half",
+              round_bf16=False, q_offset=0):
+    """Natural log of each query's softmax denominator, nested lists [B][Hq][Tq].
+
+    The softmax of "The Transformer architecture", "Softmax is a differentiable
+    allocation" divides by z_i = sum_j exp(s_ij) over the visible keys; this is
+    ln z_i, computed as max_j s_ij + ln sum_j exp(s_ij - max_j s_ij) with the
+    same scalar loops as ``naive_attention`` (s_ij = q_i . k_j * scale).
+    """
+    B, Hq, T, d = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
+    Hkv = len(k[0])
+    Tk = len(k[0][0])
+    rep = Hq // Hkv
+    sc = (1.0 / math.sqrt(d)) if (scale is None or scale <= 0) else scale
+    rnd = naive_round_bf16 if round_bf16 else None
+    out = []
+    for b in range(B):
+        ob = []
+        for h in range(Hq):
+            g = h // rep
+            row = []
+            for i in range(T):
+                if rope_base > 0:
+                    qi = _rot(q[b][h][i], q_offset + i, rope_base, rope_layout, rnd)
+                else:
+                    qi = [float(x) for x in q[b][h][i]]
+                s = []
+                for j in range(Tk):
+                    if causal and j > q_offset + i:
+                        continue
+                    if rope_base > 0:
+                        kj = _rot(k[b][g][j], j, rope_base, rope_layout, rnd)
+                    else:
+                        kj = [float(x) for x in k[b][g][j]]
+                    dot = 0.0
+                    for c in range(d):
+                        dot += qi[c] * kj[c]
+                    s.append(dot * sc)
+                mx = max(s)
+                z = 0.0
+                for x in s:
+                    z += math.exp(x - mx)
+                row.append(mx + math.log(z))
+            ob.append(row)
         out.append(ob)
     return out
 

@@ -566,6 +566,75 @@ def pin_decode_paged_equals_contiguous(o):
     assert np.max(np.abs(got - o.decode(q, kc, vc, lens))) < 1e-12
 
 
+def pin_lse_normalises_softmax(o):
+    """The log-sum-exp is the log of the softmax denominator ("The Transformer
+    architecture", "Softmax is a differentiable allocation"): exp(S*scale + M - lse)
+    is the softmax row itself and sums to 1 (GQA, RoPE, a query offset, causal and not).
+    S is formed here from the rotated operands with a plain matrix product."""
+    B, Hq, Hkv, Tq, Tk, d, sc, off = 2, 4, 2, 9, 14, 8, 0.41, 5
+    q = _rand((B, Hq, Tq, d), 400, 2.0)
+    k = _rand((B, Hkv, Tk, d), 401, 2.0)
+    qr = o.rope_rotate(q, off + np.arange(Tq), 10000.0)
+    kr = o.rope_rotate(k, np.arange(Tk), 10000.0)
+    for causal in (True, False):
+        lse = o.attention_lse(q, k, causal=causal, rope_base=10000.0, scale=sc, q_offset=off)
+        assert lse.shape == (B, Hq, Tq)
+        for b in range(B):
+            for h in range(Hq):
+                s = (qr[b, h] @ kr[b, h // (Hq // Hkv)].T) * sc
+                if causal:
+                    s = np.where(np.arange(Tk)[None, :] > off + np.arange(Tq)[:, None], -np.inf, s)
+                p = np.exp(s - lse[b, h][:, None])
+                assert np.all(np.abs(p.sum(-1) - 1.0) < 1e-12), (causal, b, h)
+                assert np.max(np.abs(p - o.softmax_rows(s))) < 1e-12
+
+
+def pin_lse_closed_forms(o):
+    """One visible key: lse = its score.  Two visible keys with equal scores s:
+    lse = s + ln 2.  Causal row 0 sees key 0 only; with k[1] = k[0] and no RoPE,
+    row 1 sees two equal scores."""
+    q = _rand((1, 2, 4, 8), 410)
+    k = _rand((1, 1, 4, 8), 411)
+    k[:, :, 1] = k[:, :, 0]
+    sc = 0.3
+    lse = o.attention_lse(q, k, causal=True, scale=sc)
+    for h in range(2):
+        s0 = float(q[0, h, 0] @ k[0, 0, 0]) * sc
+        s1 = float(q[0, h, 1] @ k[0, 0, 0]) * sc
+        assert abs(lse[0, h, 0] - s0) < 1e-13
+        assert abs(lse[0, h, 1] - (s1 + math.log(2.0))) < 1e-13
+    # decode-like chunk: one query at offset L-1 over L keys equals the last full row
+    full = o.attention_lse(q, k, causal=True, scale=sc)
+    last = o.attention_lse(q[:, :, 3:], k, causal=True, scale=sc, q_offset=3)
+    assert np.max(np.abs(full[:, :, 3:] - last)) < 1e-13
+
+
+def pin_lse_naive_agreement(o):
+    """Against the scalar loops of ``oracle.naive.naive_lse`` (separately written), on the
+    case grid of the output's brute-force pin plus a query offset and a rectangular case."""
+    cases = [
+        dict(B=1, Hkv=2, rep=1, T=9, Tk=9, d=4, causal=True, base=10000.0, layout="split_half", off=0),
+        dict(B=2, Hkv=1, rep=2, T=7, Tk=7, d=16, causal=True, base=10000.0, layout="adjacent", off=0),
+        dict(B=1, Hkv=2, rep=4, T=16, Tk=16, d=4, causal=False, base=0.0, layout="split_half", off=0),
+        dict(B=1, Hkv=1, rep=4, T=11, Tk=11, d=16, causal=True, base=500000.0, layout="split_half",
+             off=0),
+        dict(B=1, Hkv=2, rep=2, T=13, Tk=13, d=4, causal=False, base=10000.0, layout="adjacent", off=0),
+        dict(B=1, Hkv=2, rep=2, T=5, Tk=12, d=8, causal=True, base=10000.0, layout="split_half", off=7),
+        dict(B=2, Hkv=1, rep=3, T=4, Tk=10, d=4, causal=False, base=10000.0, layout="adjacent", off=3),
+    ]
+    for i, c in enumerate(cases):
+        Hq = c["Hkv"] * c["rep"]
+        q = _rand((c["B"], Hq, c["T"], c["d"]), 420 + i, 2.0)
+        k = _rand((c["B"], c["Hkv"], c["Tk"], c["d"]), 430 + i, 2.0)
+        for rnd in (False, True):
+            a = o.attention_lse(q, k, causal=c["causal"], rope_base=c["base"], scale=0.37,
+                                rope_layout=c["layout"], operand_dtype="bf16" if rnd else None,
+                                q_offset=c["off"])
+            b = np.array(ON.naive_lse(_to_list(q), _to_list(k), c["causal"], c["base"], 0.37,
+                                      c["layout"], round_bf16=rnd, q_offset=c["off"]))
+            assert np.max(np.abs(a - b)) < 1e-12, (i, rnd, np.max(np.abs(a - b)))
+
+
 ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exactly_zero,
             pin_mask_variants_differ, pin_gqa_equals_mha_repeated, pin_basis_invariance,
             pin_qq_symmetric, pin_rope_relative, pin_rope_orthogonal, pin_rope_layouts_permute,
@@ -576,7 +645,10 @@ ALL_PINS = [pin_softmax_page_example, pin_rows_sum_to_one, pin_masked_weight_exa
             pin_backward_autograd, pin_rope_transpose_inverts,
             pin_decode_paged_equals_contiguous, pin_value_width, pin_cache_append_positions,
             pin_cache_append_matches_decode_step, pin_cache_append_paged_equals_contiguous,
-            pin_prefill_paged_equals_chunk]
+            pin_prefill_paged_equals_chunk, pin_lse_normalises_softmax, pin_lse_closed_forms,
+            pin_lse_naive_agreement]
+
+LSE_PINS = [pin_lse_normalises_softmax, pin_lse_closed_forms, pin_lse_naive_agreement]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -932,3 +1004,46 @@ def test_planted_paged_prefill_positions_ignore_prefix():
             return (np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res]))
         return np.concatenate(res)
     assert _fails(_Mutant(prefill_paged=bad), [pin_prefill_paged_equals_chunk])
+
+
+def _lse_variant(log2=False, unscaled=False, no_mask=False):
+    """The oracle's log-sum-exp with one planted mistake."""
+    def lse(q, k, *, causal=True, rope_base=0.0, scale=None, rope_layout="split_half",
+            operand_dtype=None, q_offset=0):
+        q, k = np.asarray(q, np.float64), np.asarray(k, np.float64)
+        B, Hq, T, d = q.shape
+        Tk = k.shape[2]
+        sc = 1 / math.sqrt(d) if (scale is None or scale <= 0) else scale
+        if unscaled:
+            sc = 1.0
+        if rope_base > 0:
+            q = OA.round_to(OA.rope_rotate(q, q_offset + np.arange(T), rope_base, rope_layout),
+                            operand_dtype)
+            k = OA.round_to(OA.rope_rotate(k, np.arange(Tk), rope_base, rope_layout), operand_dtype)
+        kf = OA.expand_kv_heads(k, Hq)
+        mask = OA.causal_additive_mask(T, Tk, q_offset) if (causal and not no_mask) else 0.0
+        out = np.empty((B, Hq, T))
+        for b in range(B):
+            for h in range(Hq):
+                s = q[b, h] @ kf[b, h].T * sc + mask
+                m = np.max(s, axis=-1)
+                z = np.sum(np.exp(s - m[:, None]), axis=-1)
+                out[b, h] = (m + np.log2(z)) if log2 else (m + np.log(z))
+        return out
+    return lse
+
+
+def test_lse_variant_helper_is_faithful():
+    assert _fails(_Mutant(attention_lse=_lse_variant()), LSE_PINS) == []
+
+
+def test_planted_lse_log2():
+    assert _fails(_Mutant(attention_lse=_lse_variant(log2=True)), LSE_PINS)
+
+
+def test_planted_lse_unscaled():
+    assert _fails(_Mutant(attention_lse=_lse_variant(unscaled=True)), LSE_PINS)
+
+
+def test_planted_lse_ignores_mask():
+    assert _fails(_Mutant(attention_lse=_lse_variant(no_mask=True)), LSE_PINS)
