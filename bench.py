@@ -77,7 +77,7 @@ def _job_throughput(units_per_rank, seconds_per_rank, world):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms while running."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -92,7 +92,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv",
-                                          "-lms", "100", "-i", str(self.gpu)], stdout=self.f,
+                                          "-lms", "50", "-i", str(self.gpu)], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -162,6 +162,59 @@ def _traffic(kernel_file, *deps):
         if e.get("source_sha") == _source_hash(kernel_file, *deps):
             return float(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError, TypeError):
+        pass
+    return None
+
+
+def _host_link(torch, hosts, devs, stream):
+    """The host link as this run sees it: the pinned host buffers `hosts` (the prefill's
+    q, k, v: 201 MiB) copied to the device buffers `devs` and back, one direction at a
+    time, timed with CUDA events on `stream` (best of 3), plus where this process sits
+    relative to the GPU (NUMA nodes)."""
+    nbytes = sum(h.numel() * h.element_size() for h in hosts)
+    res = {"bytes": int(nbytes)}
+    for name, h2d in (("h2d_gbs", True), ("d2h_gbs", False)):
+        best = None
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for h, d in zip(hosts, devs):
+                (d.copy_(h, non_blocking=True) if h2d else h.copy_(d, non_blocking=True))
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        res[name] = round(nbytes / (best * 1e-3) / 1e9, 1)
+    res["gpu_numa_node"] = _gpu_numa_node(devs[0].device.index)
+    try:
+        cpus = sorted(os.sched_getaffinity(0))
+        res["cpus"] = f"{cpus[0]}-{cpus[-1]} ({len(cpus)})" if cpus else None
+        res["cpu_numa_nodes"] = sorted({_cpu_node(c) for c in cpus} - {None})
+    except (AttributeError, OSError):
+        pass
+    return res
+
+
+def _gpu_numa_node(index):
+    """NUMA node of the GPU's PCI function, from nvidia-smi's bus id and sysfs."""
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                              "-i", str(index)], capture_output=True, text=True, timeout=20)
+        bus = out.stdout.strip().lower()
+        if len(bus.split(":")[0]) == 8:  # 00000000:0a:00.0 -> 0000:0a:00.0
+            bus = bus[4:]
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            return int(f.read().strip())
+    except (OSError, ValueError, subprocess.SubprocessError):
+        return None
+
+
+def _cpu_node(cpu):
+    try:
+        for e in os.listdir(f"/sys/devices/system/cpu/cpu{cpu}"):
+            if e.startswith("node") and e[4:].isdigit():
+                return int(e[4:])
+    except OSError:
         pass
     return None
 
@@ -298,15 +351,19 @@ def run_gpu(args):
     _barrier(world)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    with ClockSampler(dev.index) as clocks:
-        _barrier(world)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter()
-        for i in range(args.steps):
-            step(evs[i])
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
-        _barrier(world)
+    # The sampler runs from just before the timed steps through the end-to-end leg and
+    # the other rows (all GPU-bound work of the same kernels), so that a short timed
+    # region still has clock samples under load around it.
+    clocks = ClockSampler(dev.index).__enter__()
+    t_sample = time.perf_counter()
+    _barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    _barrier(world)
     csattn.check_status(stream)
     launches = 4 * args.steps  # rope, attention, decode split, decode merge
 
@@ -336,7 +393,7 @@ def run_gpu(args):
         # the decode leg copies q, seq_lens and only the cache rows it reads (dbytes)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hl)) + int(dbytes)
         d2h = ho.numel() * ho.element_size() + hod.numel() * hod.element_size()
-        e_steps = max(1, min(args.steps, 5))
+        e_steps = max(1, min(args.steps, 10))
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e_steps)]
         # the prefill through csattn_attn_fwd_host: copies in, kernels and copies out
         # pipelined over 8 chunks of (sequence, KV head) pairs inside the call (the default)
@@ -363,8 +420,12 @@ def run_gpu(args):
         e2e = {"value": round(world * flops / (e_pre * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_pre + e_dec, 3),
+               "prefill_ms": round(e_pre, 3), "decode_ms": round(e_dec, 3),
+               "prefill_ms_each": [round(e[0].elapsed_time(e[1]), 3) for e in ev],
+               "decode_ms_each": [round(e[1].elapsed_time(e[2]), 3) for e in ev],
                "decode": {"value": round(world * dbytes / (e_dec * 1e-3) / 1e9, 1),
                           "unit": "GB/s"},
+               "host_link": _host_link(torch, (hq, hk, hv), (q, k, v), stream),
                "note": "pinned host buffers; prefill through csattn_attn_fwd_host (H2D of "
                        "q, k, v, the kernels and D2H of out pipelined over 8 chunks inside the "
                        "call); decode through csattn_attn_decode_host (H2D of q, seq_lens and "
@@ -375,6 +436,11 @@ def run_gpu(args):
     if rank == 0 and not args.no_rows:
         rows = _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_len,
                              tf_burst, hbm_peak)
+    t_sample = time.perf_counter() - t_sample
+    clocks.__exit__(None, None, None)
+    clock_summary = clocks.summary()
+    clock_summary["window"] = (f"{t_sample:.1f} s from the start of the timed steps through the "
+                               "end-to-end leg and the rows measured after them")
 
     if rank != 0:
         return 0
@@ -413,7 +479,7 @@ def run_gpu(args):
                    "bytes_per_step": dbytes, "roofline": dec_roof},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "rows": rows,
-        "clocks": clocks.summary(), "wall_s_timed": round(t_wall, 3),
+        "clocks": clock_summary, "wall_s_timed": round(t_wall, 3),
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -430,8 +496,9 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
     csattn_attn_fwd_ext, L2 flushed before each launch (its inputs are ~L2-sized).
     prefill_paged: the same chunk with the cache in 256-row pages of a shuffled pool
     (csattn_attn_prefill_paged), L2 flushed before each launch.
-    long_context, gpt2: the prefill (RoPE pass + attention) of long_gqa_bf16 (T=32768)
-    and gpt2_bf16 (d=64, L2 flushed before each launch) through csattn_attn_fwd.
+    long_context, gpt2, llama_x4: the prefill (RoPE pass + attention) of long_gqa_bf16
+    (T=32768), gpt2_bf16 (d=64, L2 flushed before each launch) and the saturation seed
+    llama_gqa_bf16_x4 (seed 1, q and k times 4) through csattn_attn_fwd.
     rectangular: llama_cross_bf16 (1024 queries against 4096 keys, no mask), the same
     entry point, L2 flushed before each launch.
     decode_step: the decode_bf16 batch with the new token appended at row L_b - 1 and
@@ -503,7 +570,8 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
     # the other prefill configurations: long-context GQA (T=32768, RoPE 5e5; > 400 MB of
     # inputs, no flush needed) and GPT-2-shaped MHA (d=64, no RoPE; L2 flushed)
     for name, wl, flush_it in (("long_context", "long_gqa_bf16", False),
-                               ("gpt2", "gpt2_bf16", True)):
+                               ("gpt2", "gpt2_bf16", True),
+                               ("llama_x4", "llama_gqa_bf16_x4", False)):
         wq = W.WORKLOADS[wl]
         q, k, v = (t.to(dev) for t in W.make_prefill_inputs(wq))
         o = torch.empty_like(q)
@@ -528,7 +596,9 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         tf = wq.flops() / (ms * 1e-3) / 1e12
         out[name] = {
             "workload": f"{wl} (B={wq.B}, Hq={wq.Hq}, Hkv={wq.Hkv}, T={wq.T}, d={wq.d}, "
-                        f"RoPE {wq.rope_base:g}; RoPE pass + attention kernel)",
+                        f"RoPE {wq.rope_base:g}"
+                        + (f", seed {wq.seed}, q and k x{wq.qk_mult:g}" if wq.qk_mult != 1 else "")
+                        + "; RoPE pass + attention kernel)",
             "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
             "flops": wq.flops(),
             "l2": "flushed before each launch" if flush_it else "inputs larger than L2",

@@ -343,16 +343,23 @@ int csattn_attn_decode_step(const void* q_new, const void* k_new, const void* v_
  *
  * Same arguments and results as csattn_attn_decode, without the workspace:
  * the split partials go to a static device buffer of
- * CSATTN_DECODE_STATIC_SCRATCH_BYTES bytes that the library defines and that
- * every GPU loading the library keeps until the process exits.  The call
- * allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
- *   - Arguments whose partials (B*Hq*splits*(d+2)*4 bytes for the split
- *     count actually used) exceed the buffer are rejected with
+ * CSATTN_DECODE_STATIC_SCRATCH_BYTES bytes that the library defines.  The
+ * call allocates nothing itself (no cudaMalloc/cudaFree, no allocating
+ * library call).
+ *   - Argument errors (as for csattn_attn_decode) are returned before any
+ *     CUDA call.  Arguments whose partials (B*Hq*splits*(d+2)*4 bytes for the
+ *     split count actually used) exceed the buffer are rejected with
  *     CSATTN_ERR_WORKSPACE and a message naming both sizes; nothing is
  *     launched.  Use fewer splits, or csattn_attn_decode with a workspace.
- *   - The first call on a device looks up the buffer's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture on the device.
+ *   - The first call on a device is a set-up call: the CUDA runtime loads the
+ *     module that holds the buffer lazily (the default module loading), so
+ *     that call reserves the 16 MiB on the device and can fail with
+ *     CSATTN_ERR_CUDA (out of memory); it then looks up the buffer's device
+ *     address (cudaGetSymbolAddress, with that device current) and caches it.
+ *     Make that first call as a warm-up before a memory pool takes the
+ *     device's free memory and before any stream capture on the device;
+ *     later calls reserve nothing and the device keeps the buffer until the
+ *     process exits.
  *   - All calls on a device share the one buffer, which keeps the previous
  *     call's contents (nothing in it has to start at zero).  Calls whose
  *     kernels overlap on the GPU (other streams, other threads) race on it:

@@ -158,6 +158,34 @@ def test_decode_rejects_invalid_arguments(lib, kw, status):
 
 
 @pytest.mark.parametrize("kw,status", [
+    (dict(seq=None), -1),
+    (dict(q=None), -1),
+    (dict(B=0), -1),
+    (dict(dtype=0), -2),
+    (dict(dtype=9), -1),
+    (dict(d=96), -2),
+    (dict(max_len=300), -1),
+    (dict(splits=-1), -1),
+    (dict(out=FAKE + 4), -1),
+    # 128 explicit splits of B=64, Hq=32, d=128 partials: 136 MB > the 16 MiB buffer
+    (dict(B=64, Hq=32, Hkv=8, Lmax=8192, max_len=8192, splits=128), -5),
+])
+def test_decode_noalloc_rejects_invalid_arguments(lib, kw, status):
+    """Every rejection happens before any CUDA call (no GPU here)."""
+    a = dict(q=FAKE, k=FAKE, v=FAKE, seq=FAKE, out=FAKE, B=2, Hq=8, Hkv=2, Lmax=256, d=128,
+             dtype=1, scale=0.0, max_len=256, splits=0)
+    a.update(kw)
+    rc = lib.csattn_attn_decode_noalloc(a["q"], a["k"], a["v"], a["seq"], a["out"], a["B"],
+                                        a["Hq"], a["Hkv"], a["Lmax"], a["d"], a["dtype"],
+                                        a["scale"], a["max_len"], a["splits"], None)
+    assert rc == status, lib.csattn_last_error()
+    msg = lib.csattn_last_error()
+    assert b"attn_decode_noalloc" in msg
+    if status == -5:
+        assert b"static scratch" in msg and str(16 * 1024 * 1024).encode() in msg
+
+
+@pytest.mark.parametrize("kw,status", [
     (dict(table=None), -1),
     (dict(table=FAKE + 2), -1),
     (dict(page_size=0), -1),

@@ -1,15 +1,18 @@
 """Backward parity: dq, dk, dv from csattn_attn_bwd against the float64 oracle's
 gradients (oracle.attn.attention_backward) on the same bf16 inputs.
 
-Tolerance.  The kernels round P and dS to bf16 for the tensor-core products
-(relative error <= 2^-9 each, independent across terms) and accumulate in fp32,
-and take out and lse from the bf16 forward; the gradients are sums of many such
-terms, so their relative L2 error is a few 2^-9 ~ 2e-3.  Bound: relative L2
-<= 1e-2 and max-abs <= 2e-2 * max(1, max |ref|) per tensor.  The relative L2 is
-taken against max(||ref||, 1e-3 sqrt(n)): where the exact gradient is zero (T = 1,
-a single key, dP and D = rowsum(dO o O) are the same dot product summed in
-different orders, so dS = P (dP - D) is fp32 rounding noise) it bounds the RMS
-error by 1e-5 instead of dividing by zero."""
+Tolerance (bf16).  The benchmark spec's bounds, max-abs 2e-2 and relative L2 5e-3,
+with one allowance: the gradients are returned in bf16, and where their entries
+exceed the attention output's range (|dv| reaches ~10 on these inputs) the
+rounding of the stored value alone is up to half a bf16 ulp, 2^(e-8) for an entry
+in [2^e, 2^(e+1)): 0.031 at 8..16, more than 2e-2 by itself.  So the max-abs bound
+is 2e-2 plus half an ulp of the largest reference entry; below 4 that adds at
+most 2^-7.  The kernels also round P and dS to bf16 for the tensor-core products
+(relative 2^-9 each, independent across terms), which puts the relative L2 error
+at ~2.5e-3.  The relative L2 is taken against max(||ref||, 1e-3 sqrt(n)): where the
+exact gradient is zero (T = 1, a single key: dP and D = rowsum(dO o O) are the same
+dot product summed in different orders, so dS = P (dP - D) is fp32 rounding noise)
+it bounds the RMS error by 5e-6 instead of dividing by zero."""
 import math
 
 import numpy as np
@@ -24,14 +27,22 @@ from tests.gpu_helpers import dev, to_np
 pytestmark = pytest.mark.gpu
 
 
-def _close(got, ref, what, rl2_tol=1e-2, abs_tol=2e-2, floor=1e-3):
+def _half_ulp_bf16(x):
+    """Half a bf16 ulp at |x| (8 significant bits): 2^(e-8) for |x| in [2^e, 2^(e+1))."""
+    x = abs(float(x))
+    return 0.0 if x == 0.0 else math.ldexp(1.0, math.frexp(x)[1] - 9)
+
+
+def _close(got, ref, what, rl2_tol=5e-3, abs_tol=2e-2, floor=1e-3, bf16_storage=True):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert np.all(np.isfinite(got)), f"{what}: non-finite"
     err = float(np.max(np.abs(got - ref)))
     rl2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), floor * math.sqrt(ref.size)))
-    assert rl2 <= rl2_tol and err <= abs_tol * max(1.0, float(np.max(np.abs(ref)))), \
-        f"{what}: max-abs {err:.3e} (ref max {np.max(np.abs(ref)):.3e}), rel-L2 {rl2:.3e}"
+    ref_max = float(np.max(np.abs(ref)))
+    bound = abs_tol + (_half_ulp_bf16(ref_max) if bf16_storage else 0.0)
+    assert rl2 <= rl2_tol and err <= bound, \
+        f"{what}: max-abs {err:.3e} (bound {bound:.3e}, ref max {ref_max:.3e}), rel-L2 {rl2:.3e}"
 
 
 def _run(q, k, v, do, causal, base, layout, scale):
@@ -144,9 +155,9 @@ def test_bwd_gqa_equals_summed_mha():
 # fp32 operands, fp32 arithmetic throughout (accurate sine/cosine for RoPE, fp32
 # forward out and lse): each gradient entry is a sum of at most T products of
 # terms carrying a few fp32 roundings (2^-24 ~ 6e-8) each, and P = exp(S - lse)
-# carries the absolute error of S and lse (~1e-6 for |S| ~ 10).  Bound: relative
-# L2 <= 1e-4 and max-abs <= 2e-4 * max(1, max |ref|); the relative L2 floor is
-# 1e-2 sqrt(n) (RMS error <= 1e-6 where the exact gradient vanishes, T = 1).
+# carries the absolute error of S and lse (~1e-6 for |S| ~ 10).  Bound: the north
+# star's fp32 max-abs 1e-5 (absolute) and relative L2 1e-5; the relative L2 floor
+# is 0.1 sqrt(n) (RMS error <= 1e-6 where the exact gradient vanishes, T = 1).
 
 FP32_CASES = [
     # (B, Hq, Hkv, T, d, causal, rope_base, layout)
@@ -174,7 +185,7 @@ def test_bwd_fp32_parity(B, hq, hkv, T, d, causal, base, layout):
     assert dq.dtype == torch.float32 and dk.dtype == torch.float32
     rq, rk, rv = OA.attention_backward(q, k, v, do, causal=causal, rope_base=base, scale=w.scale,
                                        rope_layout=layout, operand_dtype="f32")
-    tol = dict(rl2_tol=1e-4, abs_tol=2e-4, floor=1e-2)
+    tol = dict(rl2_tol=1e-5, abs_tol=1e-5, floor=0.1, bf16_storage=False)
     _close(to_np(dq), rq, "dq", **tol)
     _close(to_np(dk), rk, "dk", **tol)
     _close(to_np(dv), rv, "dv", **tol)

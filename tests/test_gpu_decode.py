@@ -76,7 +76,7 @@ def test_decode_matches_prefill_last_row():
     lens = torch.tensor([T, 311], dtype=torch.int32)
     qd = torch.stack([qr[0, :, T - 1:T], qr[1, :, 310:311]]).contiguous()
     out = _decode(qd, kr.contiguous(), v, lens, scale=w.scale, max_seq_len=T).cpu()
-    assert torch.max(torch.abs(out[0, :, 0].float() - full[0, :, T - 1].float())) <= 2e-2
+    assert_bf16_close(to_np(out[0, :, 0]), to_np(full[0, :, T - 1]), "decode vs prefill row")
     ref = OA.decode(qd, kr, v, lens.numpy(), scale=w.scale)
     assert_bf16_close(to_np(out), ref, "decode vs oracle")
 

@@ -149,8 +149,9 @@ def test_gqa_equals_mha_with_repeated_kv():
     kr = k.repeat_interleave(4, dim=1).contiguous()
     vr = v.repeat_interleave(4, dim=1).contiguous()
     b = _run(q, kr, vr, causal=True, rope_base=w.rope_base, scale=w.scale).cpu()
-    diff = (a.float() - b.float()).abs().max().item()
-    assert diff == 0.0 or diff <= 2 ** -7, diff
+    # the same kernel on the same bytes: each query row's arithmetic does not depend on
+    # which KV head number its keys carry or which tile it is paired with
+    assert torch.equal(a, b), (a.float() - b.float()).abs().max().item()
 
 
 def test_gpt2_workload_full():

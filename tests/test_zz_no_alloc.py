@@ -5,9 +5,11 @@ framework that owns all device memory, a latency-critical loop where cudaMalloc
 would synchronise the device).  For them the library keeps the split partials
 in a static device buffer instead of a caller workspace.  These tests call the
 entry point through the C ABI and hold its output to the regular
-csattn_attn_decode on the same inputs, on two calls in a row with different
-inputs (so nothing left in the shared buffer by one call can leak into the
-next).  The file is named to be collected last.
+csattn_attn_decode on the same inputs: the same kernels with the same split
+count, so the two must agree bit for bit.  Three calls run in a row with
+different inputs, the last with much shorter sequences (fewer splits) than the
+one before, so partials left in the shared buffer by an earlier call would show
+if the merge read them.  The file is named to be collected last.
 """
 import math
 
@@ -16,7 +18,7 @@ import torch
 
 import attn_workloads as W
 import transformer_causal_self_gb300 as csattn
-from tests.gpu_helpers import assert_bf16_close, dev, to_np
+from tests.gpu_helpers import dev
 
 pytestmark = pytest.mark.gpu
 
@@ -28,12 +30,19 @@ def _call_noalloc(lib, q, kc, vc, sl, out, w, max_len, splits):
                                           torch.cuda.current_stream().cuda_stream)
 
 
+def _inputs(seed, shrink=1):
+    w = W.WORKLOADS["decode_bf16"].with_(B=16, Lmax=4096, Lmin=1, seed=seed)
+    q, kc, vc, sl = (t.to(dev()) for t in W.make_decode_inputs(w))
+    if shrink > 1:  # shorter sequences over the same cache (rows past them are not read)
+        sl = torch.clamp(sl // shrink, min=1)
+    return w, q, kc, vc, sl
+
+
 @pytest.mark.parametrize("splits", [0, 5])
 def test_noalloc_decode_matches_workspace_decode(splits):
     lib = csattn.load_library()
-    for seed in (11, 12):  # two calls in a row, different inputs
-        w = W.WORKLOADS["decode_bf16"].with_(B=16, Lmax=4096, Lmin=1, seed=seed)
-        q, kc, vc, sl = (t.to(dev()) for t in W.make_decode_inputs(w))
+    for seed, shrink in ((11, 1), (12, 1), (13, 16)):  # three calls in a row, the last short
+        w, q, kc, vc, sl = _inputs(seed, shrink)
         max_len = int(sl.max().item())
         ref = csattn.attn_decode(q, kc, vc, sl, scale=w.scale, max_seq_len=max_len,
                                  num_splits=splits)
@@ -42,7 +51,22 @@ def test_noalloc_decode_matches_workspace_decode(splits):
         rc = _call_noalloc(lib, q, kc, vc, sl, out, w, max_len, splits)
         assert rc == 0, lib.csattn_last_error()
         csattn.check_status()
-        assert_bf16_close(to_np(out), to_np(ref), f"noalloc seed {seed}")
+        assert torch.equal(out, ref), f"noalloc seed {seed}: differs from the workspace decode"
+
+
+def test_noalloc_second_call_reserves_no_device_memory():
+    lib = csattn.load_library()
+    w, q, kc, vc, sl = _inputs(14)
+    max_len = int(sl.max().item())
+    out = torch.empty_like(q)
+    assert _call_noalloc(lib, q, kc, vc, sl, out, w, max_len, 0) == 0, lib.csattn_last_error()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    assert _call_noalloc(lib, q, kc, vc, sl, out, w, max_len, 0) == 0, lib.csattn_last_error()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    csattn.check_status()
+    assert free1 == free0
 
 
 def test_noalloc_rejects_partials_beyond_the_static_buffer():

@@ -476,6 +476,14 @@ int decode_check(const char* fn, const void* q, const void* k_cache, const void*
 
 }  // namespace
 
+int csattn::attn_decode_check_ptrs(const char* fn, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* seq_lens, const void* out,
+                                   int B, int Hq, int Hkv, int Lmax, int d, int dtype, float scale,
+                                   int max_seq_len, int num_splits) {
+  return decode_check(fn, q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, Lmax, d, dtype, scale,
+                      max_seq_len, num_splits);
+}
+
 int csattn::attn_decode_check(const char* fn, int B, int Hq, int Hkv, int Lmax, int d,
                               int dtype, float scale, int max_seq_len, int num_splits) {
   alignas(16) static const uint8_t dummy[16] = {};

@@ -19,9 +19,12 @@
 namespace csattn {
 namespace {
 
-// The scratch: every GPU that loads the library holds these bytes until the
-// process exits.  In host code the symbol is only a stand-in for the device
-// array; its device address comes from cudaGetSymbolAddress below.
+// The scratch.  In host code the symbol is only a stand-in for the device
+// array; its device address comes from cudaGetSymbolAddress below.  The CUDA
+// runtime loads this file's module (and with it reserves these bytes on the
+// device) lazily by default: on the first cudaGetSymbolAddress or the first
+// launch of one of its kernels on a device, i.e. on the first call of the entry
+// point there.  From then on the device holds the bytes until the process exits.
 constexpr size_t kStaticScratchBytes = CSATTN_DECODE_STATIC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
@@ -64,11 +67,33 @@ extern "C" int csattn_attn_decode_noalloc(const void* q, const void* k_cache,
                                           void* out, int B, int Hq, int Hkv, int Lmax, int d,
                                           int dtype, float scale, int max_seq_len,
                                           int num_splits, void* stream) {
+  const char* fn = "attn_decode_noalloc";
+  // Every argument error is reported before the first CUDA call (the scratch
+  // lookup below may load the module that holds the buffer).
+  int rc = csattn::attn_decode_check_ptrs(fn, q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv,
+                                          Lmax, d, dtype, scale, max_seq_len, num_splits);
+  if (rc != CSATTN_OK) return rc;
+  if (num_splits > 0) {
+    // the split count the decode will use for an explicit request (64-key multiples)
+    const int per = (max_seq_len + num_splits - 1) / num_splits;
+    const int chunk = ((per + 63) / 64) * 64;
+    const size_t splits = static_cast<size_t>((max_seq_len + chunk - 1) / chunk);
+    const size_t need = static_cast<size_t>(B) * Hq * splits * (static_cast<size_t>(d) + 2) * 4;
+    if (need > csattn::kStaticScratchBytes) {
+      char buf[200];
+      snprintf(buf, sizeof(buf),
+               "%s: the split partials need %zu bytes, more than the %zu-byte static scratch "
+               "(fewer splits, or csattn_attn_decode with a workspace)",
+               fn, need, csattn::kStaticScratchBytes);
+      csattn::set_last_error(buf);
+      return CSATTN_ERR_WORKSPACE;
+    }
+  }
   void* scratch = nullptr;
   const char* why = "";
-  const int rc = csattn::scratch_address(&scratch, &why);
+  rc = csattn::scratch_address(&scratch, &why);
   if (rc != CSATTN_OK) {
-    csattn::set_last_error((std::string("attn_decode_noalloc: static scratch lookup: ") + why).c_str());
+    csattn::set_last_error((std::string(fn) + ": static scratch lookup: " + why).c_str());
     return rc;
   }
   // The decode kernels write every partial that the merge reads in the same
@@ -79,9 +104,9 @@ extern "C" int csattn_attn_decode_noalloc(const void* q, const void* k_cache,
   if (st == CSATTN_ERR_WORKSPACE) {
     char buf[160];
     snprintf(buf, sizeof(buf),
-             "attn_decode_noalloc: the split partials exceed the %zu-byte static scratch "
+             "%s: the split partials exceed the %zu-byte static scratch "
              "(fewer splits or csattn_attn_decode with a workspace); ",
-             csattn::kStaticScratchBytes);
+             fn, csattn::kStaticScratchBytes);
     csattn::set_last_error((std::string(buf) + csattn_last_error()).c_str());
   }
   return st;

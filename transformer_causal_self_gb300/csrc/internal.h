@@ -133,6 +133,12 @@ int attn_fwd_check(const char* fn, int B, int Hq, int Hkv, int T, int d, int dty
 int attn_decode_check(const char* fn, int B, int Hq, int Hkv, int Lmax, int d, int dtype,
                       float scale, int max_seq_len, int num_splits);
 
+// The same checks including the pointers (null, alignment).  Touches no CUDA state.
+int attn_decode_check_ptrs(const char* fn, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* seq_lens, const void* out, int B,
+                           int Hq, int Hkv, int Lmax, int d, int dtype, float scale,
+                           int max_seq_len, int num_splits);
+
 // Driver entry point for cuTensorMapEncodeTiled (nullptr if unavailable).
 void* tensor_map_encoder();
 
