@@ -786,9 +786,14 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
 def run_profile_case(args):
     """A short program for ncu: one warm-up and one timed launch of one kernel group.
 
-    fwd:    the llama_gqa_bf16 prefill (RoPE pass + attention kernel), full size.
-    decode: the decode_bf16 workload with B=16 sequences (0.5 GB of cache).
-    bwd:    the llama_gqa_bf16 backward (after one forward for out and lse), full size.
+    fwd:     the llama_gqa_bf16 prefill (RoPE pass + attention kernel), full size.
+    decode:  the decode_bf16 workload with B=16 sequences (0.5 GB of cache).
+    bwd:     the llama_gqa_bf16 backward (after one forward for out and lse), full size.
+    gpt2:    the gpt2_bf16 prefill (d=64 attention kernel), full size.
+    rope:    the RoPE pass over the llama_gqa_bf16 keys.
+    append:  the 1024-token chunk append of the bench row.
+    paged16: the 1024-query chunk over 16-row pages (page gather, then the paged kernel).
+    step:    one fused decode step (RoPE + append, then the decode) on B=16 sequences.
     """
     import torch
 
@@ -813,6 +818,55 @@ def run_profile_case(args):
         for _ in range(2):
             csattn.attn_bwd(q, k, v, out, do, lse, causal=True, rope_base=w.rope_base,
                             scale=w.scale)
+    elif args.profile == "gpt2":
+        w = W.WORKLOADS["gpt2_bf16"]
+        q, k, v = (t.to(dev) for t in W.make_prefill_inputs(w))
+        out = torch.empty_like(q)
+        for _ in range(2):
+            csattn.attn_fwd(q, k, v, out, causal=True, rope_base=0.0, scale=w.scale)
+    elif args.profile == "rope":
+        w = W.WORKLOADS[PREFILL]
+        _, k, _ = (t.to(dev) for t in W.make_prefill_inputs(w))
+        k_rot = torch.empty_like(k)
+        for _ in range(2):
+            csattn.rope_rotate(k, k_rot, rope_base=w.rope_base)
+    elif args.profile == "append":
+        wc = W.WORKLOADS["llama_chunk_bf16"]
+        g = torch.Generator()
+        g.manual_seed(10)
+        kn = torch.randn(wc.B, wc.Hkv, 1024, wc.d, generator=g).to(torch.bfloat16).to(dev)
+        vn = torch.randn(wc.B, wc.Hkv, 1024, wc.d, generator=g).to(torch.bfloat16).to(dev)
+        kca = torch.zeros(wc.B, wc.Hkv, wc.Tk, wc.d, dtype=torch.bfloat16, device=dev)
+        vca = torch.zeros_like(kca)
+        at = torch.full((wc.B,), wc.q_offset, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            csattn.cache_append(kn, vn, kca, vca, at, rope_base=wc.rope_base)
+    elif args.profile == "paged16":
+        # the 1024-query chunk over 16-row pages: page gather into the workspace, then the
+        # paged prefill kernel
+        wc = W.WORKLOADS["llama_chunk_bf16"]
+        q, k, v = (t.to(dev) for t in W.make_chunk_inputs(wc))
+        k_rot = csattn.rope_rotate(k, rope_base=wc.rope_base)
+        kp, vp, table = W.page_cache(k_rot, v, [wc.Tk] * wc.B, 16, seed=12)
+        clen = torch.full((wc.B,), wc.q_offset, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        for _ in range(2):
+            csattn.attn_prefill_paged(q, kp, vp, table, clen, o, causal=True,
+                                      rope_base=wc.rope_base, scale=wc.scale)
+    elif args.profile == "step":
+        # one decode step (RoPE + append of the new token, then the decode) on B=16
+        w = W.WORKLOADS[DECODE].with_(B=16)
+        qd, kc, vc, lens = W.make_decode_inputs(w)
+        kc, vc = kc.to(dev), vc.to(dev)
+        g = torch.Generator()
+        g.manual_seed(7)
+        qn = torch.randn(w.B, w.Hq, 1, w.d, generator=g).to(torch.bfloat16).to(dev)
+        kn = torch.randn(w.B, w.Hkv, 1, w.d, generator=g).to(torch.bfloat16).to(dev)
+        vn = torch.randn(w.B, w.Hkv, 1, w.d, generator=g).to(torch.bfloat16).to(dev)
+        pos = (lens - 1).to(torch.int32).to(dev)
+        for _ in range(2):
+            csattn.attn_decode_step(qn, kn, vn, kc, vc, pos, rope_base=10000.0, scale=w.scale,
+                                    max_seq_len=int(lens.max()))
     else:
         w = W.WORKLOADS[DECODE].with_(B=16)
         qd, kc, vc, lens = W.make_decode_inputs(w)
@@ -836,7 +890,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the timing of the chunked-prefill and decode-step rows")
-    ap.add_argument("--profile", choices=["fwd", "decode", "bwd"], default=None,
+    ap.add_argument("--profile", choices=["fwd", "decode", "bwd", "gpt2", "rope", "append",
+                                          "paged16", "step"], default=None,
                     help="run a short single-kernel case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:
