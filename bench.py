@@ -151,15 +151,14 @@ def _source_hash(*names):
     return h.hexdigest()[:16]
 
 
-def _traffic(kernel_file, *deps):
-    """DRAM bytes per launch from the committed ncu summary, if it is for this source
-    (the kernel's file plus the headers it includes)."""
+def _traffic(key):
+    """DRAM bytes per launch of a row's dominant kernel from the committed ncu table, if
+    it was taken on the current sources (the kernel's file plus the headers it includes)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            t = json.load(f)
-        e = t[kernel_file]
-        if e.get("source_sha") == _source_hash(kernel_file, *deps):
+            e = json.load(f)[key]
+        if e.get("source_sha") == _source_hash(*e["sources"]):
             return float(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError, TypeError):
         pass
@@ -454,13 +453,13 @@ def run_gpu(args):
 
     roof = {"bound": "tensor", "achieved": round(fwd_tflops, 2), "peak": tf_burst,
             "unit": "TFLOP/s", "frac": round(fwd_tflops / tf_burst, 4),
-            "traffic": _traffic("fwd_sm103a_d128.cu", "fwd_units.cuh", "common.cuh"),
+            "traffic": _traffic("fwd_llama"),
             "kernel": "fwd_d128_kernel",
             "peak_kind": f"{peak_kind} bf16 dense burst (cuBLAS)",
             "frac_of_sustained": round(fwd_tflops / tf_sust, 4),
             "frac_of_spec_2250": round(fwd_tflops / 2250.0, 4)}
     dec_roof = {"bound": "hbm", "achieved": round(dec_gbs_one, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(dec_gbs_one / hbm_peak, 4), "traffic": _traffic("decode.cu", "common.cuh"),
+                "frac": round(dec_gbs_one / hbm_peak, 4), "traffic": _traffic("decode_b64"),
                 "kernel": "decode_bf16_kernel<128> + decode_combine_kernel",
                 "peak_kind": f"{peak_kind} HBM copy", "frac_of_spec_8000": round(dec_gbs_one / 8000.0, 4)}
     line = {
@@ -536,7 +535,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
         "flops": wc.flops(), "l2": "flushed before each launch",
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": _traffic("chunk"),
                      "kernel": "fwd_d128_kernel"}}
     # the same chunk over a paged cache: rows 0..4095 in 256-row pages of a shuffled pool,
     # cache_lens = 3072 (csattn_attn_prefill_paged)
@@ -563,7 +562,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
         "flops": wc.flops(), "l2": "flushed before each launch",
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": _traffic("paged256"),
                      "kernel": "fwd_d128_kernel (paged K/V)"}}
     del q, k, v, k_rot, o, kp, vp, table, clen
 
@@ -603,7 +602,9 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
             "flops": wq.flops(),
             "l2": "flushed before each launch" if flush_it else "inputs larger than L2",
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
-                         "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                         "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4),
+                         "traffic": _traffic({"long_gqa_bf16": "long", "gpt2_bf16": "gpt2",
+                                              "llama_gqa_bf16_x4": "x4"}[wl]),
                          "kernel": "fwd_d128_kernel" if wq.d == 128 else "fwd_sm103a_kernel<64>"}}
         del q, k, v, o, ws_f
 
@@ -631,7 +632,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
         "flops": wx.flops(), "l2": "flushed before each launch",
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": _traffic("cross"),
                      "kernel": "fwd_d128_kernel"}}
     del q, k, v, o, flush
 
@@ -663,7 +664,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
                     "token's q, k rotated (RoPE 1e4) and k, v written at row L_b - 1 in the call",
         "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": dbytes,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "frac": round(gbs / hbm_peak, 4), "traffic": _traffic("decode_b64"),
                      "kernel": "decode_append_kernel + decode_bf16_kernel<128> + "
                                "decode_combine_kernel"}}
     # the same decode over a paged copy of the cache: 128-row pages in a shuffled pool
@@ -689,7 +690,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
                     "128-row pages, scattered over a shuffled pool (block table per sequence)",
         "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": dbytes,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "frac": round(gbs / hbm_peak, 4), "traffic": _traffic("decpaged128"),
                      "kernel": "decode_bf16_kernel<128> (paged reads) + decode_combine_kernel"}}
     del kp, vp, table
     # the same decode over 16-row pages (the block size of vLLM-style caches)
@@ -715,7 +716,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
                     "16-row pages of a shuffled pool",
         "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": dbytes,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "frac": round(gbs / hbm_peak, 4), "traffic": _traffic("decpaged16"),
                      "kernel": "decode_bf16_kernel<128> (paged reads, one box per lane) + "
                                "decode_combine_kernel"}}
     del kp, vp, table
@@ -745,7 +746,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
                     "Lmax=4096, rows 3072..4095), keys rotated (RoPE 1e4)",
         "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": abytes,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "frac": round(gbs / hbm_peak, 4), "traffic": _traffic("append"),
                      "kernel": "cache_append_kernel"}}
     del kn, vn, kca, vca
     # backward of the headline prefill (dq, dk, dv), FLOPs = 2.5x the forward's (the
@@ -778,7 +779,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "workload": "llama_gqa_bf16 backward (dq, dk, dv; RoPE 1e4; inputs larger than L2)",
         "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": fl,
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": _traffic("bwd"),
                      "kernel": "bwd_kv_tc_kernel + bwd_q_tc_kernel (tcgen05)"}}
     return out
 
@@ -794,6 +795,9 @@ def run_profile_case(args):
     append:  the 1024-token chunk append of the bench row.
     paged16: the 1024-query chunk over 16-row pages (page gather, then the paged kernel).
     step:    one fused decode step (RoPE + append, then the decode) on B=16 sequences.
+    chunk, cross, paged256: the chunked-prefill, rectangular and paged-prefill rows.
+    x4, long: the x4-seed and long-context prefills (keys rotated first).
+    decpaged128, decpaged16: the paged-decode rows (decode_bf16, B=64).
     """
     import torch
 
@@ -853,6 +857,42 @@ def run_profile_case(args):
         for _ in range(2):
             csattn.attn_prefill_paged(q, kp, vp, table, clen, o, causal=True,
                                       rope_base=wc.rope_base, scale=wc.scale)
+    elif args.profile in ("chunk", "cross", "paged256"):
+        wc = W.WORKLOADS["llama_chunk_bf16" if args.profile != "cross" else "llama_cross_bf16"]
+        q, k, v = (t.to(dev) for t in W.make_chunk_inputs(wc))
+        k_rot = csattn.rope_rotate(k, rope_base=wc.rope_base) if wc.rope_base > 0 else k
+        o = torch.empty_like(q)
+        if args.profile == "paged256":
+            kp, vp, table = W.page_cache(k_rot, v, [wc.Tk] * wc.B, 256, seed=12)
+            clen = torch.full((wc.B,), wc.q_offset, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            if args.profile == "paged256":
+                csattn.attn_prefill_paged(q, kp, vp, table, clen, o, causal=True,
+                                          rope_base=wc.rope_base, scale=wc.scale)
+            else:
+                csattn.attn_fwd_ext(q, k_rot, v, o, q_offset=wc.q_offset, causal=wc.causal,
+                                    rope_base=wc.rope_base, scale=wc.scale,
+                                    k_prerotated=wc.rope_base > 0)
+    elif args.profile in ("x4", "long"):
+        w = W.WORKLOADS["llama_gqa_bf16_x4" if args.profile == "x4" else "long_gqa_bf16"]
+        q, k, v = (t.to(dev) for t in W.make_prefill_inputs(w))
+        k_rot = csattn.rope_rotate(k, rope_base=w.rope_base)
+        out = torch.empty_like(q)
+        for _ in range(2):
+            csattn.attn_fwd(q, k_rot, v, out, causal=True, rope_base=w.rope_base, scale=w.scale,
+                            k_prerotated=True)
+    elif args.profile in ("decpaged128", "decpaged16"):
+        # the decode_bf16 batch (B=64) over a paged copy of its cache
+        w = W.WORKLOADS[DECODE]
+        qd, kc, vc, lens = W.make_decode_inputs(w)
+        kc, vc = kc.to(dev), vc.to(dev)
+        page = 128 if args.profile == "decpaged128" else 16
+        kp, vp, table = W.page_cache(kc, vc, lens, page, seed=9 if page == 128 else 10)
+        del kc, vc
+        qd, lens_d = qd.to(dev), lens.to(dev)
+        for _ in range(2):
+            csattn.attn_decode_paged(qd, kp, vp, table, lens_d, scale=w.scale,
+                                     max_seq_len=int(lens.max()))
     elif args.profile == "step":
         # one decode step (RoPE + append of the new token, then the decode) on B=16
         w = W.WORKLOADS[DECODE].with_(B=16)
@@ -891,7 +931,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the timing of the chunked-prefill and decode-step rows")
     ap.add_argument("--profile", choices=["fwd", "decode", "bwd", "gpt2", "rope", "append",
-                                          "paged16", "step"], default=None,
+                                          "paged16", "step", "chunk", "cross", "paged256", "x4",
+                                          "long", "decpaged128", "decpaged16"], default=None,
                     help="run a short single-kernel case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:
