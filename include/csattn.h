@@ -207,6 +207,47 @@ int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out
                     void* stream);
 
 /*
+ * Bytes of device workspace csattn_attn_bwd_ext needs: fp32 rowsum(dout o out)
+ * [B, Hq, Tq] plus, with RoPE, the rotated q [B, Hq, Tq, d] and k [B, Hkv, Tk, d]
+ * in the input dtype (each block 256-byte aligned).  0 for an unknown dtype or a
+ * size below 1.
+ */
+size_t csattn_bwd_ext_workspace_size(int B, int Hq, int Hkv, int Tq, int Tk, int d, int dtype,
+                                     float rope_base);
+
+/*
+ * Backward of csattn_attn_fwd_ext: the gradients of sum(out * dout) for a chunk
+ * of Tq queries after a prefix ("The Transformer architecture", "Hands-on": the
+ * query at position p sees keys 0..p) or for rectangular attention, with value
+ * width d_v ("Transformer Math and Implementation Deep Dive", "Attention
+ * Equation": Tq and Tk, d_k and d_v need not match).  The formulas are those of
+ * csattn_attn_bwd with the mask and positions of csattn_attn_fwd_ext: query row i
+ * sits at position q_offset + i, key j at j; with causal = 1 row i sees keys
+ * j <= q_offset + i, with causal = 0 every key.
+ *   q [B, Hq, Tq, d];  k [B, Hkv, Tk, d];  v [B, Hkv, Tk, d_v]
+ *   out, dout    [B, Hq, Tq, d_v]: the forward's output and its gradient
+ *   lse          fp32 [B, Hq, Tq]: the forward's natural-log log-sum-exp
+ *   dq [B, Hq, Tq, d], dk [B, Hkv, Tk, d], dv [B, Hkv, Tk, d_v]  written, q's dtype.
+ *                A key no query sees (causal, j > q_offset + Tq - 1) gets dk = dv = 0.
+ *   d_v          <= 0 means d_v = d.  bf16: d, d_v in {64, 128} (tcgen05 kernels);
+ *                fp32: d, d_v in {16, 32, 64, 128} (SIMT kernels, fp32 throughout).
+ *   rope_base    > 0: q is rotated at q_offset + i and k at 0..Tk-1 (both given
+ *                unrotated: CSATTN_ROPE_K_PREROTATED is CSATTN_ERR_UNSUPPORTED);
+ *                dq and dk are the gradients with respect to the unrotated q and k.
+ *   workspace    >= csattn_bwd_ext_workspace_size() bytes, 16-byte aligned,
+ *                caller-owned, in use until the call's work on `stream` completes.
+ * Other arguments, ownership and errors as csattn_attn_bwd, which is this call
+ * with Tq = Tk = T, q_offset = 0 and d_v = d.  Requirements: Tq, Tk >= 1,
+ * 0 <= q_offset < 2^24, Tq, Tk < 2^24; with RoPE q_offset + Tq <= 49152 and
+ * Tk <= 49152 (CSATTN_ERR_UNSUPPORTED otherwise).  Asynchronous on `stream`.
+ */
+int csattn_attn_bwd_ext(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int Hq, int Hkv, int Tq, int Tk, int q_offset, int d, int d_v, int dtype,
+                        int causal, float rope_base, int rope_layout, float scale,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * RoPE of x [B, H, T, d] into x_rot (same shape; must not overlap x), at
  * positions 0..T-1 with theta_p = rope_base^(-2p/d), rounded to the input
  * dtype.  This is the rotation csattn_attn_fwd applies to its keys, exposed to
@@ -245,6 +286,25 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int Lmax,
                        int d, int dtype, float scale, int max_seq_len, int num_splits,
                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * csattn_attn_decode with values of their own width dv ("Transformer Math and
+ * Implementation Deep Dive", "Attention Equation": the weights come from q and k,
+ * v sets the output width).
+ *   q [B, Hq, 1, d];  k_cache [B, Hkv, Lmax, d];  v_cache [B, Hkv, Lmax, dv];
+ *   out [B, Hq, 1, dv]
+ *   d, dv        each 64 or 128 (CSATTN_ERR_UNSUPPORTED otherwise); dv <= 0 means
+ *                dv = d, which is csattn_attn_decode.  The default scale is 1/sqrt(d).
+ *   workspace    >= csattn_decode_workspace_size(B, Hq, Lmax, dv, num_splits) bytes
+ *                (the split partials have the width of v).
+ * Other arguments, checks and errors as csattn_attn_decode (messages name
+ * attn_decode_ext).
+ */
+int csattn_attn_decode_ext(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int Lmax,
+                           int d, int dv, int dtype, float scale, int max_seq_len,
+                           int num_splits, void* workspace, size_t workspace_bytes,
+                           void* stream);
 
 /*
  * Bytes of device workspace csattn_attn_decode_host needs: device copies of q, the

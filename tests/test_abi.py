@@ -441,6 +441,74 @@ def test_bwd_workspace_size(lib):
     assert lib.csattn_bwd_workspace_size(0, 32, 8, 4096, 128, 1, 10000.0) == 0
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(dout=None), -1),
+    (dict(Tq=0), -1),
+    (dict(Tk=0), -1),
+    (dict(q_offset=-1), -1),
+    (dict(Hq=6, Hkv=4), -1),
+    (dict(causal=2), -1),
+    (dict(rope_layout=5), -1),
+    (dict(rope_base=10000.0, rope_layout=0x100), -2),
+    (dict(d_v=32), -2),
+    (dict(d=256), -2),
+    (dict(dtype=0, d_v=48), -2),
+    (dict(q_offset=1 << 24), -2),
+    (dict(rope_base=10000.0, q_offset=49100, Tq=100), -2),
+    (dict(rope_base=10000.0, Tk=50000), -2),
+    (dict(dk=FAKE + 8), -1),
+    (dict(ws=FAKE, ws_bytes=512), -5),
+])
+def test_bwd_ext_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, dout=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             B=1, Hq=4, Hkv=2, Tq=64, Tk=192, q_offset=128, d=128, d_v=64, dtype=1, causal=1,
+             rope_base=0.0, rope_layout=0, scale=0.0, ws=FAKE, ws_bytes=1 << 24)
+    a.update(kw)
+    rc = lib.csattn_attn_bwd_ext(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"], a["dq"],
+                                 a["dk"], a["dv"], a["B"], a["Hq"], a["Hkv"], a["Tq"], a["Tk"],
+                                 a["q_offset"], a["d"], a["d_v"], a["dtype"], a["causal"],
+                                 a["rope_base"], a["rope_layout"], a["scale"], a["ws"],
+                                 a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"attn_bwd_ext" in lib.csattn_last_error()
+
+
+def test_bwd_ext_workspace_size(lib):
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    qrows = 2 * 8 * 300
+    assert lib.csattn_bwd_ext_workspace_size(2, 8, 2, 300, 1000, 64, 1, 0.0) == al(qrows * 4)
+    assert lib.csattn_bwd_ext_workspace_size(2, 8, 2, 300, 1000, 64, 1, 10000.0) == \
+        al(qrows * 4) + al(qrows * 64 * 2) + al(2 * 2 * 1000 * 64 * 2)
+    assert lib.csattn_bwd_ext_workspace_size(2, 8, 2, 300, 1000, 32, 0, 10000.0) == \
+        al(qrows * 4) + al(qrows * 32 * 4) + al(2 * 2 * 1000 * 32 * 4)
+    assert lib.csattn_bwd_ext_workspace_size(2, 8, 2, 300, 0, 64, 1, 0.0) == 0
+    for T in (1, 77, 4096):  # the square call's size is the ext size at Tq = Tk = T
+        assert lib.csattn_bwd_workspace_size(3, 8, 2, T, 128, 1, 10000.0) == \
+            lib.csattn_bwd_ext_workspace_size(3, 8, 2, T, T, 128, 1, 10000.0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(v=None), -1),
+    (dict(Hq=6, Hkv=4), -1),
+    (dict(dv=32), -2),
+    (dict(dv=256), -2),
+    (dict(d=96), -2),
+    (dict(dtype=0), -2),
+    (dict(max_seq_len=0), -1),
+    (dict(out=FAKE + 2), -1),
+    (dict(ws=FAKE, ws_bytes=64), -5),
+])
+def test_decode_ext_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, lens=FAKE, out=FAKE, B=2, Hq=8, Hkv=2, Lmax=512, d=128,
+             dv=64, dtype=1, scale=0.0, max_seq_len=512, splits=4, ws=FAKE, ws_bytes=1 << 24)
+    a.update(kw)
+    rc = lib.csattn_attn_decode_ext(a["q"], a["k"], a["v"], a["lens"], a["out"], a["B"], a["Hq"],
+                                    a["Hkv"], a["Lmax"], a["d"], a["dv"], a["dtype"], a["scale"],
+                                    a["max_seq_len"], a["splits"], a["ws"], a["ws_bytes"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"attn_decode_ext" in lib.csattn_last_error()
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.csattn_selftest_bounded_wait(0, None) == -1
     assert lib.csattn_selftest_bounded_wait(2000000, None) == -1

@@ -22,27 +22,10 @@ import torch
 import attn_workloads as W
 import transformer_causal_self_gb300 as csattn
 from oracle import attn as OA
+from tests.gpu_helpers import assert_grad_close as _close
 from tests.gpu_helpers import dev, to_np
 
 pytestmark = pytest.mark.gpu
-
-
-def _half_ulp_bf16(x):
-    """Half a bf16 ulp at |x| (8 significant bits): 2^(e-8) for |x| in [2^e, 2^(e+1))."""
-    x = abs(float(x))
-    return 0.0 if x == 0.0 else math.ldexp(1.0, math.frexp(x)[1] - 9)
-
-
-def _close(got, ref, what, rl2_tol=5e-3, abs_tol=2e-2, floor=1e-3, bf16_storage=True):
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
-    assert np.all(np.isfinite(got)), f"{what}: non-finite"
-    err = float(np.max(np.abs(got - ref)))
-    rl2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), floor * math.sqrt(ref.size)))
-    ref_max = float(np.max(np.abs(ref)))
-    bound = abs_tol + (_half_ulp_bf16(ref_max) if bf16_storage else 0.0)
-    assert rl2 <= rl2_tol and err <= bound, \
-        f"{what}: max-abs {err:.3e} (bound {bound:.3e}, ref max {ref_max:.3e}), rel-L2 {rl2:.3e}"
 
 
 def _run(q, k, v, do, causal, base, layout, scale):

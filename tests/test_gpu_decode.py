@@ -108,3 +108,41 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     ref = OA.attention(q, k, v, causal=True, rope_base=w.rope_base, scale=w.scale,
                        operand_dtype="bf16")
     assert_bf16_close(to_np(out), ref, "after timeout")
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,dv", [(16, 4, 128, 64), (8, 2, 64, 128), (32, 2, 64, 128),
+                                          (6, 6, 128, 64)])
+def test_decode_value_width_differs(Hq, Hkv, d, dv):
+    """csattn_attn_decode_ext: keys d wide, values and output dv wide ("Transformer Math
+    and Implementation Deep Dive", "Attention Equation"), against the oracle over ragged
+    lengths (NaN past each sequence's rows) and several split counts."""
+    lens = [1, 63, 64, 65, 300, 1000, 777]
+    B, Lmax = len(lens), 1000
+    g = torch.Generator()
+    g.manual_seed(Hq + d + 3 * dv)
+    q = torch.randn(B, Hq, 1, d, generator=g).to(torch.bfloat16)
+    kc = torch.full((B, Hkv, Lmax, d), float("nan")).to(torch.bfloat16)
+    vc = torch.full((B, Hkv, Lmax, dv), float("nan")).to(torch.bfloat16)
+    for b, L in enumerate(lens):
+        kc[b, :, :L] = torch.randn(Hkv, L, d, generator=g).to(torch.bfloat16)
+        vc[b, :, :L] = torch.randn(Hkv, L, dv, generator=g).to(torch.bfloat16)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    ref = OA.decode(q, kc, vc, sl.numpy())
+    for splits in (0, 1, 5):
+        out = csattn.attn_decode_ext(q.to(dev()), kc.to(dev()), vc.to(dev()), sl.to(dev()),
+                                     max_seq_len=Lmax, num_splits=splits)
+        csattn.check_status()
+        assert out.shape == (B, Hq, 1, dv)
+        assert_bf16_close(to_np(out), ref, f"decode_ext d={d} dv={dv} splits={splits}")
+
+
+def test_decode_ext_equal_widths_is_decode():
+    """dv = d through csattn_attn_decode_ext runs the same kernels as csattn_attn_decode:
+    the outputs are equal bit for bit."""
+    w = W.WORKLOADS["decode_bf16"].with_(B=6, Lmax=2048, Lmin=1)
+    q, kc, vc, sl = (t.to(dev()) for t in W.make_decode_inputs(w))
+    sl = sl.to(torch.int32)
+    a = csattn.attn_decode(q, kc, vc, sl, scale=w.scale, max_seq_len=2048)
+    b = csattn.attn_decode_ext(q, kc, vc, sl, scale=w.scale, max_seq_len=2048)
+    csattn.check_status()
+    assert torch.equal(a, b)

@@ -14,9 +14,13 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "CsattnError", "library_path", "load_library", "attn_fwd", "attn_fwd_host", "attn_decode",
-    "attn_decode_host", "rope_rotate", "fwd_host_workspace_size", "decode_host_workspace_size",
-    "fwd_workspace_size", "decode_workspace_size", "check_status",
+    "CsattnError", "library_path", "load_library", "attn_fwd", "attn_fwd_host", "attn_fwd_ext",
+    "attn_bwd", "attn_bwd_ext", "attn_decode", "attn_decode_ext", "attn_decode_host",
+    "attn_decode_step",
+    "attn_decode_paged", "attn_prefill_paged", "cache_append", "cache_append_paged",
+    "rope_rotate", "fwd_workspace_size", "fwd_ext_workspace_size", "fwd_host_workspace_size",
+    "bwd_workspace_size", "bwd_ext_workspace_size", "decode_workspace_size",
+    "decode_host_workspace_size", "decode_step_workspace_size", "check_status",
     "selftest_bounded_wait", "EXPORTED_SYMBOLS",
 ]
 
@@ -50,10 +54,15 @@ _SIGNATURES = {
     "csattn_bwd_workspace_size": (_c_size, [_c_int] * 6 + [_c_float]),
     "csattn_attn_bwd": (_c_int, [_vp] * 9 + [_c_int] * 7 + [_c_float, _c_int, _c_float, _vp,
                                                              _c_size, _vp]),
+    "csattn_bwd_ext_workspace_size": (_c_size, [_c_int] * 7 + [_c_float]),
+    "csattn_attn_bwd_ext": (_c_int, [_vp] * 9 + [_c_int] * 10 + [_c_float, _c_int, _c_float, _vp,
+                                                                  _c_size, _vp]),
     "csattn_rope_rotate": (_c_int, [_vp, _vp] + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "csattn_decode_workspace_size": (_c_size, [_c_int] * 5),
     "csattn_attn_decode": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp,
                                                                 _c_size, _vp]),
+    "csattn_attn_decode_ext": (_c_int, [_vp] * 5 + [_c_int] * 7 + [_c_float, _c_int, _c_int, _vp,
+                                                                    _c_size, _vp]),
     "csattn_attn_decode_noalloc": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int,
                                                                         _vp]),
     "csattn_decode_step_workspace_size": (_c_size, [_c_int] * 5),
@@ -139,6 +148,12 @@ def fwd_workspace_size(B, Hq, Hkv, T, d, dtype: torch.dtype, rope_base: float) -
 def fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, dtype: torch.dtype, rope_base: float) -> int:
     code = CSATTN_BF16 if dtype == torch.bfloat16 else CSATTN_F32
     return int(load_library().csattn_fwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, code,
+                                                            float(rope_base)))
+
+
+def bwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, dtype: torch.dtype, rope_base: float) -> int:
+    code = CSATTN_BF16 if dtype == torch.bfloat16 else CSATTN_F32
+    return int(load_library().csattn_bwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, code,
                                                             float(rope_base)))
 
 
@@ -347,6 +362,70 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
                                float(rope_base), _ROPE_LAYOUT[rope_layout], float(scale),
                                workspace.data_ptr(), workspace.numel(), _stream_handle(stream)))
     return dq, dk, dv
+
+
+def attn_bwd_ext(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                 dout: torch.Tensor, lse: torch.Tensor, *, q_offset: int = 0, causal: bool = True,
+                 rope_base: float = 0.0, scale: float = 0.0, rope_layout: str = "split_half",
+                 dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+                 dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 stream=None):
+    """Gradients of sum(out * dout) for attn_fwd_ext (C: csattn_attn_bwd_ext).
+
+    q [B,Hq,Tq,d], k [B,Hkv,Tk,d], v [B,Hkv,Tk,dv]; out, dout [B,Hq,Tq,dv]; lse fp32
+    [B,Hq,Tq] from the forward with the same q_offset, causal and RoPE arguments.
+    Returns dq, dk, dv shaped like q, k, v.
+    """
+    _need_cuda(q, k, v, out, dout, lse)
+    B, Hq, Tq, d = q.shape
+    Hkv, Tk = k.shape[1], k.shape[2]
+    d_v = v.shape[3]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need_cuda(dq, dk, dv)
+    if workspace is None:
+        n = bwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, q.dtype, rope_base)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    lib = load_library()
+    _check(lib.csattn_attn_bwd_ext(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), B, Hq, Hkv, Tq, Tk, int(q_offset), d, d_v,
+                                   _dtype_code(q), int(bool(causal)), float(rope_base),
+                                   _ROPE_LAYOUT[rope_layout], float(scale), workspace.data_ptr(),
+                                   workspace.numel(), _stream_handle(stream)))
+    return dq, dk, dv
+
+
+def attn_decode_ext(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                    seq_lens: torch.Tensor, out: Optional[torch.Tensor] = None, *,
+                    scale: float = 0.0, max_seq_len: Optional[int] = None, num_splits: int = 0,
+                    workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """KV-cache decode with a value width of its own (C: csattn_attn_decode_ext).
+
+    q [B,Hq,1,d], k_cache [B,Hkv,Lmax,d], v_cache [B,Hkv,Lmax,dv]; returns out
+    [B,Hq,1,dv].  Otherwise as attn_decode.
+    """
+    _need_cuda(q, k_cache, v_cache, seq_lens)
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    B, Hq, _, d = q.shape
+    Hkv, Lmax, dv = k_cache.shape[1], k_cache.shape[2], v_cache.shape[3]
+    if max_seq_len is None:
+        max_seq_len = Lmax
+    if out is None:
+        out = q.new_empty((B, Hq, 1, dv))
+    _need_cuda(out)
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_size(B, Hq, Lmax, dv, num_splits),
+                                dtype=torch.uint8, device=q.device)
+    lib = load_library()
+    _check(lib.csattn_attn_decode_ext(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                      seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lmax, d,
+                                      dv, _dtype_code(q), float(scale), int(max_seq_len),
+                                      int(num_splits), workspace.data_ptr(), workspace.numel(),
+                                      _stream_handle(stream)))
+    return out
 
 
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

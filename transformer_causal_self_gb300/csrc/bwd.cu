@@ -13,7 +13,7 @@
 // Jacobian transpose is the inverse rotation) and lse the forward's log-sum-exp.
 //
 // This file holds the row-dot kernel for D and the dispatch; the dK/dV and dQ
-// kernels (tcgen05, d = 64 and 128) are in bwd_tc.cu: two kernels, no atomics,
+// kernels (tcgen05, d and d_v each 64 or 128) are in bwd_tc.cu: two kernels, no atomics,
 // S and dP recomputed in both (FlashAttention-2's split, which trades two extra
 // GEMMs per tile pair for no global atomics).
 #include "internal.h"
@@ -51,12 +51,12 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __
 }  // namespace
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream) {
-  if ((a.d != 64 && a.d != 128) || a.Tq != a.Tk || a.q_off != 0) return cudaErrorInvalidValue;
-  // D = rowsum(dout o out), then the two tcgen05 kernels (bwd_tc.cu)
+  if ((a.d != 64 && a.d != 128) || (a.d_v != 64 && a.d_v != 128)) return cudaErrorInvalidValue;
+  // D = rowsum(dout o out) over the d_v channels, then the two tcgen05 kernels (bwd_tc.cu)
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.Tq;
-  bwd_rowdot_kernel<<<static_cast<unsigned>((rows * (a.d / 8) + 255) / 256), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(a.dout), static_cast<const __nv_bfloat16*>(a.out), a.dvec,
-      rows, a.d);
+  bwd_rowdot_kernel<<<static_cast<unsigned>((rows * (a.d_v / 8) + 255) / 256), 256, 0,
+                      stream>>>(static_cast<const __nv_bfloat16*>(a.dout),
+                                static_cast<const __nv_bfloat16*>(a.out), a.dvec, rows, a.d_v);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_bwd_kv_tc(a, stream);

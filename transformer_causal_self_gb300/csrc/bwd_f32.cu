@@ -1,10 +1,12 @@
 // Backward of causal GQA attention for fp32 inputs on the SIMT cores (FFMA), for
 // fp32 callers that need the gradients close to float64: the same math as
 // bwd.cu (P = exp(S - lse), D = rowsum(dout o out), dS = P o (dout V^T - D),
-// dV = P^T dout, dQ = R^T(scale dS Kr), dK = R^T(scale dS^T Qr)), one thread
-// group of d/16 threads per row, 16 channels each.
+// dV = P^T dout, dQ = R^T(scale dS Kr), dK = R^T(scale dS^T Qr)).  Head sizes d (q,
+// k) and dv (v, out) each in {16, 32, 64, 128}; Tq query rows at positions
+// q_off..q_off+Tq-1, Tk keys at 0..Tk-1.  A row is served by TPR = max(d, dv)/16
+// threads, each holding d/TPR channels of the q/k side and dv/TPR of the v/dout side.
 //
-//   rope_f32_kernel     x_rot = R x at positions 0..T-1 (accurate sine/cosine)
+//   rope_f32_kernel     x_rot = R x at positions pos0 + t (accurate sine/cosine)
 //   rowdot_f32_kernel   D
 //   bwd_dq_f32_kernel   one CTA per (ROWS query rows, query head, batch); K and V
 //                       tiles staged in shared memory; dq rotated back at the end
@@ -18,24 +20,27 @@ namespace {
 constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+template <int D, int DV>
 struct BwdF32Cfg {
-  static constexpr int TPR = D / 16;           // threads per row
+  static constexpr int DMAX = D > DV ? D : DV;
+  static constexpr int TPR = DMAX / 16;        // threads per row
   static constexpr int ROWS = kThreads / TPR;  // rows per CTA
-  static constexpr int KT = (D == 128) ? 16 : 32;  // staged rows of the other side
+  static constexpr int QC = D / TPR;           // q / k channels per thread (2..16)
+  static constexpr int VC = DV / TPR;          // v / dout channels per thread (2..16)
+  static constexpr int KT = (DMAX == 128) ? 16 : 32;  // staged rows of the other side
 };
 
-// x_rot[row] = R_pos x[row] for rows of [B*H, T, d], pos = row % T; one thread per pair.
+// x_rot[row] = R_pos x[row] for rows of [B*H, T, d], pos = pos0 + row % T; one thread per pair.
 __global__ void __launch_bounds__(256) rope_f32_kernel(const float* __restrict__ x,
                                                        float* __restrict__ x_rot, long long rows,
-                                                       int T, int d, int layout,
-                                                       RopeTable theta) {
+                                                       int T, int d, int layout, RopeTable theta,
+                                                       int pos0) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int half = d / 2;
   if (idx >= rows * half) return;
   const long long r = idx / half;
   const int pair = static_cast<int>(idx - r * half);
-  const int pos = static_cast<int>(r % T);
+  const int pos = pos0 + static_cast<int>(r % T);
   int i, j;
   if (layout == 1) {
     i = pair;
@@ -83,132 +88,153 @@ __device__ __forceinline__ void rotate_back_row(float* row, int d, int tpr, int 
   }
 }
 
-// 16 consecutive floats from 16-byte aligned shared memory.
-__device__ __forceinline__ void load16(const float* src, float (&dst)[16]) {
+// N consecutive floats (N = 2, 4, 8 or 16) from shared memory aligned to 4N bytes
+// (N <= 4) or 16 bytes.
+template <int N>
+__device__ __forceinline__ void load_n(const float* src, float (&dst)[N]) {
+  if constexpr (N == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(src);
+    dst[0] = t.x;
+    dst[1] = t.y;
+  } else {
 #pragma unroll
-  for (int c4 = 0; c4 < 4; ++c4) {
-    const float4 t = reinterpret_cast<const float4*>(src)[c4];
-    dst[4 * c4] = t.x;
-    dst[4 * c4 + 1] = t.y;
-    dst[4 * c4 + 2] = t.z;
-    dst[4 * c4 + 3] = t.w;
+    for (int c4 = 0; c4 < N / 4; ++c4) {
+      const float4 t = reinterpret_cast<const float4*>(src)[c4];
+      dst[4 * c4] = t.x;
+      dst[4 * c4 + 1] = t.y;
+      dst[4 * c4 + 2] = t.z;
+      dst[4 * c4 + 3] = t.w;
+    }
   }
 }
 
 struct BwdF32Params {
-  const float* qr;
-  const float* kr;
-  const float* v;
-  const float* dout;
+  const float* qr;    // [B, Hq, Tq, D]
+  const float* kr;    // [B, Hkv, Tk, D]
+  const float* v;     // [B, Hkv, Tk, DV]
+  const float* dout;  // [B, Hq, Tq, DV]
   const float* lse;
   const float* dvec;
   float* dq;
   float* dk;
   float* dv;
-  int Hq, Hkv, T, causal, rope;
+  int Hq, Hkv, Tq, Tk, q_off, causal, rope;
   float scale;
   RopeTable theta;
 };
 
-template <int D>
+template <int D, int DV>
 __global__ void __launch_bounds__(kThreads) bwd_dq_f32_kernel(const BwdF32Params p) {
-  using C = BwdF32Cfg<D>;
+  using C = BwdF32Cfg<D, DV>;
+  constexpr int QC = C::QC, VC = C::VC;
   __shared__ __align__(16) float sk[C::KT * D];
-  __shared__ __align__(16) float sv[C::KT * D];
+  __shared__ __align__(16) float sv[C::KT * DV];
   __shared__ __align__(16) float srow[C::ROWS * D];
   const int tid = threadIdx.x, row = tid / C::TPR, part = tid % C::TPR;
   const int h = blockIdx.y, b = blockIdx.z, g = h / (p.Hq / p.Hkv);
   const int q0 = blockIdx.x * C::ROWS, qi = q0 + row;
-  const bool live = qi < p.T;
-  const size_t qrow = (static_cast<size_t>(b) * p.Hq + h) * p.T + (live ? qi : 0);
-  float q[16], o[16], acc[16];
+  const bool live = qi < p.Tq;
+  const size_t qrow = (static_cast<size_t>(b) * p.Hq + h) * p.Tq + (live ? qi : 0);
+  float q[QC], o[VC], acc[QC];
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    q[c] = live ? p.qr[qrow * D + part * 16 + c] : 0.f;
-    o[c] = live ? p.dout[qrow * D + part * 16 + c] : 0.f;
+  for (int c = 0; c < QC; ++c) {
+    q[c] = live ? p.qr[qrow * D + part * QC + c] : 0.f;
     acc[c] = 0.f;
   }
+#pragma unroll
+  for (int c = 0; c < VC; ++c) o[c] = live ? p.dout[qrow * DV + part * VC + c] : 0.f;
   const float lse2 = live ? p.lse[qrow] * kLog2e : 0.f;
   const float dd = live ? p.dvec[qrow] : 0.f;
-  const float* kh = p.kr + (static_cast<size_t>(b) * p.Hkv + g) * p.T * D;
-  const float* vh = p.v + (static_cast<size_t>(b) * p.Hkv + g) * p.T * D;
-  const int k_end = p.causal ? min(p.T, q0 + C::ROWS) : p.T;
+  const float* kh = p.kr + (static_cast<size_t>(b) * p.Hkv + g) * p.Tk * D;
+  const float* vh = p.v + (static_cast<size_t>(b) * p.Hkv + g) * p.Tk * DV;
+  // causal: keys up to the position of the CTA's last row
+  const int k_end = p.causal ? min(p.Tk, p.q_off + q0 + C::ROWS) : p.Tk;
   for (int k0 = 0; k0 < k_end; k0 += C::KT) {
     const int nk = min(C::KT, k_end - k0);
     __syncthreads();
     for (int e = tid; e < C::KT * D; e += kThreads) {
       const int r = e / D;
       sk[e] = r < nk ? kh[static_cast<size_t>(k0 + r) * D + e % D] : 0.f;
-      sv[e] = r < nk ? vh[static_cast<size_t>(k0 + r) * D + e % D] : 0.f;
+    }
+    for (int e = tid; e < C::KT * DV; e += kThreads) {
+      const int r = e / DV;
+      sv[e] = r < nk ? vh[static_cast<size_t>(k0 + r) * DV + e % DV] : 0.f;
     }
     __syncthreads();
     for (int j = 0; j < nk; ++j) {
-      float kk[16], vv[16];
-      load16(sk + j * D + part * 16, kk);
-      load16(sv + j * D + part * 16, vv);
+      float kk[QC], vv[VC];
+      load_n<QC>(sk + j * D + part * QC, kk);
+      load_n<VC>(sv + j * DV + part * VC, vv);
       float s = 0.f, dp = 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        s = fmaf(q[c], kk[c], s);
-        dp = fmaf(o[c], vv[c], dp);
-      }
+      for (int c = 0; c < QC; ++c) s = fmaf(q[c], kk[c], s);
+#pragma unroll
+      for (int c = 0; c < VC; ++c) dp = fmaf(o[c], vv[c], dp);
 #pragma unroll
       for (int off = 1; off < C::TPR; off <<= 1) {
         s += __shfl_xor_sync(0xffffffffu, s, off);
         dp += __shfl_xor_sync(0xffffffffu, dp, off);
       }
       const int key = k0 + j;
-      if (!live || (p.causal && key > qi)) continue;
+      if (!live || (p.causal && key > p.q_off + qi)) continue;
       const float pr = exp2f(fmaf(s * p.scale, kLog2e, -lse2));
       const float ds = pr * (dp - dd) * p.scale;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) acc[c] = fmaf(ds, kk[c], acc[c]);
+      for (int c = 0; c < QC; ++c) acc[c] = fmaf(ds, kk[c], acc[c]);
     }
   }
   __syncthreads();
 #pragma unroll
-  for (int c = 0; c < 16; ++c) srow[row * D + part * 16 + c] = acc[c];
+  for (int c = 0; c < QC; ++c) srow[row * D + part * QC + c] = acc[c];
   __syncwarp();
-  if (p.rope) rotate_back_row(srow + row * D, D, C::TPR, part, p.rope, qi, p.theta);
+  if (p.rope) rotate_back_row(srow + row * D, D, C::TPR, part, p.rope, p.q_off + qi, p.theta);
   __syncwarp();
   if (live) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) p.dq[qrow * D + part * 16 + c] = srow[row * D + part * 16 + c];
+    for (int c = 0; c < QC; ++c) p.dq[qrow * D + part * QC + c] = srow[row * D + part * QC + c];
   }
 }
 
-template <int D>
+template <int D, int DV>
 __global__ void __launch_bounds__(kThreads) bwd_dkdv_f32_kernel(const BwdF32Params p) {
-  using C = BwdF32Cfg<D>;
+  using C = BwdF32Cfg<D, DV>;
+  constexpr int QC = C::QC, VC = C::VC;
   __shared__ __align__(16) float sq[C::KT * D];
-  __shared__ __align__(16) float so[C::KT * D];
+  __shared__ __align__(16) float so[C::KT * DV];
   __shared__ float slse[C::KT];
   __shared__ float sdd[C::KT];
   __shared__ __align__(16) float srow[C::ROWS * D];
   const int tid = threadIdx.x, row = tid / C::TPR, part = tid % C::TPR;
   const int g = blockIdx.y, b = blockIdx.z, rep = p.Hq / p.Hkv;
   const int k0 = blockIdx.x * C::ROWS, kj = k0 + row;
-  const bool live = kj < p.T;
-  const size_t krow = (static_cast<size_t>(b) * p.Hkv + g) * p.T + (live ? kj : 0);
-  float k[16], v[16], adk[16], adv[16];
+  const bool live = kj < p.Tk;
+  const size_t krow = (static_cast<size_t>(b) * p.Hkv + g) * p.Tk + (live ? kj : 0);
+  float k[QC], v[VC], adk[QC], adv[VC];
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    k[c] = live ? p.kr[krow * D + part * 16 + c] : 0.f;
-    v[c] = live ? p.v[krow * D + part * 16 + c] : 0.f;
+  for (int c = 0; c < QC; ++c) {
+    k[c] = live ? p.kr[krow * D + part * QC + c] : 0.f;
     adk[c] = 0.f;
+  }
+#pragma unroll
+  for (int c = 0; c < VC; ++c) {
+    v[c] = live ? p.v[krow * DV + part * VC + c] : 0.f;
     adv[c] = 0.f;
   }
-  const int q_begin = p.causal ? k0 : 0;
+  // causal: the first query row that sees key k0 sits at position k0
+  const int q_begin = p.causal ? max(0, k0 - p.q_off) : 0;
   for (int hh = 0; hh < rep; ++hh) {
     const int h = g * rep + hh;
-    const size_t qbase = (static_cast<size_t>(b) * p.Hq + h) * p.T;
-    for (int i0 = q_begin; i0 < p.T; i0 += C::KT) {
-      const int ni = min(C::KT, p.T - i0);
+    const size_t qbase = (static_cast<size_t>(b) * p.Hq + h) * p.Tq;
+    for (int i0 = q_begin; i0 < p.Tq; i0 += C::KT) {
+      const int ni = min(C::KT, p.Tq - i0);
       __syncthreads();
       for (int e = tid; e < C::KT * D; e += kThreads) {
         const int r = e / D;
         sq[e] = r < ni ? p.qr[(qbase + i0 + r) * D + e % D] : 0.f;
-        so[e] = r < ni ? p.dout[(qbase + i0 + r) * D + e % D] : 0.f;
+      }
+      for (int e = tid; e < C::KT * DV; e += kThreads) {
+        const int r = e / DV;
+        so[e] = r < ni ? p.dout[(qbase + i0 + r) * DV + e % DV] : 0.f;
       }
       for (int e = tid; e < C::KT; e += kThreads) {
         slse[e] = e < ni ? p.lse[qbase + i0 + e] * kLog2e : 0.f;
@@ -216,63 +242,70 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_f32_kernel(const BwdF32Para
       }
       __syncthreads();
       for (int i = 0; i < ni; ++i) {
-        float qq[16], oo[16];
-        load16(sq + i * D + part * 16, qq);
-        load16(so + i * D + part * 16, oo);
+        float qq[QC], oo[VC];
+        load_n<QC>(sq + i * D + part * QC, qq);
+        load_n<VC>(so + i * DV + part * VC, oo);
         float s = 0.f, dp = 0.f;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          s = fmaf(qq[c], k[c], s);
-          dp = fmaf(oo[c], v[c], dp);
-        }
+        for (int c = 0; c < QC; ++c) s = fmaf(qq[c], k[c], s);
+#pragma unroll
+        for (int c = 0; c < VC; ++c) dp = fmaf(oo[c], v[c], dp);
 #pragma unroll
         for (int off = 1; off < C::TPR; off <<= 1) {
           s += __shfl_xor_sync(0xffffffffu, s, off);
           dp += __shfl_xor_sync(0xffffffffu, dp, off);
         }
         const int qi = i0 + i;
-        if (!live || (p.causal && kj > qi)) continue;
+        if (!live || (p.causal && kj > p.q_off + qi)) continue;
         const float pr = exp2f(fmaf(s * p.scale, kLog2e, -slse[i]));
         const float ds = pr * (dp - sdd[i]) * p.scale;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          adv[c] = fmaf(pr, oo[c], adv[c]);
-          adk[c] = fmaf(ds, qq[c], adk[c]);
-        }
+        for (int c = 0; c < VC; ++c) adv[c] = fmaf(pr, oo[c], adv[c]);
+#pragma unroll
+        for (int c = 0; c < QC; ++c) adk[c] = fmaf(ds, qq[c], adk[c]);
       }
     }
   }
   __syncthreads();
 #pragma unroll
-  for (int c = 0; c < 16; ++c) srow[row * D + part * 16 + c] = adk[c];
+  for (int c = 0; c < QC; ++c) srow[row * D + part * QC + c] = adk[c];
   __syncwarp();
   if (p.rope) rotate_back_row(srow + row * D, D, C::TPR, part, p.rope, kj, p.theta);
   __syncwarp();
   if (live) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      p.dk[krow * D + part * 16 + c] = srow[row * D + part * 16 + c];
-      p.dv[krow * D + part * 16 + c] = adv[c];
-    }
+    for (int c = 0; c < QC; ++c) p.dk[krow * D + part * QC + c] = srow[row * D + part * QC + c];
+#pragma unroll
+    for (int c = 0; c < VC; ++c) p.dv[krow * DV + part * VC + c] = adv[c];
   }
 }
 
-template <int D>
+template <int D, int DV>
 cudaError_t launch_f32_d(const BwdF32Params& p, int B, cudaStream_t stream) {
-  using C = BwdF32Cfg<D>;
-  dim3 gq((p.T + C::ROWS - 1) / C::ROWS, p.Hq, B);
-  bwd_dq_f32_kernel<D><<<gq, kThreads, 0, stream>>>(p);
+  using C = BwdF32Cfg<D, DV>;
+  dim3 gq((p.Tq + C::ROWS - 1) / C::ROWS, p.Hq, B);
+  bwd_dq_f32_kernel<D, DV><<<gq, kThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 gk((p.T + C::ROWS - 1) / C::ROWS, p.Hkv, B);
-  bwd_dkdv_f32_kernel<D><<<gk, kThreads, 0, stream>>>(p);
+  dim3 gk((p.Tk + C::ROWS - 1) / C::ROWS, p.Hkv, B);
+  bwd_dkdv_f32_kernel<D, DV><<<gk, kThreads, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_f32_dv(const BwdF32Params& p, int B, int dv, cudaStream_t stream) {
+  switch (dv) {
+    case 16: return launch_f32_d<D, 16>(p, B, stream);
+    case 32: return launch_f32_d<D, 32>(p, B, stream);
+    case 64: return launch_f32_d<D, 64>(p, B, stream);
+    case 128: return launch_f32_d<D, 128>(p, B, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_f32(const BwdArgs& a, void* q_rot, void* k_rot, cudaStream_t stream) {
-  if (a.Tq != a.Tk || a.q_off != 0) return cudaErrorInvalidValue;
   const long long qrows = static_cast<long long>(a.B) * a.Hq * a.Tq;
   const long long krows = static_cast<long long>(a.B) * a.Hkv * a.Tk;
   cudaError_t e;
@@ -282,17 +315,17 @@ cudaError_t launch_bwd_f32(const BwdArgs& a, void* q_rot, void* k_rot, cudaStrea
   if (a.rope) {
     rope_f32_kernel<<<static_cast<unsigned>((qrows * (a.d / 2) + 255) / 256), 256, 0, stream>>>(
         static_cast<const float*>(a.qr), static_cast<float*>(q_rot), qrows, a.Tq, a.d, a.rope,
-        a.theta);
+        a.theta, a.q_off);
     rope_f32_kernel<<<static_cast<unsigned>((krows * (a.d / 2) + 255) / 256), 256, 0, stream>>>(
         static_cast<const float*>(a.kr), static_cast<float*>(k_rot), krows, a.Tk, a.d, a.rope,
-        a.theta);
+        a.theta, 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.qr = static_cast<const float*>(q_rot);
     p.kr = static_cast<const float*>(k_rot);
   }
   rowdot_f32_kernel<<<static_cast<unsigned>((qrows + 255) / 256), 256, 0, stream>>>(
-      static_cast<const float*>(a.dout), static_cast<const float*>(a.out), a.dvec, qrows, a.d);
+      static_cast<const float*>(a.dout), static_cast<const float*>(a.out), a.dvec, qrows, a.d_v);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   p.v = static_cast<const float*>(a.v);
@@ -304,16 +337,18 @@ cudaError_t launch_bwd_f32(const BwdArgs& a, void* q_rot, void* k_rot, cudaStrea
   p.dv = static_cast<float*>(a.dv);
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
-  p.T = a.Tq;
+  p.Tq = a.Tq;
+  p.Tk = a.Tk;
+  p.q_off = a.q_off;
   p.causal = a.causal;
   p.rope = a.rope;
   p.scale = a.scale;
   p.theta = a.theta;
   switch (a.d) {
-    case 16: return launch_f32_d<16>(p, a.B, stream);
-    case 32: return launch_f32_d<32>(p, a.B, stream);
-    case 64: return launch_f32_d<64>(p, a.B, stream);
-    case 128: return launch_f32_d<128>(p, a.B, stream);
+    case 16: return launch_f32_dv<16>(p, a.B, a.d_v, stream);
+    case 32: return launch_f32_dv<32>(p, a.B, a.d_v, stream);
+    case 64: return launch_f32_dv<64>(p, a.B, a.d_v, stream);
+    case 128: return launch_f32_dv<128>(p, a.B, a.d_v, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,14 +1,16 @@
-// dK and dV of the attention backward for head size 128 on tcgen05 (the math
-// and the split into a dK/dV kernel and a dQ kernel are described in bwd.cu).
+// dK and dV of the attention backward on tcgen05 (the math and the split into a
+// dK/dV kernel and a dQ kernel are described in bwd.cu).  Head sizes: d (q, k) and
+// dv (v, out) each 64 or 128; Tq query rows at positions q_off..q_off+Tq-1 and Tk
+// keys at 0..Tk-1 (query i sees key j iff j <= q_off + i when causal).
 //
 // One CTA per (128 keys, KV head, batch); it walks the query heads of the KV
 // group and, for each, the 128-row query tiles that see the keys.  Per tile:
 //
-//   S^T  = Kr Qr^T          M=128 keys, N=128 queries, K=128   (SS, TMEM cols [0,128))
-//   dP^T = V dO^T           same shapes                         (SS, cols [128,256))
+//   S^T  = Kr Qr^T          M=128 keys, N=128 queries, K=d      (SS, TMEM cols [0,128))
+//   dP^T = V dO^T           M=128 keys, N=128 queries, K=dv     (SS, cols [128,256))
 //   P^T  = exp(scale*S^T - lse)   dS^T = P^T o (dP^T - D)      (softmax warpgroups)
-//   dV  += P^T dO           M=128 keys, N=128 channels, K=128 queries (SS, cols [256,384))
-//   dK  += dS^T Qr          same                                      (TS, cols [384,512))
+//   dV  += P^T dO           M=128 keys, N=dv channels, K=128 queries (SS, cols [256,256+dv))
+//   dK  += dS^T Qr          M=128 keys, N=d channels               (TS, cols [384,384+d))
 //
 // P^T (bf16) goes to shared memory (K-major, 128-byte swizzle) and feeds dV as
 // the A operand, so the S^T columns are free as soon as the softmax warps have
@@ -40,27 +42,38 @@ constexpr uint64_t kDrainNs = 100000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, 0, 0);  // both K-major (S^T, dP^T, S, dP)
 
-// Head-size dependent sizes (d = 64 or 128): a Q / dO / K / V tile is d/64 column
-// blocks of 128 rows; dV, dK and dQ are N = d products with B read MN-major.
-template <int D>
+// Head-size dependent sizes (d = D, dv = DV, each 64 or 128): a Q or K tile is D/64
+// and a V or dO tile DV/64 column blocks of 128 rows; dK and dQ are N = D, dV an
+// N = DV product, with B read MN-major.
+template <int D, int DV>
 struct BwdCfg {
-  static_assert(D == 64 || D == 128, "head size 64 or 128");
-  static constexpr int TILE = BQ * D * 2;
-  static constexpr int SMEM_DATA = 2 * TILE + NSQ * 2 * TILE + PTILE + NSQ * VEC;
+  static_assert((D == 64 || D == 128) && (DV == 64 || DV == 128), "head sizes 64 or 128");
+  static constexpr int TILE_QK = BQ * D * 2;   // a Q or K tile
+  static constexpr int TILE_VO = BQ * DV * 2;  // a V or dO tile
+  static constexpr int SMEM_DATA = (1 + NSQ) * (TILE_QK + TILE_VO) + PTILE + NSQ * VEC;
   static constexpr int SMEM_BYTES = SMEM_DATA + 256;
-  static constexpr uint32_t IDESC_N = idesc_bf16_f32(128, D, 0, 1);  // A K-major, B MN-major
+  static constexpr uint32_t IDESC_DK = idesc_bf16_f32(128, D, 0, 1);   // A K-major, B MN-major
+  static constexpr uint32_t IDESC_DV = idesc_bf16_f32(128, DV, 0, 1);
 };
 
 struct KvParams {
-  const float* lse;   // [B, Hq, T], natural log
-  const float* dvec;  // [B, Hq, T]
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  const float* lse;   // [B, Hq, Tq], natural log
+  const float* dvec;  // [B, Hq, Tq]
+  __nv_bfloat16* dk;  // [B, Hkv, Tk, D]
+  __nv_bfloat16* dv;  // [B, Hkv, Tk, DV]
   uint32_t* status;
-  int Hq, Hkv, T, causal, rope;
+  int Hq, Hkv, Tq, Tk, q_off, causal, rope;
   float scale, sl2;
   RopeTable theta;
 };
+
+// First 128-row query tile holding a query that sees key k0 (causal: the tile's last
+// row sits at or after k0).
+__device__ __forceinline__ int first_query_tile(int k0, int q_off, int causal) {
+  if (!causal) return 0;
+  const int num = k0 - q_off - (BQ - 1);
+  return num > 0 ? (num + BQ - 1) / BQ : 0;
+}
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
@@ -73,21 +86,21 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
   return static_cast<uint32_t>(kk < 4 ? 8 * kk : 64 + 8 * (kk - 4));
 }
 
-template <int D>
+template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_tc_kernel(const __grid_constant__ KvParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_do) {
-  using C = BwdCfg<D>;
-  constexpr int TILE = C::TILE;
+  using C = BwdCfg<D, DV>;
+  constexpr int TQK = C::TILE_QK, TVO = C::TILE_VO;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sK = smem;
-  uint8_t* sV = smem + TILE;
-  uint8_t* sQ = smem + 2 * TILE;                 // [NSQ] tiles
-  uint8_t* sO = smem + (2 + NSQ) * TILE;         // [NSQ] dO tiles
-  uint8_t* sP = smem + (2 + 2 * NSQ) * TILE;     // P^T: rows = keys, queries contiguous
-  float* sVec = reinterpret_cast<float*>(smem + (2 + 2 * NSQ) * TILE + PTILE);  // [NSQ][lse | D]
+  uint8_t* sV = smem + TQK;
+  uint8_t* sQ = sV + TVO;                        // [NSQ] Qr tiles
+  uint8_t* sO = sQ + NSQ * TQK;                  // [NSQ] dO tiles
+  uint8_t* sP = sO + NSQ * TVO;                  // P^T: rows = keys, queries contiguous
+  float* sVec = reinterpret_cast<float*>(sP + PTILE);  // [NSQ][lse | D]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_DATA);
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;   // [NSQ]: Qr and dO tiles (TMA bytes)
@@ -114,9 +127,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kt = blockIdx.z;
   const int k0 = kt * BK, g = blockIdx.x, b = blockIdx.y;
   const int rep = p.Hq / p.Hkv;
-  const int n_qt = (p.T + BQ - 1) / BQ;
-  const int i_begin = p.causal ? kt : 0;  // query tiles that see these keys
-  const int per_head = n_qt - i_begin;
+  const int n_qt = (p.Tq + BQ - 1) / BQ;
+  const int i_begin = first_query_tile(k0, p.q_off, p.causal);  // query tiles that see these keys
+  const int per_head = n_qt > i_begin ? n_qt - i_begin : 0;
   const int n_it = rep * per_head;
 
   if (threadIdx.x == 0) {
@@ -148,12 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * TILE);
+      mbar_arrive_expect_tx(kv_full, TQK + TVO);
       const int zk = b * p.Hkv + g;
-      for (int kb = 0; kb < D / 64; ++kb) {
-        tma_load_3d(sK + kb * BLOCK, &tm_k, kv_full, kb * 64, k0, zk);
-        tma_load_3d(sV + kb * BLOCK, &tm_v, kv_full, kb * 64, k0, zk);
-      }
+      for (int kb = 0; kb < D / 64; ++kb) tma_load_3d(sK + kb * BLOCK, &tm_k, kv_full, kb * 64, k0, zk);
+      for (int kb = 0; kb < DV / 64; ++kb) tma_load_3d(sV + kb * BLOCK, &tm_v, kv_full, kb * 64, k0, zk);
     }
     int issued = 0;
     for (int it = 0; it < n_it; ++it) {
@@ -163,18 +174,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = (i_begin + it % per_head) * BQ;
       const int zq = b * p.Hq + h;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&q_full[st], 2 * TILE);
-        for (int kb = 0; kb < D / 64; ++kb) {
-          tma_load_3d(sQ + st * TILE + kb * BLOCK, &tm_q, &q_full[st], kb * 64, q0, zq);
-          tma_load_3d(sO + st * TILE + kb * BLOCK, &tm_do, &q_full[st], kb * 64, q0, zq);
-        }
+        mbar_arrive_expect_tx(&q_full[st], TQK + TVO);
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_3d(sQ + st * TQK + kb * BLOCK, &tm_q, &q_full[st], kb * 64, q0, zq);
+        for (int kb = 0; kb < DV / 64; ++kb)
+          tma_load_3d(sO + st * TVO + kb * BLOCK, &tm_do, &q_full[st], kb * 64, q0, zq);
       }
       float* vec = sVec + st * 2 * BQ;
-      const size_t rb = static_cast<size_t>(zq) * p.T;
+      const size_t rb = static_cast<size_t>(zq) * p.Tq;
       for (int e = lane; e < BQ; e += 32) {
         const int q = q0 + e;
-        vec[e] = q < p.T ? p.lse[rb + q] * kLog2e : 0.f;
-        vec[BQ + e] = q < p.T ? p.dvec[rb + q] : 0.f;
+        vec[e] = q < p.Tq ? p.lse[rb + q] * kLog2e : 0.f;
+        vec[BQ + e] = q < p.Tq ? p.dvec[rb + q] : 0.f;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&vec_full[st]);
@@ -198,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       const uint32_t k_s = smem_u32(sK), v_s = smem_u32(sV);
       wait(kv_full, 0);  // also when there is nothing to do: the loads must land first
-      auto q_tile = [&](int it) { return smem_u32(sQ + (it % NSQ) * TILE); };
-      auto o_tile = [&](int it) { return smem_u32(sO + (it % NSQ) * TILE); };
+      auto q_tile = [&](int it) { return smem_u32(sQ + (it % NSQ) * TQK); };
+      auto o_tile = [&](int it) { return smem_u32(sO + (it % NSQ) * TVO); };
       auto issue_st = [&](int it) {  // S^T = Kr Qr^T
         const uint32_t q_s = q_tile(it);
 #pragma unroll
@@ -213,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_dpt = [&](int it) {  // dP^T = V dO^T
         const uint32_t o_s = o_tile(it);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
           umma_ss(tmem + 128u, smem_desc_sw128(v_s + off, 16, 1024),
                   smem_desc_sw128(o_s + off, 16, 1024), IDESC_SS, kk > 0 ? 1u : 0u);
@@ -242,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
           umma_ss(tmem + 256u, smem_desc_sw128(p_s + off, 16, 1024),
-                  smem_desc_sw128(o_s + 2048u * kk, BLOCK, 1024), C::IDESC_N,
+                  smem_desc_sw128(o_s + 2048u * kk, BLOCK, 1024), C::IDESC_DV,
                   (it > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(dv_done);
@@ -251,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
           umma_ts(tmem + 384u, tmem + 128u + packed_col(kk),
-                  smem_desc_sw128(q_s + 2048u * kk, BLOCK, 1024), C::IDESC_N,
+                  smem_desc_sw128(q_s + 2048u * kk, BLOCK, 1024), C::IDESC_DK,
                   (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&q_empty[it % NSQ]);
         if (next) issue_dpt(it + 1);
@@ -297,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(s_free);
         // every (key, query) of this warpgroup's half tile is visible: no per-element test
         const bool all_vis =
-            q0 + 63 < p.T && k0 + BK <= p.T && (!p.causal || q0 >= k0 + BK - 1);
+            q0 + 63 < p.Tq && k0 + BK <= p.Tk && (!p.causal || p.q_off + q0 >= k0 + BK - 1);
         if (all_vis) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
@@ -306,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const int q = q0 + c;
-            const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
+            const bool vis = q < p.Tq && key < p.Tk && (!p.causal || key <= p.q_off + q);
             pt[c] = vis ? ex2_approx(fmaf(__uint_as_float(r[c]), p.sl2, -lse2[c])) : 0.f;
           }
         }
@@ -350,22 +361,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     }
-    // epilogue: warps 0-3 write dV, warps 4-7 dK = R^T (scale dK); channels in 32-column
-    // chunks 32c and d/2 + 32c so that split-half RoPE pairs (i, i + d/2) meet
+    // epilogue: warps 0-3 write dV (W = DV channels), warps 4-7 dK = R^T (scale dK)
+    // (W = D); channels in 32-column chunks 32c and W/2 + 32c so that split-half RoPE
+    // pairs (i, i + d/2) meet
     if (ok && (n_it == 0 || warp_wait(acc_full, 0, abort_flag, p.status))) {
       tc_fence_after();
+      const int W = x ? D : DV;
       const uint32_t tacc = tmem + lane_off + (x ? 384u : 256u);
-      __nv_bfloat16* dst =
-          (x ? p.dk : p.dv) + (static_cast<size_t>(b * p.Hkv + g) * p.T + (key < p.T ? key : 0)) * D;
+      __nv_bfloat16* dst = (x ? p.dk : p.dv) +
+                           (static_cast<size_t>(b * p.Hkv + g) * p.Tk + (key < p.Tk ? key : 0)) * W;
 #pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {
+      for (int c = 0; c < W / 64; ++c) {
         float a0[32], a1[32];
         {
           uint32_t r[32];
           tmem_ld32_sync(tacc + 32u * c, r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) a0[e] = n_it > 0 ? __uint_as_float(r[e]) : 0.f;
-          tmem_ld32_sync(tacc + static_cast<uint32_t>(D / 2) + 32u * c, r);
+          tmem_ld32_sync(tacc + static_cast<uint32_t>(W / 2) + 32u * c, r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) a1[e] = n_it > 0 ? __uint_as_float(r[e]) : 0.f;
         }
@@ -401,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (key < p.T) {
+        if (key < p.Tk) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
             reinterpret_cast<uint4*>(dst + 32 * c)[v4] =
@@ -409,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            pack_bf16x2(a0[8 * v4 + 2], a0[8 * v4 + 3]),
                            pack_bf16x2(a0[8 * v4 + 4], a0[8 * v4 + 5]),
                            pack_bf16x2(a0[8 * v4 + 6], a0[8 * v4 + 7]));
-            reinterpret_cast<uint4*>(dst + D / 2 + 32 * c)[v4] =
+            reinterpret_cast<uint4*>(dst + W / 2 + 32 * c)[v4] =
                 make_uint4(pack_bf16x2(a1[8 * v4], a1[8 * v4 + 1]),
                            pack_bf16x2(a1[8 * v4 + 2], a1[8 * v4 + 3]),
                            pack_bf16x2(a1[8 * v4 + 4], a1[8 * v4 + 5]),
@@ -429,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dQ for d = 128, persistent: one CTA per SM walks work items (128 queries of one
+// dQ, persistent: one CTA per SM walks work items (128 queries of one
 // query head), longest first (causally the last query tiles), in rounds of
 // gridDim.x items with alternating direction.  Per item, per key tile j:
 //   S  = Qr Kr_j^T, dP = dO V_j^T   (SS, TMEM columns [0,128) and [128,256))
@@ -449,11 +462,11 @@ constexpr int kRegsCtlQ = 96;
 constexpr int kRegsEpiQ = 112;
 
 struct QParams {
-  const float* lse;
-  const float* dvec;
-  __nv_bfloat16* dq;
+  const float* lse;   // [B, Hq, Tq]
+  const float* dvec;  // [B, Hq, Tq]
+  __nv_bfloat16* dq;  // [B, Hq, Tq, D]
   uint32_t* status;
-  int B, Hq, Hkv, T, causal, rope, n_items;
+  int B, Hq, Hkv, Tq, Tk, q_off, causal, rope, n_items;
   float scale, sl2;
   RopeTable theta;
 };
@@ -469,15 +482,17 @@ __device__ __forceinline__ int q_item_index(int i) {
 }
 
 __device__ __forceinline__ QItem q_item(const QParams& p, int u) {
-  const int n_qtiles = (p.T + BQ - 1) / BQ;
-  const int n_kt = (p.T + BK - 1) / BK;
+  const int n_qtiles = (p.Tq + BQ - 1) / BQ;
+  const int n_kt = (p.Tk + BK - 1) / BK;
   const int per = p.B * p.Hq;
   const int r = u / per, rem = u - r * per;
   QItem it;
   it.qt = p.causal ? n_qtiles - 1 - r : r;
   it.b = rem / p.Hq;
   it.h = rem - it.b * p.Hq;
-  it.n_it = p.causal ? min(n_kt, it.qt + 1) : n_kt;
+  // causal: key tiles up to the one holding the position of the tile's last row
+  const int last = p.q_off + min(it.qt * BQ + BQ, p.Tq) - 1;
+  it.n_it = p.causal ? min(n_kt, last / BK + 1) : n_kt;
   return it;
 }
 
@@ -490,18 +505,19 @@ __device__ __forceinline__ void q_regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int D>
+template <int D, int DV>
 __global__ void __launch_bounds__(kThreadsQ, 1)
     bwd_q_tc_kernel(const __grid_constant__ QParams p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do) {
-  constexpr int TILE = BwdCfg<D>::TILE;
-  constexpr int Q_SMEM_DATA = 2 * TILE + NSKV * 2 * TILE;
+  using C = BwdCfg<D, DV>;
+  constexpr int TQK = C::TILE_QK, TVO = C::TILE_VO, STAGE = TQK + TVO;
+  constexpr int Q_SMEM_DATA = (1 + NSKV) * STAGE;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sQ = smem;
-  uint8_t* sO = smem + TILE;
-  uint8_t* sKV = smem + 2 * TILE;  // [NSKV] x (K tile, V tile)
+  uint8_t* sO = smem + TQK;
+  uint8_t* sKV = smem + STAGE;  // [NSKV] x (K tile, V tile)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Q_SMEM_DATA);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;   // the item's last S and dP completed
@@ -563,11 +579,11 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         const QItem it = q_item(p, u);
         const int zq = it.b * p.Hq + it.h, zk = it.b * p.Hkv + it.h / (p.Hq / p.Hkv);
         if (i > 0 && !mbar_wait(q_empty, (i - 1) & 1, abort_flag, p.status, kWaitNs)) break;
-        mbar_arrive_expect_tx(q_full, 2 * TILE);
-        for (int kb = 0; kb < D / 64; ++kb) {
+        mbar_arrive_expect_tx(q_full, STAGE);
+        for (int kb = 0; kb < D / 64; ++kb)
           tma_load_3d(sQ + kb * BLOCK, &tm_q, q_full, kb * 64, it.qt * BQ, zq);
+        for (int kb = 0; kb < DV / 64; ++kb)
           tma_load_3d(sO + kb * BLOCK, &tm_do, q_full, kb * 64, it.qt * BQ, zq);
-        }
         ++items;
         for (int j = 0; j < it.n_it; ++j, ++g) {
           const int st = g % NSKV, use = g / NSKV;
@@ -575,12 +591,12 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             ok = false;
             break;
           }
-          uint8_t* dst = sKV + st * 2 * TILE;
-          mbar_arrive_expect_tx(&kv_full[st], 2 * TILE);
-          for (int kb = 0; kb < D / 64; ++kb) {
+          uint8_t* dst = sKV + st * STAGE;
+          mbar_arrive_expect_tx(&kv_full[st], STAGE);
+          for (int kb = 0; kb < D / 64; ++kb)
             tma_load_3d(dst + kb * BLOCK, &tm_k, &kv_full[st], kb * 64, j * BK, zk);
-            tma_load_3d(dst + TILE + kb * BLOCK, &tm_v, &kv_full[st], kb * 64, j * BK, zk);
-          }
+          for (int kb = 0; kb < DV / 64; ++kb)
+            tma_load_3d(dst + TQK + kb * BLOCK, &tm_v, &kv_full[st], kb * 64, j * BK, zk);
           ++issued;
         }
       }
@@ -601,7 +617,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         return ok;
       };
       const uint32_t q_s = smem_u32(sQ), o_s = smem_u32(sO);
-      auto k_tile = [&](int g) { return smem_u32(sKV + (g % NSKV) * 2 * TILE); };
+      auto k_tile = [&](int g) { return smem_u32(sKV + (g % NSKV) * STAGE); };
       auto issue_s = [&](int g) {  // S = Qr Kr^T
         const uint32_t k_s = k_tile(g);
 #pragma unroll
@@ -613,9 +629,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         tc_commit(s_full);
       };
       auto issue_dp = [&](int g) {  // dP = dO V^T
-        const uint32_t v_s = k_tile(g) + TILE;
+        const uint32_t v_s = k_tile(g) + TQK;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
           umma_ss(tmem + 128u, smem_desc_sw128(o_s + off, 16, 1024),
                   smem_desc_sw128(v_s + off, 16, 1024), IDESC_SS, kk > 0 ? 1u : 0u);
@@ -652,7 +668,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             umma_ts(t_acc, tmem + 128u + packed_col(kk), smem_desc_sw128(k_s + 2048u * kk, BLOCK, 1024),
-                    BwdCfg<D>::IDESC_N, (j > 0 || kk > 0) ? 1u : 0u);
+                    C::IDESC_DK, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&kv_empty[g % NSKV]);
           if (next) {
             issue_dp(g + 1);
@@ -681,9 +697,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       if (u >= p.n_items) break;
       const QItem it = q_item(p, u);
       const int q0 = it.qt * BQ, q = q0 + row;
-      const size_t rb = static_cast<size_t>(it.b * p.Hq + it.h) * p.T;
-      const float lse2 = q < p.T ? p.lse[rb + q] * kLog2e : 0.f;
-      const float dq_d = q < p.T ? p.dvec[rb + q] : 0.f;
+      const size_t rb = static_cast<size_t>(it.b * p.Hq + it.h) * p.Tq;
+      const float lse2 = q < p.Tq ? p.lse[rb + q] * kLog2e : 0.f;
+      const float dq_d = q < p.Tq ? p.dvec[rb + q] : 0.f;
       for (int j = 0; j < it.n_it; ++j, ++g) {
         if (!warp_wait(s_full, g & 1, abort_flag, p.status)) {
           ok = false;
@@ -701,7 +717,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         float pr[64];
         // every (query, key) of this warpgroup's half tile is visible: no per-element test
         const bool all_vis =
-            kb0 + 63 < p.T && q0 + BQ <= p.T && (!p.causal || kb0 + 63 <= q0);
+            kb0 + 63 < p.Tk && q0 + BQ <= p.Tq && (!p.causal || kb0 + 63 <= p.q_off + q0);
         if (all_vis) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) pr[c] = ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2));
@@ -709,7 +725,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const int key = kb0 + c;
-            const bool vis = q < p.T && key < p.T && (!p.causal || key <= q);
+            const bool vis = q < p.Tq && key < p.Tk && (!p.causal || key <= p.q_off + q);
             pr[c] = vis ? ex2_approx(fmaf(__uint_as_float(rs[c]), p.sl2, -lse2)) : 0.f;
           }
         }
@@ -750,10 +766,11 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       const QItem it = q_item(p, u);
       const int ab = i & 1;
       const int q = it.qt * BQ + row;
+      const int qpos = p.q_off + q;  // RoPE position of the row
       if (!warp_wait(&acc_full[ab], (i >> 1) & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t t_acc = tmem + lane_off + 256u + 128u * static_cast<uint32_t>(ab);
-      __nv_bfloat16* dst = p.dq + (static_cast<size_t>(it.b * p.Hq + it.h) * p.T + q) * D;
+      __nv_bfloat16* dst = p.dq + (static_cast<size_t>(it.b * p.Hq + it.h) * p.Tq + q) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         float a0[32], a1[32];
@@ -770,7 +787,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             float cs, sn;
-            rope_cos_sin<false>(q, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
+            rope_cos_sin<false>(qpos, p.theta.hi[32 * c + e], p.theta.lo[32 * c + e], cs, sn);
             const float u0 = a0[e], w = a1[e];
             a0[e] = fmaf(u0, cs, w * sn);
             a1[e] = fmaf(-u0, sn, w * cs);
@@ -779,19 +796,19 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
             float cs, sn;
-            rope_cos_sin<false>(q, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
+            rope_cos_sin<false>(qpos, p.theta.hi[16 * c + t], p.theta.lo[16 * c + t], cs, sn);
             float u0 = a0[2 * t], w = a0[2 * t + 1];
             a0[2 * t] = fmaf(u0, cs, w * sn);
             a0[2 * t + 1] = fmaf(-u0, sn, w * cs);
-            rope_cos_sin<false>(q, p.theta.hi[D / 4 + 16 * c + t], p.theta.lo[D / 4 + 16 * c + t],
-                                cs, sn);
+            rope_cos_sin<false>(qpos, p.theta.hi[D / 4 + 16 * c + t],
+                                p.theta.lo[D / 4 + 16 * c + t], cs, sn);
             u0 = a1[2 * t];
             w = a1[2 * t + 1];
             a1[2 * t] = fmaf(u0, cs, w * sn);
             a1[2 * t + 1] = fmaf(-u0, sn, w * cs);
           }
         }
-        if (q < p.T) {
+        if (q < p.Tq) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
             reinterpret_cast<uint4*>(dst + 32 * c)[v4] =
@@ -824,9 +841,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 
 }  // namespace
 
-template <int D>
+template <int D, int DV>
 cudaError_t launch_kv_d(const BwdArgs& a, cudaStream_t stream) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, DV>;
   KvParams p{};
   p.lse = a.lse;
   p.dvec = a.dvec;
@@ -835,7 +852,9 @@ cudaError_t launch_kv_d(const BwdArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
-  p.T = a.Tq;
+  p.Tq = a.Tq;
+  p.Tk = a.Tk;
+  p.q_off = a.q_off;
   p.causal = a.causal;
   p.rope = a.rope;
   p.scale = a.scale;
@@ -844,20 +863,22 @@ cudaError_t launch_kv_d(const BwdArgs& a, cudaStream_t stream) {
   alignas(64) CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_bf16_3d(&tq, a.qr, D, a.Tq, a.B * a.Hq, BQ) ||
       !make_tmap_bf16_3d(&tk, a.kr, D, a.Tk, a.B * a.Hkv, BK) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BK) ||
-      !make_tmap_bf16_3d(&tdo, a.dout, D, a.Tq, a.B * a.Hq, BQ))
+      !make_tmap_bf16_3d(&tv, a.v, DV, a.Tk, a.B * a.Hkv, BK) ||
+      !make_tmap_bf16_3d(&tdo, a.dout, DV, a.Tq, a.B * a.Hq, BQ))
     return cudaErrorInvalidValue;
   static SmemLimitOnce smem_limit;
-  cudaError_t e = smem_limit.set(bwd_kv_tc_kernel<D>, C::SMEM_BYTES);
+  cudaError_t e = smem_limit.set(bwd_kv_tc_kernel<D, DV>, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(a.Hkv, a.B, (a.Tk + BK - 1) / BK);
-  bwd_kv_tc_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
+  bwd_kv_tc_kernel<D, DV><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tq, tk, tv, tdo);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return launch_kv_d<64>(a, stream);
-  if (a.d == 128) return launch_kv_d<128>(a, stream);
+  if (a.d == 64 && a.d_v == 64) return launch_kv_d<64, 64>(a, stream);
+  if (a.d == 64 && a.d_v == 128) return launch_kv_d<64, 128>(a, stream);
+  if (a.d == 128 && a.d_v == 64) return launch_kv_d<128, 64>(a, stream);
+  if (a.d == 128 && a.d_v == 128) return launch_kv_d<128, 128>(a, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -865,9 +886,9 @@ cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream) {
 
 namespace csattn {
 
-template <int D>
+template <int D, int DV>
 cudaError_t launch_q_d(const BwdArgs& a, cudaStream_t stream) {
-  constexpr int smem_bytes = (2 + 2 * NSKV) * BwdCfg<D>::TILE + 256;
+  constexpr int smem_bytes = (1 + NSKV) * (BwdCfg<D, DV>::TILE_QK + BwdCfg<D, DV>::TILE_VO) + 256;
   QParams p{};
   p.lse = a.lse;
   p.dvec = a.dvec;
@@ -876,7 +897,9 @@ cudaError_t launch_q_d(const BwdArgs& a, cudaStream_t stream) {
   p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
-  p.T = a.Tq;
+  p.Tq = a.Tq;
+  p.Tk = a.Tk;
+  p.q_off = a.q_off;
   p.causal = a.causal;
   p.rope = a.rope;
   p.n_items = a.B * a.Hq * ((a.Tq + BQ - 1) / BQ);
@@ -886,21 +909,23 @@ cudaError_t launch_q_d(const BwdArgs& a, cudaStream_t stream) {
   alignas(64) CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_bf16_3d(&tq, a.qr, D, a.Tq, a.B * a.Hq, BQ) ||
       !make_tmap_bf16_3d(&tk, a.kr, D, a.Tk, a.B * a.Hkv, BK) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, a.B * a.Hkv, BK) ||
-      !make_tmap_bf16_3d(&tdo, a.dout, D, a.Tq, a.B * a.Hq, BQ))
+      !make_tmap_bf16_3d(&tv, a.v, DV, a.Tk, a.B * a.Hkv, BK) ||
+      !make_tmap_bf16_3d(&tdo, a.dout, DV, a.Tq, a.B * a.Hq, BQ))
     return cudaErrorInvalidValue;
   static SmemLimitOnce smem_limit;
-  cudaError_t e = smem_limit.set(bwd_q_tc_kernel<D>, smem_bytes);
+  cudaError_t e = smem_limit.set(bwd_q_tc_kernel<D, DV>, smem_bytes);
   if (e != cudaSuccess) return e;
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
   const int grid = p.n_items < sms ? p.n_items : sms;
-  bwd_q_tc_kernel<D><<<grid, kThreadsQ, smem_bytes, stream>>>(p, tq, tk, tv, tdo);
+  bwd_q_tc_kernel<D, DV><<<grid, kThreadsQ, smem_bytes, stream>>>(p, tq, tk, tv, tdo);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return launch_q_d<64>(a, stream);
-  if (a.d == 128) return launch_q_d<128>(a, stream);
+  if (a.d == 64 && a.d_v == 64) return launch_q_d<64, 64>(a, stream);
+  if (a.d == 64 && a.d_v == 128) return launch_q_d<64, 128>(a, stream);
+  if (a.d == 128 && a.d_v == 64) return launch_q_d<128, 64>(a, stream);
+  if (a.d == 128 && a.d_v == 128) return launch_q_d<128, 128>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -293,59 +293,81 @@ int csattn_attn_fwd_ext(const void* q, const void* k, const void* v, void* out, 
 
 size_t csattn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int d, int dtype,
                                  float rope_base) {
-  if ((dtype != CSATTN_BF16 && dtype != CSATTN_F32) || B < 1 || Hq < 1 || Hkv < 1 || T < 1 ||
-      d < 1)
+  return csattn_bwd_ext_workspace_size(B, Hq, Hkv, T, T, d, dtype, rope_base);
+}
+
+size_t csattn_bwd_ext_workspace_size(int B, int Hq, int Hkv, int Tq, int Tk, int d, int dtype,
+                                     float rope_base) {
+  if ((dtype != CSATTN_BF16 && dtype != CSATTN_F32) || B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 ||
+      Tk < 1 || d < 1)
     return 0;
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  const size_t rows = static_cast<size_t>(B) * Hq * T;
+  const size_t rows = static_cast<size_t>(B) * Hq * Tq;
   const size_t esz = dtype == CSATTN_F32 ? 4 : 2;
   size_t bytes = al(rows * 4);  // rowsum(dout o out), fp32
   if (rope_base > 0.f)          // rotated q and k
-    bytes += al(rows * d * esz) + al(static_cast<size_t>(B) * Hkv * T * d * esz);
+    bytes += al(rows * d * esz) + al(static_cast<size_t>(B) * Hkv * Tk * d * esz);
   return bytes;
 }
 
-int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out,
-                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
-                    int Hq, int Hkv, int T, int d, int dtype, int causal, float rope_base,
-                    int rope_layout, float scale, void* workspace, size_t workspace_bytes,
-                    void* stream) {
-  const char* fn = "attn_bwd";
+}  // extern "C"
+
+namespace {
+
+// Shared by csattn_attn_bwd (Tq = Tk = T, q_offset = 0, dv = d) and csattn_attn_bwd_ext.
+int attn_bwd_impl(const char* fn, const void* q, const void* k, const void* v, const void* out,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int Hq,
+                  int Hkv, int Tq, int Tk, int q_offset, int d, int d_v, int dtype, int causal,
+                  float rope_base, int rope_layout, float scale, void* workspace,
+                  size_t workspace_bytes, void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || dout == nullptr ||
       lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: null pointer argument", fn);
-  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1)
-    return fail(CSATTN_ERR_INVALID_ARG, "%s: B=%d Hq=%d Hkv=%d T=%d must be >= 1", fn, B, Hq,
-                Hkv, T);
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1)
+    return fail(CSATTN_ERR_INVALID_ARG, "%s: B=%d Hq=%d Hkv=%d Tq=%d Tk=%d must be >= 1", fn, B,
+                Hq, Hkv, Tq, Tk);
+  if (q_offset < 0) return fail(CSATTN_ERR_INVALID_ARG, "%s: q_offset=%d < 0", fn, q_offset);
   if (Hq % Hkv != 0)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: Hq=%d is not a multiple of Hkv=%d", fn, Hq, Hkv);
   if (dtype != CSATTN_BF16 && dtype != CSATTN_F32)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, dtype);
-  if (dtype == CSATTN_BF16 && d != 64 && d != 128)
-    return fail(CSATTN_ERR_UNSUPPORTED, "%s: bf16 d=%d not in {64,128}", fn, d);
-  if (dtype == CSATTN_F32 && d != 16 && d != 32 && d != 64 && d != 128)
-    return fail(CSATTN_ERR_UNSUPPORTED, "%s: fp32 d=%d not in {16,32,64,128}", fn, d);
   if (causal != 0 && causal != 1)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
+  if ((rope_layout & CSATTN_ROPE_K_PREROTATED) != 0)
+    return fail(CSATTN_ERR_UNSUPPORTED,
+                "%s: the backward takes k unrotated (CSATTN_ROPE_K_PREROTATED is not accepted)",
+                fn);
   if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: unknown rope_layout %d", fn, rope_layout);
   if (!std::isfinite(rope_base) || !std::isfinite(scale))
     return fail(CSATTN_ERR_INVALID_ARG, "%s: rope_base and scale must be finite", fn);
-  if (T >= (1 << 24)) return fail(CSATTN_ERR_UNSUPPORTED, "%s: T=%d >= 2^24", fn, T);
-  if (rope_base > 0.f && T > kMaxRopePositions)
-    return fail(CSATTN_ERR_UNSUPPORTED, "%s: RoPE supports T <= %d, got %d", fn,
-                kMaxRopePositions, T);
+  auto width_ok = [&](int w) {
+    return dtype == CSATTN_BF16 ? (w == 64 || w == 128) : (w == 16 || w == 32 || w == 64 || w == 128);
+  };
+  if (!width_ok(d) || !width_ok(d_v))
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: %s d=%d, dv=%d not in %s", fn,
+                dtype == CSATTN_BF16 ? "bf16" : "fp32", d, d_v,
+                dtype == CSATTN_BF16 ? "{64,128}" : "{16,32,64,128}");
+  if (Tq >= (1 << 24) || Tk >= (1 << 24) || q_offset >= (1 << 24))
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: Tq=%d, Tk=%d and q_offset=%d must be < 2^24", fn, Tq,
+                Tk, q_offset);
+  if (rope_base > 0.f && (q_offset + Tq > kMaxRopePositions || Tk > kMaxRopePositions))
+    return fail(CSATTN_ERR_UNSUPPORTED,
+                "%s: RoPE supports positions < %d (q_offset + Tq = %d, Tk = %d)", fn,
+                kMaxRopePositions, q_offset + Tq, Tk);
+  if (static_cast<long long>(B) * Hq > (1LL << 31) - 1)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: B*Hq too large", fn);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
-  const size_t need = csattn_bwd_workspace_size(B, Hq, Hkv, T, d, dtype, rope_base);
+  const size_t need = csattn_bwd_ext_workspace_size(B, Hq, Hkv, Tq, Tk, d, dtype, rope_base);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
     return fail(CSATTN_ERR_WORKSPACE,
                 "%s: needs a 16-byte aligned workspace of %zu bytes (got %zu)", fn, need,
                 workspace_bytes);
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  const size_t rows = static_cast<size_t>(B) * Hq * T;
+  const size_t rows = static_cast<size_t>(B) * Hq * Tq;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
   BwdArgs a{};
@@ -360,10 +382,11 @@ int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
-  a.Tq = T;
-  a.Tk = T;
-  a.q_off = 0;
+  a.Tq = Tq;
+  a.Tk = Tk;
+  a.q_off = q_offset;
   a.d = d;
+  a.d_v = d_v;
   a.causal = causal;
   a.rope = rope_base > 0.f ? (rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2) : 0;
   a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
@@ -377,27 +400,55 @@ int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   a.qr = q;
   a.kr = k;
+  char what[64];
   if (dtype == CSATTN_F32) {
     void* qr = ws + al(rows * 4);
     void* kr = static_cast<uint8_t*>(qr) + al(rows * d * 4);
     cudaError_t e = launch_bwd_f32(a, qr, kr, st);
-    if (e != cudaSuccess) return fail_cuda(e, "attn_bwd: fp32 kernel launch");
+    std::snprintf(what, sizeof(what), "%s: fp32 kernel launch", fn);
+    if (e != cudaSuccess) return fail_cuda(e, what);
     return CSATTN_OK;
   }
-  if (d == 128 && tensor_map_encoder() == nullptr)
+  if (tensor_map_encoder() == nullptr)
     return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
   if (a.rope) {
     void* qr = ws + al(rows * 4);
     void* kr = static_cast<uint8_t*>(qr) + al(rows * d * 2);
-    cudaError_t e = launch_rope_rotate_bf16(q, qr, B, Hq, T, d, a.rope, a.theta, st);
-    if (e == cudaSuccess) e = launch_rope_rotate_bf16(k, kr, B, Hkv, T, d, a.rope, a.theta, st);
-    if (e != cudaSuccess) return fail_cuda(e, "attn_bwd: RoPE kernel launch");
+    cudaError_t e = launch_rope_rotate_bf16(q, qr, B, Hq, Tq, d, a.rope, a.theta, st, q_offset);
+    if (e == cudaSuccess) e = launch_rope_rotate_bf16(k, kr, B, Hkv, Tk, d, a.rope, a.theta, st);
+    std::snprintf(what, sizeof(what), "%s: RoPE kernel launch", fn);
+    if (e != cudaSuccess) return fail_cuda(e, what);
     a.qr = qr;
     a.kr = kr;
   }
   cudaError_t e = launch_bwd_bf16(a, st);
-  if (e != cudaSuccess) return fail_cuda(e, "attn_bwd: kernel launch");
+  std::snprintf(what, sizeof(what), "%s: kernel launch", fn);
+  if (e != cudaSuccess) return fail_cuda(e, what);
   return CSATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int csattn_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                    int Hq, int Hkv, int T, int d, int dtype, int causal, float rope_base,
+                    int rope_layout, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  return attn_bwd_impl("attn_bwd", q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, T, T, 0, d, d,
+                       dtype, causal, rope_base, rope_layout, scale, workspace, workspace_bytes,
+                       stream);
+}
+
+int csattn_attn_bwd_ext(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int Hq, int Hkv, int Tq, int Tk, int q_offset, int d, int d_v, int dtype,
+                        int causal, float rope_base, int rope_layout, float scale,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_impl("attn_bwd_ext", q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Tq, Tk,
+                       q_offset, d, d_v > 0 ? d_v : d, dtype, causal, rope_base, rope_layout,
+                       scale, workspace, workspace_bytes, stream);
 }
 
 int csattn_rope_rotate(const void* x, void* x_rot, int B, int H, int T, int d, int dtype,
@@ -494,16 +545,18 @@ int csattn::attn_decode_check(const char* fn, int B, int Hq, int Hkv, int Lmax, 
 
 namespace {
 
-// Shared by csattn_attn_decode (len_add 0) and csattn_attn_decode_step (len_add 1:
-// the appended row).
+// Shared by csattn_attn_decode (len_add 0), csattn_attn_decode_ext (dv may differ
+// from d) and csattn_attn_decode_step (len_add 1: the appended row).
 int decode_impl(const char* fn, const void* q, const void* k_cache, const void* v_cache,
                 const int32_t* seq_lens, int len_add, void* out, int B, int Hq, int Hkv, int Lmax,
                 int d, int dtype, float scale, int max_seq_len, int num_splits, void* workspace,
                 size_t workspace_bytes, void* stream, const int32_t* block_table = nullptr,
-                int page_size = 0, int num_pages = 0, int max_pages = 0) {
+                int page_size = 0, int num_pages = 0, int max_pages = 0, int dv = 0) {
   int rc = decode_check(fn, q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, Lmax, d, dtype, scale,
                         max_seq_len, num_splits);
   if (rc != CSATTN_OK) return rc;
+  if (dv <= 0) dv = d;
+  if (dv != 64 && dv != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: dv=%d", fn, dv);
   DecodeArgs a{};
   a.q = q;
   a.k_cache = k_cache;
@@ -520,6 +573,7 @@ int decode_impl(const char* fn, const void* q, const void* k_cache, const void* 
   a.Hkv = Hkv;
   a.Lmax = Lmax;
   a.d = d;
+  a.dv = dv;
   a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   a.max_seq_len = max_seq_len;
   int num_sms = 0;
@@ -538,7 +592,7 @@ int decode_impl(const char* fn, const void* q, const void* k_cache, const void* 
       a.chunk *= 2;
   }
   a.n_splits = (max_seq_len + a.chunk - 1) / a.chunk;
-  const size_t need = static_cast<size_t>(B) * Hq * a.n_splits * (static_cast<size_t>(d) + 2) * 4;
+  const size_t need = static_cast<size_t>(B) * Hq * a.n_splits * (static_cast<size_t>(dv) + 2) * 4;
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
     return fail(CSATTN_ERR_WORKSPACE,
                 "%s: needs a 16-byte aligned workspace of %zu bytes (got %zu)", fn, need,
@@ -548,7 +602,7 @@ int decode_impl(const char* fn, const void* q, const void* k_cache, const void* 
     if (rc != CSATTN_OK) return rc;
   }
   a.part_o = static_cast<float*>(workspace);
-  a.part_ml = a.part_o + static_cast<size_t>(B) * Hq * a.n_splits * d;
+  a.part_ml = a.part_o + static_cast<size_t>(B) * Hq * a.n_splits * dv;
   if (tensor_map_encoder() == nullptr)
     return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
   cudaError_t e = launch_decode_bf16(a, static_cast<cudaStream_t>(stream));
@@ -566,6 +620,16 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                        void* workspace, size_t workspace_bytes, void* stream) {
   return decode_impl("attn_decode", q, k_cache, v_cache, seq_lens, 0, out, B, Hq, Hkv, Lmax, d,
                      dtype, scale, max_seq_len, num_splits, workspace, workspace_bytes, stream);
+}
+
+int csattn_attn_decode_ext(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int Lmax,
+                           int d, int dv, int dtype, float scale, int max_seq_len,
+                           int num_splits, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  return decode_impl("attn_decode_ext", q, k_cache, v_cache, seq_lens, 0, out, B, Hq, Hkv, Lmax,
+                     d, dtype, scale, max_seq_len, num_splits, workspace, workspace_bytes, stream,
+                     nullptr, 0, 0, 0, dv > 0 ? dv : d);
 }
 
 int csattn_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,

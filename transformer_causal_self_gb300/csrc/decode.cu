@@ -5,7 +5,8 @@
 // cache.pos and the keys run from 0 to cache.pos).  The whole cost is reading
 // K and V once: 2 * n_kv * d_head * L * sizeof(bf16) bytes per sequence, the
 // pages' KV-cache formula with one layer (same page, section "What else the
-// modern decoder-only model changed").
+// modern decoder-only model changed").  Keys have d channels and values dv
+// (each 64 or 128; "Scaled dot-product attention" lets the widths differ).
 //
 // Grid (split, kv_head, batch).  One CTA reads a chunk of one sequence's K/V
 // rows once for all the query heads of the KV head's group:
@@ -32,13 +33,16 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+template <int D, int DV>
 struct DCfg {
-  static constexpr int KB = D / 64;
+  static constexpr int KBK = D / 64;                // 64-column blocks of a K tile
+  static constexpr int KBV = DV / 64;               // ... of a V tile
   static constexpr int BLOCK_BYTES = KT * 128;      // one 64-column block of a 64-row tile
-  static constexpr int TILE_BYTES = KT * D * 2;     // K or V tile
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int K_BYTES = KT * D * 2;        // K tile
+  static constexpr int V_BYTES = KT * DV * 2;       // V tile
+  static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
   static constexpr int SMEM_BYTES = NS * STAGE_BYTES + 1024 + 1024;
+  static_assert(4 * 16 * DV * 4 <= NS * STAGE_BYTES, "per-warp results fit in the ring");
 };
 
 struct DParams {
@@ -84,11 +88,11 @@ __device__ __forceinline__ uint32_t tile_off(int r, int cc) {
   return static_cast<uint32_t>((cc >> 3) * (KT * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4));
 }
 
-template <int D>
+template <int D, int DV>
 __global__ void __launch_bounds__(kThreads)
     decode_bf16_kernel(const __grid_constant__ DParams p, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v) {
-  using C = DCfg<D>;
+  using C = DCfg<D, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(kThreads)
         __syncwarp();
         if (lane < nbox) {
           uint8_t* kdst = smem + s * C::STAGE_BYTES;
-          uint8_t* vdst = kdst + C::TILE_BYTES;
+          uint8_t* vdst = kdst + C::K_BYTES;
           const int r0 = lane * p.box_rows, tr = k_begin + t * KT + r0;
           int plane = p.num_pages * p.Hkv, prow = 0;
           if (tr < L) {
@@ -163,12 +167,12 @@ __global__ void __launch_bounds__(kThreads)
               atomicOr(p.status, kStatusDeviceArg);
             prow = tr % p.page_size;
           }
-          for (int kb = 0; kb < C::KB; ++kb) {
+          for (int kb = 0; kb < C::KBK; ++kb)
             tma_load_3d(kdst + kb * C::BLOCK_BYTES + r0 * 128, &tm_k, &full[s], kb * 64, prow,
                         plane);
+          for (int kb = 0; kb < C::KBV; ++kb)
             tma_load_3d(vdst + kb * C::BLOCK_BYTES + r0 * 128, &tm_v, &full[s], kb * 64, prow,
                         plane);
-          }
         }
         __syncwarp();
         ++issued;
@@ -190,13 +194,13 @@ __global__ void __launch_bounds__(kThreads)
         if (use > 0 && !ctl_wait(&empty[s], (use - 1) & 1, abort_flag, p.status, kWaitNs)) break;
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         uint8_t* kdst = smem + s * C::STAGE_BYTES;
-        uint8_t* vdst = kdst + C::TILE_BYTES;
+        uint8_t* vdst = kdst + C::K_BYTES;
         const int row = k_begin + t * KT;
         if (p.block_table == nullptr) {
-          for (int kb = 0; kb < C::KB; ++kb) {
+          for (int kb = 0; kb < C::KBK; ++kb)
             tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &full[s], kb * 64, row, z);
+          for (int kb = 0; kb < C::KBV; ++kb)
             tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &full[s], kb * 64, row, z);
-          }
         } else {
           // paged: boxes of box_rows rows (64, or the page size when it is 16 or 32)
           // never cross a page; a box past the sequence, or a page index outside the
@@ -213,12 +217,12 @@ __global__ void __launch_bounds__(kThreads)
                 atomicOr(p.status, kStatusDeviceArg);
               prow = tr % p.page_size;
             }
-            for (int kb = 0; kb < C::KB; ++kb) {
+            for (int kb = 0; kb < C::KBK; ++kb)
               tma_load_3d(kdst + kb * C::BLOCK_BYTES + r0 * 128, &tm_k, &full[s], kb * 64, prow,
                           plane);
+            for (int kb = 0; kb < C::KBV; ++kb)
               tma_load_3d(vdst + kb * C::BLOCK_BYTES + r0 * 128, &tm_v, &full[s], kb * 64, prow,
                           plane);
-            }
           }
         }
         ++issued;
@@ -247,9 +251,9 @@ __global__ void __launch_bounds__(kThreads)
     qa[kk][3] = (r0 + 8 < p.rep) ? q8[(16 * kk + 8 + cq) >> 1] : 0u;
   }
 
-  float o[D / 8][4];
+  float o[DV / 8][4];
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  for (int n = 0; n < DV / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m_used[2] = {-INFINITY, -INFINITY};  // rows r0, r0 + 8
   float l_part[2] = {0.f, 0.f};
   const float sl2 = p.scale_log2;
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(kThreads)
       break;
     }
     const uint32_t kbase = smem_base + s * C::STAGE_BYTES;
-    const uint32_t vbase = kbase + C::TILE_BYTES;
+    const uint32_t vbase = kbase + C::K_BYTES;
     const int key0 = k_begin + t * KT + 16 * warp;  // first key of this warp's slice
     const int nvalid = k_end - key0;                // keys of the slice that exist (may be <= 0)
 
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
+      for (int n = 0; n < DV / 8; ++n) {
         o[n][0] *= f[0];
         o[n][1] *= f[0];
         o[n][2] *= f[1];
@@ -337,10 +341,10 @@ __global__ void __launch_bounds__(kThreads)
     // V rows past the end of the sequence may hold anything: zero them
     const bool zeroed = nvalid < 16;
     if (zeroed) {
-      uint8_t* vtile = smem + s * C::STAGE_BYTES + C::TILE_BYTES;
+      uint8_t* vtile = smem + s * C::STAGE_BYTES + C::K_BYTES;
       const int first = nvalid < 0 ? 0 : nvalid;
-      for (int e = lane; e < 16 * (D / 8); e += 32) {
-        const int rr = e / (D / 8), cc = e % (D / 8);
+      for (int e = lane; e < 16 * (DV / 8); e += 32) {
+        const int rr = e / (DV / 8), cc = e % (DV / 8);
         if (rr >= first)
           *reinterpret_cast<uint4*>(vtile + tile_off(16 * warp + rr, cc)) = make_uint4(0, 0, 0, 0);
       }
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(kThreads)
       const int mi = lane >> 3;
       const int vr = 16 * warp + (lane & 7) + 8 * (mi & 1);
 #pragma unroll
-      for (int np = 0; np < D / 16; ++np) {
+      for (int np = 0; np < DV / 16; ++np) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vbase + tile_off(vr, 2 * np + (mi >> 1)), b0, b1, b2, b3);
         mma_bf16(o[2 * np], pa0, pa1, pa2, pa3, b0, b1);
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(kThreads)
   // all tiles consumed: the ring is free to hold the per-warp results
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
   if (!ok || *abort_flag) return;
-  float* s_o = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][D]
+  float* s_o = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][DV]
   if ((lane & 3) == 0) {
     s_ml[(warp * 16 + r0) * 2 + 0] = m_used[0];
     s_ml[(warp * 16 + r0) * 2 + 1] = l_part[0];
@@ -380,17 +384,17 @@ __global__ void __launch_bounds__(kThreads)
     s_ml[(warp * 16 + r0 + 8) * 2 + 1] = l_part[1];
   }
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) {
+  for (int n = 0; n < DV / 8; ++n) {
     const int c = 8 * n + cq;
-    s_o[(warp * 16 + r0) * D + c] = o[n][0];
-    s_o[(warp * 16 + r0) * D + c + 1] = o[n][1];
-    s_o[(warp * 16 + r0 + 8) * D + c] = o[n][2];
-    s_o[(warp * 16 + r0 + 8) * D + c + 1] = o[n][3];
+    s_o[(warp * 16 + r0) * DV + c] = o[n][0];
+    s_o[(warp * 16 + r0) * DV + c + 1] = o[n][1];
+    s_o[(warp * 16 + r0 + 8) * DV + c] = o[n][2];
+    s_o[(warp * 16 + r0 + 8) * DV + c + 1] = o[n][3];
   }
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
   // merge the four warps; write this split's partial for each head of the group
-  for (int e = threadIdx.x; e < p.rep * D; e += 32 * kComputeWarps) {
-    const int r = e / D, c = e % D;
+  for (int e = threadIdx.x; e < p.rep * DV; e += 32 * kComputeWarps) {
+    const int r = e / DV, c = e % DV;
     float m = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kComputeWarps; ++w) m = fmaxf(m, s_ml[(w * 16 + r) * 2]);
@@ -399,11 +403,11 @@ __global__ void __launch_bounds__(kThreads)
     for (int w = 0; w < kComputeWarps; ++w) {
       const float mw = s_ml[(w * 16 + r) * 2];
       const float fw = (mw == -INFINITY) ? 0.f : ex2_approx(mw - m);
-      acc += fw * s_o[(w * 16 + r) * D + c];
+      acc += fw * s_o[(w * 16 + r) * DV + c];
       l += fw * s_ml[(w * 16 + r) * 2 + 1];
     }
     const size_t row = (static_cast<size_t>(b) * p.Hq + kvh * p.rep + r) * p.n_splits + split;
-    p.part_o[row * D + c] = acc;
+    p.part_o[row * DV + c] = acc;
     if (c == 0) {
       p.part_ml[row * 2 + 0] = m;
       p.part_ml[row * 2 + 1] = l;
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// out[b, h, :] = merge of the splits that hold keys of sequence b.
+// out[b, h, :] = merge of the splits that hold keys of sequence b (D = the value width).
 __global__ void decode_combine_kernel(const float* __restrict__ part_o,
                                       const float* __restrict__ part_ml,
                                       const int32_t* __restrict__ seq_lens, int len_add,
@@ -443,9 +447,9 @@ __global__ void decode_combine_kernel(const float* __restrict__ part_o,
   }
 }
 
-template <int D>
+template <int D, int DV>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
-  using C = DCfg<D>;
+  using C = DCfg<D, DV>;
   DParams p{};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.seq_lens = a.seq_lens;
@@ -473,18 +477,18 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   const int planes = a.block_table != nullptr ? a.num_pages * a.Hkv : a.B * a.Hkv;
   const int box = a.block_table != nullptr ? p.box_rows : KT;
   if (!make_tmap_bf16_3d(&tk, a.k_cache, D, rows, planes, box) ||
-      !make_tmap_bf16_3d(&tv, a.v_cache, D, rows, planes, box))
+      !make_tmap_bf16_3d(&tv, a.v_cache, DV, rows, planes, box))
     return cudaErrorInvalidValue;
   static SmemLimitOnce smem_limit;
-  cudaError_t e = smem_limit.set(decode_bf16_kernel<D>, C::SMEM_BYTES);
+  cudaError_t e = smem_limit.set(decode_bf16_kernel<D, DV>, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_splits, a.Hkv, a.B);
-  decode_bf16_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tk, tv);
+  decode_bf16_kernel<D, DV><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p, tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.B * a.Hq, 1, 1);
-  cfg.blockDim = dim3(D, 1, 1);
+  cfg.blockDim = dim3(DV, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -494,17 +498,18 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float*>(a.part_o),
                             static_cast<const float*>(a.part_ml), a.seq_lens, a.len_add,
                             static_cast<__nv_bfloat16*>(a.out), a.Hq, a.n_splits, a.chunk,
-                            a.max_seq_len, D);
+                            a.max_seq_len, DV);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream) {
-  switch (a.d) {
-    case 64: return launch_d<64>(a, stream);
-    case 128: return launch_d<128>(a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  const int dv = a.dv > 0 ? a.dv : a.d;
+  if (a.d == 64 && dv == 64) return launch_d<64, 64>(a, stream);
+  if (a.d == 64 && dv == 128) return launch_d<64, 128>(a, stream);
+  if (a.d == 128 && dv == 64) return launch_d<128, 64>(a, stream);
+  if (a.d == 128 && dv == 128) return launch_d<128, 128>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace csattn

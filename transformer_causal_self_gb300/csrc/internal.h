@@ -41,9 +41,11 @@ struct FwdArgs {
 // fp32 SIMT path (d and dv each in {16,32,64,128}).
 cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t stream);
 
-// bf16 path: x_rot = RoPE(x) for x [B, H, T, d] bf16 (rope 1 split-half, 2 adjacent).
+// bf16 path: x_rot = RoPE(x) for x [B, H, T, d] bf16 (rope 1 split-half, 2 adjacent),
+// row t rotated at position pos0 + t.
 cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, int T, int d,
-                                    int rope, const RopeTable& theta, cudaStream_t stream);
+                                    int rope, const RopeTable& theta, cudaStream_t stream,
+                                    int pos0 = 0);
 
 // bf16 tcgen05 prefill; `k_eff` is k itself or its rotated copy.  q, k have d
 // and v, out dv channels (each 64 or 128): dv = 64 runs the kernel in
@@ -51,9 +53,12 @@ cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, in
 cudaError_t launch_fwd_sm103a(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
 cudaError_t launch_fwd_sm103a_d128(const FwdArgs& a, const void* k_eff, cudaStream_t stream);
 
-// Backward (bf16 d in {64, 128}; fp32 d in {16, 32, 64, 128}): dq, dk, dv of sum(out * dout).  qr, kr are the
-// rotated operands of the forward; dvec is fp32 scratch [B, Hq, Tq] for
-// rowsum(dout o out); lse is the forward's natural-log log-sum-exp.
+// Backward (bf16: d, d_v in {64, 128}; fp32: d, d_v in {16, 32, 64, 128}): dq, dk, dv
+// of sum(out * dout).  q [B, Hq, Tq, d], k [B, Hkv, Tk, d], v [B, Hkv, Tk, d_v], out and
+// dout [B, Hq, Tq, d_v]; query row i sits at position q_off + i, key j at j.  qr, kr
+// are the rotated operands of the forward (bf16; the fp32 path rotates them itself);
+// dvec is fp32 scratch [B, Hq, Tq] for rowsum(dout o out); lse is the forward's
+// natural-log log-sum-exp.
 struct BwdArgs {
   const void* qr;
   const void* kr;
@@ -66,6 +71,7 @@ struct BwdArgs {
   void* dk;
   void* dv;
   int B, Hq, Hkv, Tq, Tk, q_off, d;
+  int d_v;      // head size of v, out, dout and dv
   int num_sms;  // persistent dQ kernel grid
   int causal;
   int rope;  // 0 none, 1 split-half, 2 adjacent: dq, dk are rotated back by R^T
@@ -75,13 +81,12 @@ struct BwdArgs {
 };
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream);
-// fp32 backward on the SIMT cores (d in {16,32,64,128}, square T, q_off = 0).
-// a.qr, a.kr are q and k as given; with RoPE they are rotated into q_rot, k_rot
-// (fp32 scratch of q's and k's sizes) first.
+// fp32 backward on the SIMT cores.  a.qr, a.kr are q and k as given; with RoPE they
+// are rotated into q_rot, k_rot (fp32 scratch of q's and k's sizes) first.
 cudaError_t launch_bwd_f32(const BwdArgs& a, void* q_rot, void* k_rot, cudaStream_t stream);
-// dK, dV for d = 128 on tcgen05 (square T, q_off = 0); called by launch_bwd_bf16
+// dK, dV on tcgen05; called by launch_bwd_bf16
 cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t stream);
-// dQ for d = 128 on tcgen05 (square T, q_off = 0); called by launch_bwd_bf16
+// dQ on tcgen05; called by launch_bwd_bf16
 cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t stream);
 
 struct DecodeArgs {
@@ -97,11 +102,12 @@ struct DecodeArgs {
   int page_size, num_pages, max_pages;
   void* out;
   int B, Hq, Hkv, Lmax, d;
+  int dv;          // head size of v_cache and out (<= 0: d)
   float scale;
   int max_seq_len;
   int chunk;       // keys per split, multiple of 64
   int n_splits;    // ceil(max_seq_len / chunk)
-  float* part_o;   // [B, Hq, n_splits, d]
+  float* part_o;   // [B, Hq, n_splits, dv]
   float* part_ml;  // [B, Hq, n_splits, 2]
   uint32_t* status;
 };
@@ -142,8 +148,6 @@ int attn_decode_check_ptrs(const char* fn, const void* q, const void* k_cache,
 // Driver entry point for cuTensorMapEncodeTiled (nullptr if unavailable).
 void* tensor_map_encoder();
 
-// 3-D bf16 tensor map over rows of `d` elements: dims {d, rows, planes},
-// box {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
 // Appends Tn rotated keys and values per sequence at rows cache_lens[b] + t of
 // contiguous caches [B, Hkv, Lmax, d] (block_table == nullptr) or paged caches
 // [num_pages, Hkv, page_size, d] with Lmax = max_pages * page_size.
@@ -180,6 +184,8 @@ struct SmemLimitOnce {
   }
 };
 
+// 3-D bf16 tensor map over rows of `d` elements: dims {d, rows, planes},
+// box {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
 bool make_tmap_bf16_3d(void* tmap_out, const void* base, int d, int rows, int planes,
                        int box_rows);
 

@@ -1,4 +1,4 @@
-// RoPE on bf16 keys, once per call: x_rot[b,h,t,:] = R_t x[b,h,t,:], rounded
+// RoPE on bf16 keys, once per call: x_rot[b,h,t,:] = R_{pos0+t} x[b,h,t,:], rounded
 // to bf16 (round-to-nearest-even) as the pages' apply_rope returns the input
 // dtype ("The Transformer architecture" (cooking-agi), section "Now: RoPE";
 // angle pos * base^(-2p/d) from "Transformer" (ai-notes), RoPE section).
@@ -36,7 +36,7 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&f)[8]) {
 // x, x_rot: [B, H, T, d]; thread -> (b, t, c) with c in [0, d/16): pairs 8c..8c+7.
 __global__ void __launch_bounds__(256) rope_rotate_bf16_kernel(
     const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ x_rot, int B, int H, int T,
-    int d, int layout, RopeTable theta) {
+    int d, int layout, RopeTable theta, int pos0) {
   const int chunks = d / 16;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long total = (long long)B * T * chunks;
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) rope_rotate_bf16_kernel(
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int p = 8 * c + i;
-    rope_cos_sin<false>(t, theta.hi[p], theta.lo[p], cs[i], sn[i]);
+    rope_cos_sin<false>(pos0 + t, theta.hi[p], theta.lo[p], cs[i], sn[i]);
   }
   // element offsets of the two 8-wide vectors this thread rotates
   int e0, e1;
@@ -89,13 +89,14 @@ __global__ void __launch_bounds__(256) rope_rotate_bf16_kernel(
 }  // namespace
 
 cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, int T, int d,
-                                       int rope, const RopeTable& theta, cudaStream_t stream) {
+                                    int rope, const RopeTable& theta, cudaStream_t stream,
+                                    int pos0) {
   const long long total = (long long)B * T * (d / 16);
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   rope_rotate_bf16_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(x_rot), B, H, T, d, rope,
-      theta);
+      theta, pos0);
   return cudaGetLastError();
 }
 
