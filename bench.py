@@ -634,7 +634,7 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": _traffic("cross"),
                      "kernel": "fwd_d128_kernel"}}
-    del q, k, v, o, flush
+    del q, k, v, o
 
     g = torch.Generator()
     g.manual_seed(7)
@@ -721,34 +721,66 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
                                "decode_combine_kernel"}}
     del kp, vp, table
     # a 1024-token chunk of the llama_chunk_bf16 shape appended (keys rotated) at row 3072
-    # of contiguous caches; bytes = the chunk's K and V read once and written once
+    # of contiguous caches; bytes = the chunk's K and V read once and written once.  The
+    # call takes ~10 us, so a bracket of CUDA events around each launch mostly measures
+    # the events: the row times NSET back-to-back appends, each with its own chunk and
+    # caches (NSET x 33.5 MB of reads and writes, more than L2), after one L2 flush.
     g.manual_seed(10)
-    kn = torch.randn(wc.B, wc.Hkv, 1024, wc.d, generator=g).to(torch.bfloat16).to(dev)
-    vn = torch.randn(wc.B, wc.Hkv, 1024, wc.d, generator=g).to(torch.bfloat16).to(dev)
-    kca = torch.zeros(wc.B, wc.Hkv, wc.Tk, wc.d, dtype=torch.bfloat16, device=dev)
-    vca = torch.zeros_like(kca)
+    nset = 8
+    kns = [torch.randn(wc.B, wc.Hkv, 1024, wc.d, generator=g).to(torch.bfloat16).to(dev)
+           for _ in range(nset)]
+    vns = [torch.randn(wc.B, wc.Hkv, 1024, wc.d, generator=g).to(torch.bfloat16).to(dev)
+           for _ in range(nset)]
+    kcas = [torch.zeros(wc.B, wc.Hkv, wc.Tk, wc.d, dtype=torch.bfloat16, device=dev)
+            for _ in range(nset)]
+    vcas = [torch.zeros_like(kcas[0]) for _ in range(nset)]
     at = torch.full((wc.B,), wc.q_offset, dtype=torch.int32, device=dev)
     ts = []
     for i in range(3 + reps):
+        flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        csattn.cache_append(kn, vn, kca, vca, at, rope_base=wc.rope_base, stream=stream)
+        for s_ in range(nset):
+            csattn.cache_append(kns[s_], vns[s_], kcas[s_], vcas[s_], at, rope_base=wc.rope_base,
+                                stream=stream)
         e1.record(stream)
         if i >= 3:
             ts.append((e0, e1))
     torch.cuda.synchronize()
     csattn.check_status(stream)
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
-    abytes = 2.0 * 2 * kn.numel() * 2
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts) / nset
+    abytes = 2.0 * 2 * kns[0].numel() * 2
     gbs = abytes / (ms * 1e-3) / 1e9
+    # context: a plain device copy of the same bytes (16.8 MB read + 16.8 MB written),
+    # timed the same way (NSET distinct buffers per bracket, L2 flushed before each)
+    csrc_ = [torch.cat([a.reshape(-1), b.reshape(-1)]) for a, b in zip(kns, vns)]
+    cdst_ = [torch.empty_like(x) for x in csrc_]
+    tc_ = []
+    for i in range(3 + reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for s_ in range(nset):
+                cdst_[s_].copy_(csrc_[s_])
+        e1.record(stream)
+        if i >= 3:
+            tc_.append((e0, e1))
+    torch.cuda.synchronize()
+    copy_ms = statistics.mean(a.elapsed_time(b) for a, b in tc_) / nset
+    del csrc_, cdst_
     out["cache_append"] = {
         "workload": "1024-token chunk appended to contiguous caches (B=4, Hkv=8, d=128, "
-                    "Lmax=4096, rows 3072..4095), keys rotated (RoPE 1e4)",
+                    "Lmax=4096, rows 3072..4095), keys rotated (RoPE 1e4); 8 back-to-back "
+                    "appends of distinct chunks into distinct caches per timed bracket, L2 "
+                    "flushed before each bracket",
         "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": abytes,
+        "same_bytes_device_copy": {"ms": round(copy_ms, 4),
+                                   "gbs": round(abytes / (copy_ms * 1e-3) / 1e9, 1)},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(gbs / hbm_peak, 4), "traffic": _traffic("append"),
                      "kernel": "cache_append_kernel"}}
-    del kn, vn, kca, vca
+    del kns, vns, kcas, vcas, flush
     # backward of the headline prefill (dq, dk, dv), FLOPs = 2.5x the forward's (the
     # convention for QK^T recomputation + dV + dP + dQ + dK)
     wp = W.WORKLOADS["llama_gqa_bf16"]

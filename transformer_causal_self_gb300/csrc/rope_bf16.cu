@@ -7,50 +7,34 @@
 // inside the attention kernel would repeat the same rotation T/128 times per
 // key; this bandwidth-bound pass does it once (read + write of K).  One thread
 // owns 8 channel pairs of one position and applies the same 8 (cos, sin) to
-// that position in every head of the batch entry, so the angles are computed
-// once per (b, t) rather than once per head.
+// that position in up to 4 heads of the batch entry, so the angles are computed
+// once per (b, t) and head group rather than once per head.
 #include "internal.h"
 
 namespace csattn {
 namespace {
 
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = bf16lo_to_f32(w[i]);
-    f[2 * i + 1] = bf16hi_to_f32(w[i]);
-  }
-}
+// x, x_rot: [B, H, T, d]; thread -> (b, head group, t, c) with c in [0, d/16): pairs
+// 8c..8c+7 of position pos0 + t in the kRopeHeads heads of the group.  The thread
+// issues the loads of all of its heads, then computes the 8 angles while they are in
+// flight, then rotates and stores (a loop of load-rotate-store per head keeps two
+// loads in flight per thread and leaves the kernel waiting on memory).
+constexpr int kRopeHeads = 4;
 
-__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&f)[8]) {
-  uint4 u;
-  u.x = pack_bf16x2(f[0], f[1]);
-  u.y = pack_bf16x2(f[2], f[3]);
-  u.z = pack_bf16x2(f[4], f[5]);
-  u.w = pack_bf16x2(f[6], f[7]);
-  *reinterpret_cast<uint4*>(p) = u;
-}
-
-// x, x_rot: [B, H, T, d]; thread -> (b, t, c) with c in [0, d/16): pairs 8c..8c+7.
 __global__ void __launch_bounds__(256) rope_rotate_bf16_kernel(
     const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ x_rot, int B, int H, int T,
     int d, int layout, RopeTable theta, int pos0) {
   const int chunks = d / 16;
+  const int groups = (H + kRopeHeads - 1) / kRopeHeads;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long total = (long long)B * T * chunks;
+  const long long total = (long long)B * groups * T * chunks;
   if (idx >= total) return;
   const int c = static_cast<int>(idx % chunks);
   const int t = static_cast<int>((idx / chunks) % T);
-  const int b = static_cast<int>(idx / ((long long)chunks * T));
-
-  float cs[8], sn[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int p = 8 * c + i;
-    rope_cos_sin<false>(pos0 + t, theta.hi[p], theta.lo[p], cs[i], sn[i]);
-  }
+  const long long bg = idx / ((long long)chunks * T);
+  const int hgrp = static_cast<int>(bg % groups);
+  const int b = static_cast<int>(bg / groups);
+  const int h0 = hgrp * kRopeHeads;
   // element offsets of the two 8-wide vectors this thread rotates
   int e0, e1;
   if (layout == 1) {  // split-half: channel p with p + d/2
@@ -60,29 +44,46 @@ __global__ void __launch_bounds__(256) rope_rotate_bf16_kernel(
     e0 = 16 * c;
     e1 = 16 * c + 8;
   }
-  for (int h = 0; h < H; ++h) {
-    const size_t base = (((size_t)b * H + h) * (size_t)T + t) * d;
-    float u[8], w[8], ou[8], ow[8];
-    load8(x + base + e0, u);
-    load8(x + base + e1, w);
-    if (layout == 1) {
+  uint4 lo[kRopeHeads], hi[kRopeHeads];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        ou[i] = fmaf(u[i], cs[i], -w[i] * sn[i]);
-        ow[i] = fmaf(u[i], sn[i], w[i] * cs[i]);
-      }
-    } else {
-      // pairs (u0,u1),(u2,u3),(u4,u5),(u6,u7) -> pairs 0..3; (w0,w1).. -> pairs 4..7
+  for (int k = 0; k < kRopeHeads; ++k) {
+    if (h0 + k < H) {
+      const size_t base = (((size_t)b * H + h0 + k) * (size_t)T + t) * d;
+      lo[k] = __ldg(reinterpret_cast<const uint4*>(x + base + e0));
+      hi[k] = __ldg(reinterpret_cast<const uint4*>(x + base + e1));
+    }
+  }
+  float cs[8], sn[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        ou[2 * i] = fmaf(u[2 * i], cs[i], -u[2 * i + 1] * sn[i]);
-        ou[2 * i + 1] = fmaf(u[2 * i], sn[i], u[2 * i + 1] * cs[i]);
-        ow[2 * i] = fmaf(w[2 * i], cs[4 + i], -w[2 * i + 1] * sn[4 + i]);
-        ow[2 * i + 1] = fmaf(w[2 * i], sn[4 + i], w[2 * i + 1] * cs[4 + i]);
+  for (int i = 0; i < 8; ++i) {
+    const int p = 8 * c + i;
+    rope_cos_sin<false>(pos0 + t, theta.hi[p], theta.lo[p], cs[i], sn[i]);
+  }
+#pragma unroll
+  for (int k = 0; k < kRopeHeads; ++k) {
+    if (h0 + k >= H) continue;
+    const size_t base = (((size_t)b * H + h0 + k) * (size_t)T + t) * d;
+    // one 32-bit word of each half at a time: the pairs of word i are (u_j, w_j), j = 2i,
+    // 2i + 1 (split-half), or (u0, u1) = pair i and (w0, w1) = pair 4 + i (adjacent)
+    uint32_t wa[4] = {lo[k].x, lo[k].y, lo[k].z, lo[k].w};
+    uint32_t wb[4] = {hi[k].x, hi[k].y, hi[k].z, hi[k].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float u0 = bf16lo_to_f32(wa[i]), u1 = bf16hi_to_f32(wa[i]);
+      const float w0 = bf16lo_to_f32(wb[i]), w1 = bf16hi_to_f32(wb[i]);
+      if (layout == 1) {
+        wa[i] = pack_bf16x2(fmaf(u0, cs[2 * i], -w0 * sn[2 * i]),
+                            fmaf(u1, cs[2 * i + 1], -w1 * sn[2 * i + 1]));
+        wb[i] = pack_bf16x2(fmaf(u0, sn[2 * i], w0 * cs[2 * i]),
+                            fmaf(u1, sn[2 * i + 1], w1 * cs[2 * i + 1]));
+      } else {
+        wa[i] = pack_bf16x2(fmaf(u0, cs[i], -u1 * sn[i]), fmaf(u0, sn[i], u1 * cs[i]));
+        wb[i] = pack_bf16x2(fmaf(w0, cs[4 + i], -w1 * sn[4 + i]),
+                            fmaf(w0, sn[4 + i], w1 * cs[4 + i]));
       }
     }
-    store8(x_rot + base + e0, ou);
-    store8(x_rot + base + e1, ow);
+    *reinterpret_cast<uint4*>(x_rot + base + e0) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+    *reinterpret_cast<uint4*>(x_rot + base + e1) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
   }
 }
 
@@ -91,7 +92,8 @@ __global__ void __launch_bounds__(256) rope_rotate_bf16_kernel(
 cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, int T, int d,
                                     int rope, const RopeTable& theta, cudaStream_t stream,
                                     int pos0) {
-  const long long total = (long long)B * T * (d / 16);
+  const long long total =
+      (long long)B * ((H + kRopeHeads - 1) / kRopeHeads) * T * (d / 16);
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   rope_rotate_bf16_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
