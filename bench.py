@@ -208,6 +208,25 @@ def _gpu_numa_node(index):
         return None
 
 
+def _bind_near_gpu(index):
+    """Restrict this process to the allowed CPUs on the GPU's NUMA node, so that the
+    pinned host buffers allocated next are placed on that node (first touch) and the
+    copy threads run next to the GPU.  Returns (previous CPU set, CPUs now used), or
+    (None, None) when the node is unknown or no allowed CPU sits on it."""
+    try:
+        node = _gpu_numa_node(index)
+        allowed = os.sched_getaffinity(0)
+        if node is None:
+            return None, None
+        near = {c for c in allowed if _cpu_node(c) == node}
+        if not near or near == allowed:
+            return None, None
+        os.sched_setaffinity(0, near)
+        return allowed, near
+    except (OSError, AttributeError):
+        return None, None
+
+
 def _cpu_node(cpu):
     try:
         for e in os.listdir(f"/sys/devices/system/cpu/cpu{cpu}"):
@@ -385,6 +404,7 @@ def run_gpu(args):
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     e2e = None
     if rank == 0 or world > 1:
+        prev_cpus, near_cpus = _bind_near_gpu(dev.index)
         pin = lambda t: t.pin_memory()  # noqa: E731
         hq, hk, hv = pin(q_h), pin(k_h), pin(v_h)
         hqd, hkc, hvc, hl = pin(qd_h), pin(kc_h), pin(vc_h), pin(lens_h)
@@ -425,11 +445,18 @@ def run_gpu(args):
                "decode": {"value": round(world * dbytes / (e_dec * 1e-3) / 1e9, 1),
                           "unit": "GB/s"},
                "host_link": _host_link(torch, (hq, hk, hv), (q, k, v), stream),
+               "cpu_binding": (f"{len(near_cpus)} CPUs on the GPU's NUMA node (of "
+                               f"{len(prev_cpus)} allowed) while the pinned buffers were "
+                               "allocated and the leg ran" if near_cpus else
+                               "unchanged (every allowed CPU is on the GPU's NUMA node, or "
+                               "the node is unknown)"),
                "note": "pinned host buffers; prefill through csattn_attn_fwd_host (H2D of "
                        "q, k, v, the kernels and D2H of out pipelined over 8 chunks inside the "
                        "call); decode through csattn_attn_decode_host (H2D of q, seq_lens and "
                        "the K/V rows below seq_lens, the kernels and D2H of out, pipelined "
                        "over 4 chunks of sequences), inside each timed step"}
+        if prev_cpus:
+            os.sched_setaffinity(0, prev_cpus)
 
     rows = None
     if rank == 0 and not args.no_rows:
