@@ -168,8 +168,8 @@ def _traffic(key):
 def _host_link(torch, hosts, devs, stream):
     """The host link as this run sees it: the pinned host buffers `hosts` (the prefill's
     q, k, v: 201 MiB) copied to the device buffers `devs` and back, one direction at a
-    time, timed with CUDA events on `stream` (best of 3), plus where this process sits
-    relative to the GPU (NUMA nodes)."""
+    time and both at once (bytes moved in both directions / time), timed with CUDA
+    events (best of 3), plus where this process sits relative to the GPU (NUMA nodes)."""
     nbytes = sum(h.numel() * h.element_size() for h in hosts)
     res = {"bytes": int(nbytes)}
     for name, h2d in (("h2d_gbs", True), ("d2h_gbs", False)):
@@ -184,6 +184,28 @@ def _host_link(torch, hosts, devs, stream):
             ms = e0.elapsed_time(e1)
             best = ms if best is None else min(best, ms)
         res[name] = round(nbytes / (best * 1e-3) / 1e9, 1)
+    # both directions at once (the end-to-end calls overlap them): the same bytes in on
+    # `stream` while as many go out on a second stream into other pinned buffers
+    outs = [torch.empty_like(h).pin_memory() for h in hosts]
+    side = torch.cuda.Stream(device=devs[0].device)
+    best = None
+    for _ in range(3):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        side.wait_event(e0)
+        for h, d in zip(hosts, devs):
+            d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(side):
+            for o, d in zip(outs, devs):
+                o.copy_(d, non_blocking=True)
+        e1.record(stream)
+        e2.record(side)
+        e1.synchronize()
+        e2.synchronize()
+        ms = max(e0.elapsed_time(e1), e0.elapsed_time(e2))
+        best = ms if best is None else min(best, ms)
+    res["both_directions_gbs"] = round(2 * nbytes / (best * 1e-3) / 1e9, 1)
+    del outs
     res["gpu_numa_node"] = _gpu_numa_node(devs[0].device.index)
     try:
         cpus = sorted(os.sched_getaffinity(0))
