@@ -4,7 +4,7 @@ import math
 import numpy as np
 import torch
 
-# Spec bounds: fp32 inputs max-abs 1e-5; bf16 inputs (fp32 accumulation)
+# Parity bounds: fp32 inputs max-abs 1e-5; bf16 inputs (fp32 accumulation)
 # max-abs 2e-2 and relative L2 5e-3.
 F32_ATOL = 1e-5
 BF16_ATOL = 2e-2

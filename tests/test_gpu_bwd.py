@@ -1,7 +1,7 @@
 """Backward parity: dq, dk, dv from csattn_attn_bwd against the float64 oracle's
 gradients (oracle.attn.attention_backward) on the same bf16 inputs.
 
-Tolerance (bf16).  The benchmark spec's bounds, max-abs 2e-2 and relative L2 5e-3,
+Tolerance (bf16).  The parity bounds, max-abs 2e-2 and relative L2 5e-3,
 with one allowance: the gradients are returned in bf16, and where their entries
 exceed the attention output's range (|dv| reaches ~10 on these inputs) the
 rounding of the stored value alone is up to half a bf16 ulp, 2^(e-8) for an entry
@@ -138,8 +138,8 @@ def test_bwd_gqa_equals_summed_mha():
 # fp32 operands, fp32 arithmetic throughout (accurate sine/cosine for RoPE, fp32
 # forward out and lse): each gradient entry is a sum of at most T products of
 # terms carrying a few fp32 roundings (2^-24 ~ 6e-8) each, and P = exp(S - lse)
-# carries the absolute error of S and lse (~1e-6 for |S| ~ 10).  Bound: the north
-# star's fp32 max-abs 1e-5 (absolute) and relative L2 1e-5; the relative L2 floor
+# carries the absolute error of S and lse (~1e-6 for |S| ~ 10).  Bound: the
+# fp32 parity bound, max-abs 1e-5 (absolute), and relative L2 1e-5; the relative L2 floor
 # is 0.1 sqrt(n) (RMS error <= 1e-6 where the exact gradient vanishes, T = 1).
 
 FP32_CASES = [
