@@ -502,6 +502,22 @@ def pin_backward_finite_differences(o):
     got = o.attention_backward(q, k, v, do, **kw)
     for name, a, b in zip("qkv", got, _fd_grads(o, q, k, v, do, kw)):
         assert np.max(np.abs(a - b)) < 1e-7, ("offset", name)
+    # values of their own width: a chunk (d_v > d_k) and an unmasked rectangle (d_v < d_k,
+    # Tq > Tk) with RoPE at an offset
+    for tag, shp, kw in (("dv>dk", (2, 1, 3, 7, 4, 6), dict(causal=True, rope_base=100.0,
+                                                            scale=0.5, q_offset=4)),
+                         ("rect", (2, 2, 5, 3, 8, 4), dict(causal=False, rope_base=60.0,
+                                                           scale=0.35, q_offset=2,
+                                                           rope_layout="adjacent"))):
+        hq, hkv, tq, tk, dk, dv = shp
+        q = _rand((1, hq, tq, dk), 254)
+        k = _rand((1, hkv, tk, dk), 255)
+        v = _rand((1, hkv, tk, dv), 256)
+        do = _rand((1, hq, tq, dv), 257)
+        got = o.attention_backward(q, k, v, do, **kw)
+        assert got[0].shape == q.shape and got[1].shape == k.shape and got[2].shape == v.shape
+        for name, a, b in zip("qkv", got, _fd_grads(o, q, k, v, do, kw)):
+            assert np.max(np.abs(a - b)) < 1e-7, (tag, name, np.max(np.abs(a - b)))
 
 
 def pin_backward_autograd(o):
