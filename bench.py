@@ -862,6 +862,42 @@ def _measure_rows(csattn, W, torch, dev, stream, kc, vc, lens, lens_h, wd, max_l
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4), "traffic": _traffic("bwd"),
                      "kernel": "bwd_kv_tc_kernel + bwd_q_tc_kernel (tcgen05)"}}
+    del q, k, v, do, lse, o, dq, dk, dv, ws
+    # backward of the chunked prefill (llama_chunk_bf16: 1024 queries at offset 3072
+    # against 4096 keys) through csattn_attn_bwd_ext; FLOPs = 2.5x the chunk's forward
+    q, k, v = (t.to(dev) for t in W.make_chunk_inputs(wc))
+    g.manual_seed(9)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
+    lse = torch.empty(wc.B, wc.Hq, wc.Tq, dtype=torch.float32, device=dev)
+    o = csattn.attn_fwd_ext(q, k, v, q_offset=wc.q_offset, causal=True, rope_base=wc.rope_base,
+                            scale=wc.scale, lse=lse, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(csattn.bwd_ext_workspace_size(wc.B, wc.Hq, wc.Hkv, wc.Tq, wc.Tk, wc.d,
+                                                   q.dtype, wc.rope_base),
+                     dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(3 + max(3, reps // 5)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csattn.attn_bwd_ext(q, k, v, o, do, lse, q_offset=wc.q_offset, causal=True,
+                            rope_base=wc.rope_base, scale=wc.scale, dq=dq, dk=dk, dv=dv,
+                            workspace=ws, stream=stream)
+        e1.record(stream)
+        if i >= 3:
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    csattn.check_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    fl = 2.5 * wc.flops()
+    tf = fl / (ms * 1e-3) / 1e12
+    out["backward_chunk"] = {
+        "workload": "llama_chunk_bf16 backward (B=4, Hq=32, Hkv=8, 1024 queries at offset 3072, "
+                    "Tk=4096, d=128, RoPE 1e4; dq, dk, dv)",
+        "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": fl,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": tf_burst,
+                     "unit": "TFLOP/s", "frac": round(tf / tf_burst, 4),
+                     "traffic": _traffic("bwd_chunk"),
+                     "kernel": "bwd_kv_tc_kernel + bwd_q_tc_kernel (tcgen05)"}}
     return out
 
 
@@ -871,6 +907,7 @@ def run_profile_case(args):
     fwd:     the llama_gqa_bf16 prefill (RoPE pass + attention kernel), full size.
     decode:  the decode_bf16 workload with B=16 sequences (0.5 GB of cache).
     bwd:     the llama_gqa_bf16 backward (after one forward for out and lse), full size.
+    bwdchunk: the llama_chunk_bf16 backward (csattn_attn_bwd_ext), full size.
     gpt2:    the gpt2_bf16 prefill (d=64 attention kernel), full size.
     rope:    the RoPE pass over the llama_gqa_bf16 keys.
     append:  the 1024-token chunk append of the bench row.
@@ -903,6 +940,16 @@ def run_profile_case(args):
         for _ in range(2):
             csattn.attn_bwd(q, k, v, out, do, lse, causal=True, rope_base=w.rope_base,
                             scale=w.scale)
+    elif args.profile == "bwdchunk":
+        wc = W.WORKLOADS["llama_chunk_bf16"]
+        q, k, v = (t.to(dev) for t in W.make_chunk_inputs(wc))
+        do = torch.randn_like(q)
+        lse = torch.empty(wc.B, wc.Hq, wc.Tq, dtype=torch.float32, device=dev)
+        out = csattn.attn_fwd_ext(q, k, v, q_offset=wc.q_offset, causal=True,
+                                  rope_base=wc.rope_base, scale=wc.scale, lse=lse)
+        for _ in range(2):
+            csattn.attn_bwd_ext(q, k, v, out, do, lse, q_offset=wc.q_offset, causal=True,
+                                rope_base=wc.rope_base, scale=wc.scale)
     elif args.profile == "gpt2":
         w = W.WORKLOADS["gpt2_bf16"]
         q, k, v = (t.to(dev) for t in W.make_prefill_inputs(w))
@@ -1011,9 +1058,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the timing of the chunked-prefill and decode-step rows")
-    ap.add_argument("--profile", choices=["fwd", "decode", "bwd", "gpt2", "rope", "append",
-                                          "paged16", "step", "chunk", "cross", "paged256", "x4",
-                                          "long", "decpaged128", "decpaged16"], default=None,
+    ap.add_argument("--profile", choices=["fwd", "decode", "bwd", "bwdchunk", "gpt2", "rope",
+                                          "append", "paged16", "step", "chunk", "cross",
+                                          "paged256", "x4", "long", "decpaged128", "decpaged16"],
+                    default=None,
                     help="run a short single-kernel case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:

@@ -137,3 +137,26 @@ def test_bwd_ext_chunk_rows_match_full_sequence():
     assert_grad_close(to_np(chunk[0]), rq, "dq chunk")
     assert_grad_close(to_np(chunk[1]), rk, "dk chunk")
     assert_grad_close(to_np(chunk[2]), rv, "dv chunk")
+
+
+def test_bwd_ext_llama_chunk_workload_one_group():
+    """The bench's chunk workload at full size (B=4, Hq=32, Hkv=8, 1024 queries at offset
+    3072, Tk=4096, d=128, RoPE 1e4): one KV group (4 query heads) of one sequence against
+    the oracle."""
+    import attn_workloads as W
+    wc = W.WORKLOADS["llama_chunk_bf16"]
+    q, k, v = W.make_chunk_inputs(wc)
+    g = torch.Generator()
+    g.manual_seed(31)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv = _run(q, k, v, do, wc.q_offset, True, wc.rope_base, "split_half")
+    b, grp = 3, 6
+    rep = wc.Hq // wc.Hkv
+    hs = slice(grp * rep, (grp + 1) * rep)
+    rq, rk, rv = OA.attention_backward(q[b:b + 1, hs], k[b:b + 1, grp:grp + 1],
+                                       v[b:b + 1, grp:grp + 1], do[b:b + 1, hs], causal=True,
+                                       rope_base=wc.rope_base, scale=wc.scale,
+                                       operand_dtype="bf16", q_offset=wc.q_offset)
+    assert_grad_close(to_np(dq[b:b + 1, hs]), rq, "dq chunk group")
+    assert_grad_close(to_np(dk[b:b + 1, grp:grp + 1]), rk, "dk chunk group")
+    assert_grad_close(to_np(dv[b:b + 1, grp:grp + 1]), rv, "dv chunk group")
