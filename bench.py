@@ -437,7 +437,7 @@ def run_gpu(args):
         e_steps = max(1, min(args.steps, 10))
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e_steps)]
         # the prefill through csattn_attn_fwd_host: copies in, kernels and copies out
-        # pipelined over 8 chunks of (sequence, KV head) pairs inside the call (the default)
+        # pipelined over 16 chunks of (sequence, KV head) pairs inside the call (the default)
         ws_host = torch.empty(csattn.fwd_host_workspace_size(wp.B, wp.Hq, wp.Hkv, wp.T, wp.d,
                                                              torch.bfloat16, wp.rope_base),
                               dtype=torch.uint8, device=dev)
@@ -473,7 +473,7 @@ def run_gpu(args):
                                "unchanged (every allowed CPU is on the GPU's NUMA node, or "
                                "the node is unknown)"),
                "note": "pinned host buffers; prefill through csattn_attn_fwd_host (H2D of "
-                       "q, k, v, the kernels and D2H of out pipelined over 8 chunks inside the "
+                       "q, k, v, the kernels and D2H of out pipelined over 16 chunks inside the "
                        "call); decode through csattn_attn_decode_host (H2D of q, seq_lens and "
                        "the K/V rows below seq_lens, the kernels and D2H of out, pipelined "
                        "over 4 chunks of sequences), inside each timed step"}

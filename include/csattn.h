@@ -119,7 +119,7 @@ size_t csattn_fwd_host_workspace_size(int B, int Hq, int Hkv, int T, int d, int 
  * The results equal csattn_attn_fwd's bit for bit.
  *   q_h, k_h, v_h, out_h, lse_h  host pointers; page-locked memory (cudaHostAlloc or
  *                cudaHostRegister) lets the copies run asynchronously
- *   num_chunks   0: automatic (8, at most B * Hkv); otherwise 1..16 (capped at B*Hkv)
+ *   num_chunks   0: automatic (16, at most B * Hkv); otherwise 1..16 (capped at B*Hkv)
  *   workspace    device buffer of >= csattn_fwd_host_workspace_size() bytes,
  *                16-byte aligned, in use until the call's work on `stream` completes
  * Other arguments, checks and return codes as csattn_attn_fwd (messages name

@@ -22,7 +22,7 @@ namespace csattn {
 namespace {
 
 constexpr int kMaxChunks = 16;
-constexpr int kDefaultChunks = 8;
+constexpr int kDefaultChunks = 16;
 constexpr int kMaxDev = 64;
 
 int hfail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
