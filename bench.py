@@ -249,6 +249,28 @@ def _bind_near_gpu(index):
         return None, None
 
 
+def _prefer_node(node):
+    """Memory policy of the calling thread: new pages preferably on NUMA node `node`
+    (None: back to the default policy).  Linux set_mempolicy through syscall(2);
+    returns True when the call succeeded."""
+    import ctypes
+    import platform
+    nr = {"x86_64": 238, "aarch64": 237}.get(platform.machine())
+    if nr is None:
+        return False
+    try:
+        libc = ctypes.CDLL(None, use_errno=True)
+        libc.syscall.restype = ctypes.c_long
+        if node is None:
+            return libc.syscall(ctypes.c_long(nr), ctypes.c_long(0), None, ctypes.c_ulong(0)) == 0
+        mask = (ctypes.c_ulong * 16)()
+        mask[node // 64] = 1 << (node % 64)
+        return libc.syscall(ctypes.c_long(nr), ctypes.c_long(1), mask,
+                            ctypes.c_ulong(16 * 64)) == 0
+    except (OSError, AttributeError, ValueError):
+        return False
+
+
 def _cpu_node(cpu):
     try:
         for e in os.listdir(f"/sys/devices/system/cpu/cpu{cpu}"):
@@ -427,10 +449,14 @@ def run_gpu(args):
     e2e = None
     if rank == 0 or world > 1:
         prev_cpus, near_cpus = _bind_near_gpu(dev.index)
+        gpu_node = _gpu_numa_node(dev.index)
+        mem_pref = gpu_node is not None and _prefer_node(gpu_node)
         pin = lambda t: t.pin_memory()  # noqa: E731
         hq, hk, hv = pin(q_h), pin(k_h), pin(v_h)
         hqd, hkc, hvc, hl = pin(qd_h), pin(kc_h), pin(vc_h), pin(lens_h)
         ho, hod = torch.empty_like(hq).pin_memory(), torch.empty_like(hqd).pin_memory()
+        if mem_pref:
+            _prefer_node(None)
         # the decode leg copies q, seq_lens and only the cache rows it reads (dbytes)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hl)) + int(dbytes)
         d2h = ho.numel() * ho.element_size() + hod.numel() * hod.element_size()
@@ -467,6 +493,8 @@ def run_gpu(args):
                "decode": {"value": round(world * dbytes / (e_dec * 1e-3) / 1e9, 1),
                           "unit": "GB/s"},
                "host_link": _host_link(torch, (hq, hk, hv), (q, k, v), stream),
+               "memory_placement": ("pinned buffers allocated with the GPU's NUMA node "
+                                    "preferred" if mem_pref else "default policy"),
                "cpu_binding": (f"{len(near_cpus)} CPUs on the GPU's NUMA node (of "
                                f"{len(prev_cpus)} allowed) while the pinned buffers were "
                                "allocated and the leg ran" if near_cpus else
