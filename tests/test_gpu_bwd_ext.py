@@ -82,6 +82,37 @@ def test_bwd_ext_bf16(B, hq, hkv, Tq, Tk, off, d, dv, causal, base, layout):
         assert torch.count_nonzero(dv_[:, :, off + Tq:]).item() == 0
 
 
+EDGE_CASES = [
+    # (dtype, B, Hq, Hkv, Tq, Tk, q_offset, d, dv, causal, rope_base)
+    ("bf16", 1, 2, 1, 300, 1, 0, 128, 128, False, 10000.0),       # one key, many queries
+    ("bf16", 1, 2, 2, 1, 1, 0, 64, 128, True, 10000.0),           # one query, one key
+    ("bf16", 1, 4, 1, 128, 640, 49024, 128, 128, True, 10000.0),  # last row at position 49151
+    ("f32", 1, 2, 1, 1, 1, 0, 16, 16, True, 10000.0),
+    ("f32", 1, 2, 2, 40, 1, 7, 32, 64, True, 10000.0),            # one key seen by every row
+]
+
+
+@pytest.mark.parametrize("dtype,B,hq,hkv,Tq,Tk,off,d,dv,causal,base", EDGE_CASES)
+def test_bwd_ext_edges(dtype, B, hq, hkv, Tq, Tk, off, d, dv, causal, base):
+    """Degenerate shapes and the largest RoPE position: a single key (every visible
+    row puts all its weight on it, so dq is zero up to rounding), a single query and
+    key, and queries at positions 49024..49151 (all 640 keys visible to each)."""
+    q, k, v, do = _inputs(B, hq, hkv, Tq, Tk, d, dv, dtype, seed=Tq + Tk + d + dv + 11)
+    if Tk > 1:
+        _check(q, k, v, do, off, causal, base, "split_half", dtype, f"edge {dtype}")
+        return
+    # one key: dS = P (dP - D) with P = 1 and dP = D exactly, so the exact dq and dk are
+    # zero and only rounding of the two dot products remains (a relative L2 against zero
+    # means nothing): max-abs for dq and dk, the full bounds for dv
+    dq, dk, dv_ = _run(q, k, v, do, off, causal, base, "split_half")
+    rq, rk, rv = OA.attention_backward(q, k, v, do, causal=causal, rope_base=base,
+                                       operand_dtype=dtype, q_offset=off)
+    assert float(abs(rq).max()) < 1e-12 and float(abs(rk).max()) < 1e-12
+    atol = 1e-5 if dtype == "f32" else 2e-2
+    assert float(dq.abs().max()) <= atol and float(dk.abs().max()) <= atol
+    assert_grad_close(to_np(dv_), rv, f"edge {dtype} dv", **({} if dtype == "bf16" else F32_TOL))
+
+
 FP32_CASES = [
     # (B, Hq, Hkv, Tq, Tk, q_offset, d, dv, causal, rope_base, layout)
     (2, 4, 1, 16, 64, 48, 16, 16, True, 10000.0, "split_half"),
