@@ -267,11 +267,14 @@ size_t csattn_decode_workspace_size(int B, int Hq, int Lmax, int d, int num_spli
 
 /*
  * KV-cache decode: one new query per sequence.
- *   q        [B, Hq, 1, d]     bf16, already rotated to position seq_lens[b]-1
- *   k_cache  [B, Hkv, Lmax, d] bf16, keys already rotated (RoPE) at their positions
- *   v_cache  [B, Hkv, Lmax, d] bf16
+ *   q        [B, Hq, 1, d]     already rotated to position seq_lens[b]-1
+ *   k_cache  [B, Hkv, Lmax, d] keys already rotated (RoPE) at their positions
+ *   v_cache  [B, Hkv, Lmax, d]
  *   seq_lens device int32 [B]: valid rows of sequence b, 1 <= seq_lens[b] <= max_seq_len
- *   out      [B, Hq, 1, d]     bf16
+ *   out      [B, Hq, 1, d]
+ *   dtype    CSATTN_BF16 (d in {64, 128}, Hq / Hkv <= 16; tensor-core kernels) or
+ *            CSATTN_F32 (d in {16, 32, 64, 128}; SIMT kernels in fp32 throughout, for
+ *            callers that want the decode close to float64), all tensors that dtype
  *   scale    > 0: logit scale; <= 0: 1/sqrt(d)
  *   max_seq_len  host-side upper bound of seq_lens (<= Lmax); sizes the grid.
  *   num_splits   0: automatic; > 0: split every sequence's keys into that many
@@ -279,8 +282,8 @@ size_t csattn_decode_workspace_size(int B, int Hq, int Lmax, int d, int num_spli
  *   workspace    >= csattn_decode_workspace_size(B, Hq, Lmax, d, num_splits) bytes.
  * Rows at or beyond seq_lens[b] are never read.  A seq_lens[b] outside
  * [1, max_seq_len] raises CSATTN_ERR_DEVICE_ARG in the status word (the
- * sequence's output is then zero or partial).  Requirements: Hq % Hkv == 0,
- * Hq / Hkv <= 16, d in {64, 128}.
+ * sequence's output is then zero or partial).  Requirements: Hq % Hkv == 0 and
+ * the dtype's d (and group size) above; the other decode calls are bf16 only.
  */
 int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int Lmax,

@@ -136,7 +136,10 @@ def test_fwd_ext_rejects_invalid_arguments(lib, kw, status):
     (dict(seq=None), -1),
     (dict(B=0), -1),
     (dict(Hq=6, Hkv=4), -1),
-    (dict(dtype=0), -2),
+    (dict(dtype=0, d=48), -2),
+    (dict(dtype=0, d=256), -2),
+    (dict(dtype=0, Hq=6, Hkv=4), -1),
+    (dict(dtype=0, splits=2, ws=FAKE, ws_bytes=16), -5),
     (dict(dtype=9), -1),
     (dict(d=96), -2),
     (dict(Hq=34, Hkv=2), -2),

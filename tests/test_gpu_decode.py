@@ -8,7 +8,7 @@ import torch
 import attn_workloads as W
 import transformer_causal_self_gb300 as csattn
 from oracle import attn as OA
-from tests.gpu_helpers import assert_bf16_close, dev, to_np
+from tests.gpu_helpers import assert_bf16_close, assert_f32_close, dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -146,3 +146,41 @@ def test_decode_ext_equal_widths_is_decode():
     b = csattn.attn_decode_ext(q, kc, vc, sl, scale=w.scale, max_seq_len=2048)
     csattn.check_status()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 2, 128), (4, 4, 64), (12, 3, 32), (2, 1, 16),
+                                      (40, 2, 64)])
+def test_decode_fp32_parity(Hq, Hkv, d):
+    """fp32 decode (SIMT, fp32 throughout) against the oracle at the fp32 parity bound
+    (max-abs 1e-5), ragged lengths with NaN past each sequence's rows, several split
+    counts; the group of 20 query heads is past the bf16 kernels' limit of 16."""
+    lens = [1, 31, 32, 33, 300, 777, 1000]
+    w = W.DecodeWorkload("dec32", B=len(lens), Hq=Hq, Hkv=Hkv, d=d, Lmax=1000, Lmin=1,
+                         dtype="f32", scale=1.0 / math.sqrt(d), seed=Hq + d)
+    q, kc, vc, sl = W.make_decode_inputs(w, seq_lens=lens)
+    assert q.dtype == torch.float32
+    ref = OA.decode(q, kc, vc, sl.numpy(), scale=w.scale)
+    for splits in (0, 1, 3, 16):
+        out = _decode(q, kc, vc, sl, scale=w.scale, max_seq_len=1000, num_splits=splits)
+        assert out.dtype == torch.float32
+        assert_f32_close(to_np(out), ref, f"fp32 decode splits={splits}")
+
+
+def test_decode_fp32_rows_equal_prefill_rows():
+    """The incremental decode reproduces the one-shot forward ("The Transformer
+    architecture", "Hands-on": in fp32 the two agree to a few 1e-7): decoding query t
+    over keys 0..t gives row t of the fp32 causal prefill on the same K and V."""
+    B, Hq, Hkv, T, d = 2, 8, 2, 300, 64
+    g = torch.Generator()
+    g.manual_seed(123)
+    q = torch.randn(B, Hq, T, d, generator=g)
+    k = torch.randn(B, Hkv, T, d, generator=g)
+    v = torch.randn(B, Hkv, T, d, generator=g)
+    pre = csattn.attn_fwd(q.to(dev()), k.to(dev()), v.to(dev()), causal=True, rope_base=0.0)
+    csattn.check_status()
+    worst = 0.0
+    for t in (0, 1, 127, 128, 200, T - 1):
+        lens = torch.full((B,), t + 1, dtype=torch.int32)
+        out = _decode(q[:, :, t:t + 1].contiguous(), k, v, lens, max_seq_len=T)
+        worst = max(worst, float((out[:, :, 0] - pre[:, :, t]).abs().max()))
+    assert worst <= 1e-6, worst

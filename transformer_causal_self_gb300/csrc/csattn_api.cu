@@ -498,7 +498,8 @@ namespace {
 // placeholder when the queries are produced on the device).
 int decode_check(const char* fn, const void* q, const void* k_cache, const void* v_cache,
                  const int32_t* seq_lens, const void* out, int B, int Hq, int Hkv, int Lmax, int d,
-                 int dtype, float scale, int max_seq_len, int num_splits) {
+                 int dtype, float scale, int max_seq_len, int num_splits,
+                 bool allow_f32 = false) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
       out == nullptr)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: null pointer argument", fn);
@@ -508,12 +509,17 @@ int decode_check(const char* fn, const void* q, const void* k_cache, const void*
   if (Hq % Hkv != 0)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: Hq=%d is not a multiple of Hkv=%d", fn, Hq,
                 Hkv);
-  if (dtype != CSATTN_BF16)
+  if (dtype != CSATTN_BF16 && !(allow_f32 && dtype == CSATTN_F32))
     return fail(dtype == CSATTN_F32 ? CSATTN_ERR_UNSUPPORTED : CSATTN_ERR_INVALID_ARG,
                 "%s: only bf16 is implemented (dtype %d)", fn, dtype);
-  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d", fn, d);
-  if (Hq / Hkv > 16)
-    return fail(CSATTN_ERR_UNSUPPORTED, "%s: group size %d > 16", fn, Hq / Hkv);
+  if (dtype == CSATTN_F32) {
+    if (d != 16 && d != 32 && d != 64 && d != 128)
+      return fail(CSATTN_ERR_UNSUPPORTED, "%s: fp32 d=%d not in {16,32,64,128}", fn, d);
+  } else {
+    if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: d=%d", fn, d);
+    if (Hq / Hkv > 16)
+      return fail(CSATTN_ERR_UNSUPPORTED, "%s: group size %d > 16", fn, Hq / Hkv);
+  }
   if (max_seq_len < 1 || max_seq_len > Lmax)
     return fail(CSATTN_ERR_INVALID_ARG, "%s: max_seq_len=%d not in [1, Lmax=%d]", fn,
                 max_seq_len, Lmax);
@@ -551,12 +557,14 @@ int decode_impl(const char* fn, const void* q, const void* k_cache, const void* 
                 const int32_t* seq_lens, int len_add, void* out, int B, int Hq, int Hkv, int Lmax,
                 int d, int dtype, float scale, int max_seq_len, int num_splits, void* workspace,
                 size_t workspace_bytes, void* stream, const int32_t* block_table = nullptr,
-                int page_size = 0, int num_pages = 0, int max_pages = 0, int dv = 0) {
+                int page_size = 0, int num_pages = 0, int max_pages = 0, int dv = 0,
+                bool allow_f32 = false) {
   int rc = decode_check(fn, q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, Lmax, d, dtype, scale,
-                        max_seq_len, num_splits);
+                        max_seq_len, num_splits, allow_f32);
   if (rc != CSATTN_OK) return rc;
   if (dv <= 0) dv = d;
-  if (dv != 64 && dv != 128) return fail(CSATTN_ERR_UNSUPPORTED, "%s: dv=%d", fn, dv);
+  if (dtype == CSATTN_BF16 ? (dv != 64 && dv != 128) : dv != d)
+    return fail(CSATTN_ERR_UNSUPPORTED, "%s: dv=%d", fn, dv);
   DecodeArgs a{};
   a.q = q;
   a.k_cache = k_cache;
@@ -603,6 +611,11 @@ int decode_impl(const char* fn, const void* q, const void* k_cache, const void* 
   }
   a.part_o = static_cast<float*>(workspace);
   a.part_ml = a.part_o + static_cast<size_t>(B) * Hq * a.n_splits * dv;
+  if (dtype == CSATTN_F32) {
+    cudaError_t e = launch_decode_f32(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "attn_decode: fp32 kernel launch");
+    return CSATTN_OK;
+  }
   if (tensor_map_encoder() == nullptr)
     return fail(CSATTN_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", fn);
   cudaError_t e = launch_decode_bf16(a, static_cast<cudaStream_t>(stream));
@@ -619,7 +632,8 @@ int csattn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                        int d, int dtype, float scale, int max_seq_len, int num_splits,
                        void* workspace, size_t workspace_bytes, void* stream) {
   return decode_impl("attn_decode", q, k_cache, v_cache, seq_lens, 0, out, B, Hq, Hkv, Lmax, d,
-                     dtype, scale, max_seq_len, num_splits, workspace, workspace_bytes, stream);
+                     dtype, scale, max_seq_len, num_splits, workspace, workspace_bytes, stream,
+                     nullptr, 0, 0, 0, 0, true);
 }
 
 int csattn_attn_decode_ext(const void* q, const void* k_cache, const void* v_cache,

@@ -113,6 +113,9 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream);
+// fp32 decode on the SIMT cores (contiguous cache, d in {16, 32, 64, 128}, dv = d);
+// the partials in the same layout, m in natural-log units.
+cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t stream);
 
 // One decode step's cache append: for sequence b at position p = cache_lens[b],
 // q_rot[b,h] = RoPE_p(q_new[b,h]) for every query head, k_cache[b,g,p] =
@@ -135,7 +138,7 @@ void set_last_error(const char* msg);
 int attn_fwd_check(const char* fn, int B, int Hq, int Hkv, int T, int d, int dtype, int causal,
                    float rope_base, int rope_layout, float scale);
 
-// The host-side argument checks of csattn_attn_decode (all but the pointers).
+// The host-side argument checks of the bf16 decodes (all but the pointers).
 int attn_decode_check(const char* fn, int B, int Hq, int Hkv, int Lmax, int d, int dtype,
                       float scale, int max_seq_len, int num_splits);
 
