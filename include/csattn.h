@@ -251,8 +251,9 @@ int csattn_attn_bwd_ext(const void* q, const void* k, const void* v, const void*
  * RoPE of x [B, H, T, d] into x_rot (same shape; must not overlap x), at
  * positions 0..T-1 with theta_p = rope_base^(-2p/d), rounded to the input
  * dtype.  This is the rotation csattn_attn_fwd applies to its keys, exposed to
- * build a rotated KV cache for csattn_attn_decode.  dtype must be CSATTN_BF16;
- * d in {64, 128}; rope_base > 0; T <= 49152.
+ * build a rotated KV cache for csattn_attn_decode.  bf16 with d in {64, 128}, or
+ * fp32 with d in {16, 32, 64, 128} (fp32 arithmetic, the accurate sine/cosine, as
+ * the fp32 prefill rotates); rope_base > 0; T <= 49152.
  */
 int csattn_rope_rotate(const void* x, void* x_rot, int B, int H, int T, int d, int dtype,
                        float rope_base, int rope_layout, void* stream);

@@ -512,6 +512,31 @@ def test_decode_ext_rejects_invalid_arguments(lib, kw, status):
     assert b"attn_decode_ext" in lib.csattn_last_error()
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), -1),
+    (dict(T=0), -1),
+    (dict(dtype=7), -1),
+    (dict(d=32), -2),
+    (dict(dtype=0, d=48), -2),
+    (dict(dtype=0, d=256), -2),
+    (dict(base=0.0), -1),
+    (dict(base=float("nan")), -1),
+    (dict(layout=3), -1),
+    (dict(T=50000), -2),
+    (dict(xr=FAKE + 8), -1),
+    (dict(xr=FAKE + 64), -1),               # overlaps x
+    (dict(dtype=0, d=16, xr=FAKE + 256), -1),  # fp32 rows are 4-byte elements: overlap
+])
+def test_rope_rotate_rejects_invalid_arguments(lib, kw, status):
+    a = dict(x=FAKE, xr=FAKE + (1 << 24), B=1, H=2, T=64, d=128, dtype=1, base=10000.0,
+             layout=0)
+    a.update(kw)
+    rc = lib.csattn_rope_rotate(a["x"], a["xr"], a["B"], a["H"], a["T"], a["d"], a["dtype"],
+                                a["base"], a["layout"], None)
+    assert rc == status, lib.csattn_last_error()
+    assert b"rope_rotate" in lib.csattn_last_error()
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.csattn_selftest_bounded_wait(0, None) == -1
     assert lib.csattn_selftest_bounded_wait(2000000, None) == -1

@@ -184,3 +184,29 @@ def test_decode_fp32_rows_equal_prefill_rows():
         out = _decode(q[:, :, t:t + 1].contiguous(), k, v, lens, max_seq_len=T)
         worst = max(worst, float((out[:, :, 0] - pre[:, :, t]).abs().max()))
     assert worst <= 1e-6, worst
+
+
+@pytest.mark.parametrize("layout", ["split_half", "adjacent"])
+def test_decode_fp32_generation_with_rope(layout):
+    """An fp32 generation loop through the library alone: the RoPE pass in fp32 builds the
+    rotated queries and key cache (checked against the oracle's rotation), and decoding
+    query t over keys 0..t reproduces row t of the fp32 prefill with RoPE."""
+    B, Hq, Hkv, T, d, base = 2, 4, 2, 200, 32, 10000.0
+    g = torch.Generator()
+    g.manual_seed(77)
+    q = torch.randn(B, Hq, T, d, generator=g)
+    k = torch.randn(B, Hkv, T, d, generator=g)
+    v = torch.randn(B, Hkv, T, d, generator=g)
+    qd, kd, vd = q.to(dev()), k.to(dev()), v.to(dev())
+    pre = csattn.attn_fwd(qd, kd, vd, causal=True, rope_base=base, rope_layout=layout)
+    q_rot = csattn.rope_rotate(qd, rope_base=base, rope_layout=layout)
+    k_rot = csattn.rope_rotate(kd, rope_base=base, rope_layout=layout)
+    csattn.check_status()
+    ref_k = OA.rope_rotate(k.double().numpy(), np.arange(T), base, layout)
+    assert np.max(np.abs(to_np(k_rot) - ref_k)) < 2e-6
+    worst = 0.0
+    for t in (0, 63, 64, 150, T - 1):
+        lens = torch.full((B,), t + 1, dtype=torch.int32)
+        out = _decode(q_rot[:, :, t:t + 1].contiguous(), k_rot, vd, lens, max_seq_len=T)
+        worst = max(worst, float((out[:, :, 0] - pre[:, :, t]).abs().max()))
+    assert worst <= 2e-6, worst

@@ -6,7 +6,8 @@
 // q_off..q_off+Tq-1, Tk keys at 0..Tk-1.  A row is served by TPR = max(d, dv)/16
 // threads, each holding d/TPR channels of the q/k side and dv/TPR of the v/dout side.
 //
-//   rope_f32_kernel     x_rot = R x at positions pos0 + t (accurate sine/cosine)
+//   rope_f32_kernel     x_rot = R x at positions pos0 + t (accurate sine/cosine); also
+//                       csattn_rope_rotate's fp32 path
 //   rowdot_f32_kernel   D
 //   bwd_dq_f32_kernel   one CTA per (ROWS query rows, query head, batch); K and V
 //                       tiles staged in shared memory; dq rotated back at the end
@@ -304,6 +305,14 @@ cudaError_t launch_f32_dv(const BwdF32Params& p, int B, int dv, cudaStream_t str
 }
 
 }  // namespace
+
+cudaError_t launch_rope_rotate_f32(const void* x, void* x_rot, int B, int H, int T, int d,
+                                   int rope, const RopeTable& theta, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(B) * H * T;
+  rope_f32_kernel<<<static_cast<unsigned>((rows * (d / 2) + 255) / 256), 256, 0, stream>>>(
+      static_cast<const float*>(x), static_cast<float*>(x_rot), rows, T, d, rope, theta, 0);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_f32(const BwdArgs& a, void* q_rot, void* k_rot, cudaStream_t stream) {
   const long long qrows = static_cast<long long>(a.B) * a.Hq * a.Tq;

@@ -457,10 +457,10 @@ int csattn_rope_rotate(const void* x, void* x_rot, int B, int H, int T, int d, i
     return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: null pointer argument");
   if (B < 1 || H < 1 || T < 1)
     return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: B=%d H=%d T=%d must be >= 1", B, H, T);
-  if (dtype != CSATTN_BF16)
-    return fail(dtype == CSATTN_F32 ? CSATTN_ERR_UNSUPPORTED : CSATTN_ERR_INVALID_ARG,
-                "rope_rotate: only bf16 is implemented (dtype %d)", dtype);
-  if (d != 64 && d != 128) return fail(CSATTN_ERR_UNSUPPORTED, "rope_rotate: d=%d", d);
+  if (dtype != CSATTN_BF16 && dtype != CSATTN_F32)
+    return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: unknown dtype %d", dtype);
+  if (dtype == CSATTN_BF16 ? (d != 64 && d != 128) : (d != 16 && d != 32 && d != 64 && d != 128))
+    return fail(CSATTN_ERR_UNSUPPORTED, "rope_rotate: d=%d", d);
   if (!(rope_base > 0.f) || !std::isfinite(rope_base))
     return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: rope_base must be finite and > 0");
   if (rope_layout != CSATTN_ROPE_SPLIT_HALF && rope_layout != CSATTN_ROPE_ADJACENT)
@@ -469,15 +469,19 @@ int csattn_rope_rotate(const void* x, void* x_rot, int B, int H, int T, int d, i
     return fail(CSATTN_ERR_UNSUPPORTED, "rope_rotate: T <= %d, got %d", kMaxRopePositions, T);
   if (!aligned16(x) || !aligned16(x_rot))
     return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: x, x_rot must be 16-byte aligned");
-  const size_t bytes = static_cast<size_t>(B) * H * T * d * 2;
+  const size_t bytes = static_cast<size_t>(B) * H * T * d * (dtype == CSATTN_F32 ? 4 : 2);
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(x), b0 = reinterpret_cast<uintptr_t>(x_rot);
   if (a0 < b0 + bytes && b0 < a0 + bytes)
     return fail(CSATTN_ERR_INVALID_ARG, "rope_rotate: x and x_rot overlap");
   RopeTable th;
   rope_table(&th, d, static_cast<double>(rope_base));
-  cudaError_t e = launch_rope_rotate_bf16(x, x_rot, B, H, T, d,
-                                          rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2, th,
-                                          static_cast<cudaStream_t>(stream));
+  const int layout = rope_layout == CSATTN_ROPE_SPLIT_HALF ? 1 : 2;
+  cudaError_t e =
+      dtype == CSATTN_F32
+          ? launch_rope_rotate_f32(x, x_rot, B, H, T, d, layout, th,
+                                   static_cast<cudaStream_t>(stream))
+          : launch_rope_rotate_bf16(x, x_rot, B, H, T, d, layout, th,
+                                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "rope_rotate: kernel launch");
   return CSATTN_OK;
 }

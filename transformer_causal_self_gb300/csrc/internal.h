@@ -46,6 +46,9 @@ cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_rope_rotate_bf16(const void* x, void* x_rot, int B, int H, int T, int d,
                                     int rope, const RopeTable& theta, cudaStream_t stream,
                                     int pos0 = 0);
+// fp32: the same rotation in fp32 with the accurate sine/cosine (bwd_f32.cu).
+cudaError_t launch_rope_rotate_f32(const void* x, void* x_rot, int B, int H, int T, int d,
+                                   int rope, const RopeTable& theta, cudaStream_t stream);
 
 // bf16 tcgen05 prefill; `k_eff` is k itself or its rotated copy.  q, k have d
 // and v, out dv channels (each 64 or 128): dv = 64 runs the kernel in
