@@ -18,7 +18,7 @@
 // is written back into TMEM over the dP^T columns and feeds dK from there.
 // Warps 0-3 handle queries 0-63 of the tile, warps 4-7 queries 64-127 (thread =
 // key row = TMEM lane); warp 8 loads (TMA for Qr and dO, plain loads for lse and
-// D); warp 9 allocates TMEM and issues the MMAs in the order S^T(it+1), dV(it),
+// D); warp 9 allocates TMEM and issues the MMAs in the order dV(it), S^T(it+1),
 // dK(it), dP^T(it+1): dK(it) frees the dS^T columns for dP^T(it+1).
 //
 // Every wait is bounded (2 s) and sets the status word's timeout bit; no named
@@ -231,8 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(dp_full);
       };
-      // Order per tile: S^T(it+1) as soon as the softmax warps have read S^T(it), so it
-      // overlaps their work on tile it; dK(it) frees the dS^T columns for dP^T(it+1).
+      // Order per tile: dV(it), S^T(it+1), dK(it), dP^T(it+1).  S^T(it+1) runs two
+      // products ahead of dV(it+1), which needs the softmax warps' P^T(it+1); and it
+      // comes after dV(it) so that the Q/dO stage of tile it+1, freed when dK(it-1)
+      // completes, has the time of dP^T(it) and dV(it) to land before the MMA thread
+      // waits for it.  dK(it) frees the dS^T columns for dP^T(it+1).
       if (n_it > 0 && wait(&q_full[0], 0)) {
         issue_st(0);
         issue_dpt(0);
@@ -241,11 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < n_it && ok; ++it) {
         const uint32_t q_s = q_tile(it), o_s = o_tile(it);
         const bool next = it + 1 < n_it;
-        if (next) {
-          if (!wait(s_free, it & 1)) break;
-          if (!wait(&q_full[(it + 1) % NSQ], ((it + 1) / NSQ) & 1)) break;
-          issue_st(it + 1);
-        }
         if (!wait(p_full, it & 1)) break;
         // dV += P^T dO: A = P^T (shared memory, K-major), B = dO (rows = queries,
         // channels contiguous)
@@ -257,6 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                   (it > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(dv_done);
+        if (next) {
+          if (!wait(s_free, it & 1)) break;
+          if (!wait(&q_full[(it + 1) % NSQ], ((it + 1) / NSQ) & 1)) break;
+          issue_st(it + 1);
+        }
         if (!wait(ds_full, it & 1)) break;
         // dK += dS^T Qr
 #pragma unroll
