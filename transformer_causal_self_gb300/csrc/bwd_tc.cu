@@ -182,10 +182,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float* vec = sVec + st * 2 * BQ;
       const size_t rb = static_cast<size_t>(zq) * p.Tq;
-      for (int e = lane; e < BQ; e += 32) {
-        const int q = q0 + e;
-        vec[e] = q < p.Tq ? p.lse[rb + q] * kLog2e : 0.f;
-        vec[BQ + e] = q < p.Tq ? p.dvec[rb + q] : 0.f;
+      // all loads before the shared-memory stores, so that their latencies overlap
+      float lv[BQ / 32], dvl[BQ / 32];
+#pragma unroll
+      for (int i = 0; i < BQ / 32; ++i) {
+        const int q = q0 + lane + 32 * i;
+        lv[i] = q < p.Tq ? __ldg(p.lse + rb + q) : 0.f;
+        dvl[i] = q < p.Tq ? __ldg(p.dvec + rb + q) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < BQ / 32; ++i) {
+        vec[lane + 32 * i] = lv[i] * kLog2e;
+        vec[BQ + lane + 32 * i] = dvl[i];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&vec_full[st]);
