@@ -462,15 +462,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   dQ += dS Kr_j                   (TS, B = Kr_j with channels contiguous)
 // into one of two accumulators ([256,384) for even items, [384,512) for odd ones),
 // so the next item's products start while warps 12-15 drain the finished dQ
-// (R^T, scale, store).  K_j and V_j arrive by TMA through a two-stage ring that
-// runs across items; S(g+1) is issued as soon as the softmax warps have read S(g)
-// (g counts key tiles over all items of the CTA), dP(g+1) follows dQ(g).
-constexpr int NSKV = 2;
+// (R^T, scale, store).  K_j and V_j arrive by TMA through rings that run across
+// items, three stages for K (read by S and dQ) and two for V (read by dP only), so
+// the load into a freed stage has about a tile's products of time to land; S(g+1) is
+// issued as soon as the softmax warps have read S(g) (g counts key tiles over all
+// items of the CTA), dP(g+1) follows dQ(g).
+constexpr int NSK = 3;
+constexpr int NSV = 2;
 constexpr int kThreadsQ = 512;
 constexpr int kWarpEpiQ = 12;       // warps 12-15: dQ epilogue (TMEM lane quadrants 0-3)
 constexpr int kRegsSoftmaxQ = 152;  // 2*128*152 + 128*96 + 128*112 = 65536 = 512 * 128
 constexpr int kRegsCtlQ = 96;
 constexpr int kRegsEpiQ = 112;
+
+// Shared memory of the dQ kernel: Q and dO of the item, NSK K and NSV V stages.
+template <int D, int DV>
+struct BwdQSmem {
+  static constexpr int DATA = (1 + NSK) * BwdCfg<D, DV>::TILE_QK + (1 + NSV) * BwdCfg<D, DV>::TILE_VO;
+  static_assert(DATA + 256 <= 227 * 1024, "dQ kernel shared memory");
+};
 
 struct QParams {
   const float* lse;   // [B, Hq, Tq]
@@ -523,25 +533,28 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do) {
   using C = BwdCfg<D, DV>;
-  constexpr int TQK = C::TILE_QK, TVO = C::TILE_VO, STAGE = TQK + TVO;
-  constexpr int Q_SMEM_DATA = (1 + NSKV) * STAGE;
+  constexpr int TQK = C::TILE_QK, TVO = C::TILE_VO;
+  constexpr int Q_SMEM_DATA = BwdQSmem<D, DV>::DATA;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sQ = smem;
   uint8_t* sO = smem + TQK;
-  uint8_t* sKV = smem + STAGE;  // [NSKV] x (K tile, V tile)
+  uint8_t* sK = sO + TVO;        // [NSK] K tiles
+  uint8_t* sV = sK + NSK * TQK;  // [NSV] V tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Q_SMEM_DATA);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;   // the item's last S and dP completed
-  uint64_t* kv_full = bars + 2;   // [NSKV]
-  uint64_t* kv_empty = bars + 4;  // [NSKV]
-  uint64_t* s_full = bars + 6;
-  uint64_t* s_free = bars + 7;    // 8 warps: S(g) read
-  uint64_t* dp_full = bars + 8;
-  uint64_t* ds_full = bars + 9;   // 8 warps
-  uint64_t* acc_full = bars + 10;   // [2] dQ accumulator complete
-  uint64_t* acc_empty = bars + 12;  // [2] 4 epilogue warps have read it
-  uint64_t* teardown = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* k_full = bars + 2;    // [NSK]
+  uint64_t* k_empty = bars + 5;   // [NSK]: S and dQ of the stage's tile completed
+  uint64_t* v_full = bars + 8;    // [NSV]
+  uint64_t* v_empty = bars + 10;  // [NSV]: dP of the stage's tile completed
+  uint64_t* s_full = bars + 12;
+  uint64_t* s_free = bars + 13;   // 8 warps: S(g) read
+  uint64_t* dp_full = bars + 14;
+  uint64_t* ds_full = bars + 15;  // 8 warps
+  uint64_t* acc_full = bars + 16;   // [2] dQ accumulator complete
+  uint64_t* acc_empty = bars + 18;  // [2] 4 epilogue warps have read it
+  uint64_t* teardown = bars + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -552,9 +565,13 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < NSKV; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < NSK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, 8);
@@ -583,39 +600,46 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       bool ok = true;
-      int g = 0, issued = 0, items = 0;
+      int g = 0, k_issued = 0, v_issued = 0, items = 0;
       for (int i = 0; ok; ++i) {
         const int u = q_item_index(i);
         if (u >= p.n_items) break;
         const QItem it = q_item(p, u);
         const int zq = it.b * p.Hq + it.h, zk = it.b * p.Hkv + it.h / (p.Hq / p.Hkv);
         if (i > 0 && !mbar_wait(q_empty, (i - 1) & 1, abort_flag, p.status, kWaitNs)) break;
-        mbar_arrive_expect_tx(q_full, STAGE);
+        mbar_arrive_expect_tx(q_full, TQK + TVO);
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_3d(sQ + kb * BLOCK, &tm_q, q_full, kb * 64, it.qt * BQ, zq);
         for (int kb = 0; kb < DV / 64; ++kb)
           tma_load_3d(sO + kb * BLOCK, &tm_do, q_full, kb * 64, it.qt * BQ, zq);
         ++items;
         for (int j = 0; j < it.n_it; ++j, ++g) {
-          const int st = g % NSKV, use = g / NSKV;
-          if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, abort_flag, p.status, kWaitNs)) {
+          const int sk = g % NSK, uk = g / NSK;
+          if (uk > 0 && !mbar_wait(&k_empty[sk], (uk - 1) & 1, abort_flag, p.status, kWaitNs)) {
             ok = false;
             break;
           }
-          uint8_t* dst = sKV + st * STAGE;
-          mbar_arrive_expect_tx(&kv_full[st], STAGE);
+          mbar_arrive_expect_tx(&k_full[sk], TQK);
           for (int kb = 0; kb < D / 64; ++kb)
-            tma_load_3d(dst + kb * BLOCK, &tm_k, &kv_full[st], kb * 64, j * BK, zk);
+            tma_load_3d(sK + sk * TQK + kb * BLOCK, &tm_k, &k_full[sk], kb * 64, j * BK, zk);
+          ++k_issued;
+          const int sv = g % NSV, uv = g / NSV;
+          if (uv > 0 && !mbar_wait(&v_empty[sv], (uv - 1) & 1, abort_flag, p.status, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[sv], TVO);
           for (int kb = 0; kb < DV / 64; ++kb)
-            tma_load_3d(dst + TQK + kb * BLOCK, &tm_v, &kv_full[st], kb * 64, j * BK, zk);
-          ++issued;
+            tma_load_3d(sV + sv * TVO + kb * BLOCK, &tm_v, &v_full[sv], kb * 64, j * BK, zk);
+          ++v_issued;
         }
       }
       if (*abort_flag) {
         if (items > 0) mbar_wait(q_full, (items - 1) & 1, nullptr, p.status, kDrainNs);
-        const int first = issued > NSKV ? issued - NSKV : 0;
-        for (int t = first; t < issued; ++t)
-          mbar_wait(&kv_full[t % NSKV], (t / NSKV) & 1, nullptr, p.status, kDrainNs);
+        for (int t = k_issued > NSK ? k_issued - NSK : 0; t < k_issued; ++t)
+          mbar_wait(&k_full[t % NSK], (t / NSK) & 1, nullptr, p.status, kDrainNs);
+        for (int t = v_issued > NSV ? v_issued - NSV : 0; t < v_issued; ++t)
+          mbar_wait(&v_full[t % NSV], (t / NSV) & 1, nullptr, p.status, kDrainNs);
       }
     }
    } else if (warp == kWarpMma) {
@@ -628,7 +652,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         return ok;
       };
       const uint32_t q_s = smem_u32(sQ), o_s = smem_u32(sO);
-      auto k_tile = [&](int g) { return smem_u32(sKV + (g % NSKV) * STAGE); };
+      auto k_tile = [&](int g) { return smem_u32(sK + (g % NSK) * TQK); };
+      auto v_tile = [&](int g) { return smem_u32(sV + (g % NSV) * TVO); };
       auto issue_s = [&](int g) {  // S = Qr Kr^T
         const uint32_t k_s = k_tile(g);
 #pragma unroll
@@ -639,8 +664,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         }
         tc_commit(s_full);
       };
-      auto issue_dp = [&](int g) {  // dP = dO V^T
-        const uint32_t v_s = k_tile(g) + TQK;
+      auto issue_dp = [&](int g) {  // dP = dO V^T, then V's stage is released
+        const uint32_t v_s = v_tile(g);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * BLOCK + (kk & 3) * 32);
@@ -648,6 +673,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                   smem_desc_sw128(v_s + off, 16, 1024), IDESC_SS, kk > 0 ? 1u : 0u);
         }
         tc_commit(dp_full);
+        tc_commit(&v_empty[g % NSV]);
       };
       int g = 0;
       for (int i = 0; ok; ++i) {
@@ -660,15 +686,16 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         // (s_free of the previous tile), the dP columns consumed (dQ issued before)
         if (!wait(q_full, i & 1)) break;
         if (g > 0 && !wait(s_free, (g - 1) & 1)) break;
-        if (!wait(&kv_full[g % NSKV], (g / NSKV) & 1)) break;
+        if (!wait(&k_full[g % NSK], (g / NSK) & 1)) break;
         issue_s(g);
+        if (!wait(&v_full[g % NSV], (g / NSV) & 1)) break;
         issue_dp(g);
         if (it.n_it == 1) tc_commit(q_empty);
         for (int j = 0; j < it.n_it && ok; ++j, ++g) {
           const bool next = j + 1 < it.n_it;
           if (next) {
             if (!wait(s_free, g & 1)) break;
-            if (!wait(&kv_full[(g + 1) % NSKV], ((g + 1) / NSKV) & 1)) break;
+            if (!wait(&k_full[(g + 1) % NSK], ((g + 1) / NSK) & 1)) break;
             issue_s(g + 1);
           }
           if (!wait(ds_full, g & 1)) break;
@@ -680,8 +707,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
           for (int kk = 0; kk < BK / 16; ++kk)
             umma_ts(t_acc, tmem + 128u + packed_col(kk), smem_desc_sw128(k_s + 2048u * kk, BLOCK, 1024),
                     C::IDESC_DK, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&kv_empty[g % NSKV]);
+          tc_commit(&k_empty[g % NSK]);
           if (next) {
+            if (!wait(&v_full[(g + 1) % NSV], ((g + 1) / NSV) & 1)) break;
             issue_dp(g + 1);
             if (j + 2 == it.n_it) tc_commit(q_empty);  // S and dP of the last key tile issued
           } else {
@@ -899,7 +927,7 @@ namespace csattn {
 
 template <int D, int DV>
 cudaError_t launch_q_d(const BwdArgs& a, cudaStream_t stream) {
-  constexpr int smem_bytes = (1 + NSKV) * (BwdCfg<D, DV>::TILE_QK + BwdCfg<D, DV>::TILE_VO) + 256;
+  constexpr int smem_bytes = BwdQSmem<D, DV>::DATA + 256;
   QParams p{};
   p.lse = a.lse;
   p.dvec = a.dvec;
